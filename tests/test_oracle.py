@@ -1,0 +1,262 @@
+"""Pins for the W12 oracle: checks against facts that do not come from the oracle.
+
+- lossless / bit-exact ("StargazerX0/SpecPilot" §What it is; "SpecPilot"
+  §Differentiation): every BF16 bit pattern survives encode -> decode;
+- a hand-worked 2x2 blob fixes the byte layout;
+- the exponent table is a top-15 set and the escapes are exactly the histogram
+  mass outside it;
+- Gaussian weights: bits/weight close to 12 ("SpecPilot: an agent doubled ..."
+  §The mechanisms it found) and an escape rate matching the normal CDF;
+- the fp64 GEMM against numpy's float64 matmul and exact special cases.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from lossless_bit_weight_encode_gb300 import workloads as wl
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+FACTS = json.load(open(os.path.join(HERE, "golden", "pages_facts.json")))
+
+
+def _hdr(blob, off, n):
+    return int.from_bytes(bytes(blob[off:off + n]), "little")
+
+
+def _seg_headers(blob):
+    off, nbytes = _hdr(blob, 0x58, 8), _hdr(blob, 0x60, 8)
+    return np.asarray(blob[off:off + nbytes]).reshape(-1, 32)
+
+
+def _padded(w):
+    n, k = w.shape
+    npad, kpad = -(-n // 128) * 128, -(-k // 32) * 32
+    out = np.zeros((npad, kpad), dtype=np.uint16)
+    out[:n, :k] = w
+    return out
+
+
+@pytest.mark.parametrize("shuffle", [None, 1, 2, 3])
+def test_exhaustive_bf16_round_trip(shuffle):
+    w = wl.all_bf16_patterns(shuffle)
+    assert np.array_equal(oracle.decode(oracle.encode(w)), w)
+
+
+@pytest.mark.parametrize("shape", [(128, 512), (512, 128), (64, 1024), (1000, 70), (3, 21845)])
+def test_exhaustive_patterns_other_shapes(shape):
+    v = wl.all_bf16_patterns(5).reshape(-1)
+    n, k = shape
+    w = np.resize(v, n * k).reshape(n, k)
+    assert np.array_equal(oracle.decode(oracle.encode(w)), w)
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (1, 33), (129, 31), (127, 257), (300, 1000)])
+def test_ragged_round_trip(shape):
+    w = wl.gaussian_weights(*shape, seed=11)
+    assert np.array_equal(oracle.decode(oracle.encode(w)), w)
+
+
+def test_special_groups_round_trip():
+    rng = np.random.default_rng(3)
+    # one exponent everywhere
+    one = ((rng.integers(0, 2, (256, 512)) << 15) | (120 << 7) | rng.integers(0, 128, (256, 512))).astype(np.uint16)
+    # exactly 16 distinct exponents -> exactly one exponent escapes per segment
+    e16 = rng.integers(100, 116, (256, 512))
+    sixteen = ((e16 << 7) | rng.integers(0, 128, (256, 512))).astype(np.uint16)
+    # every weight escapes: 256 exponents in equal shares, most outside any table
+    allesc = wl.forced_escape_weights(256, 512, 1.0, seed=4)
+    for w in (one, sixteen, allesc):
+        assert np.array_equal(oracle.decode(oracle.encode(w)), w)
+    blob = oracle.encode(one)
+    assert _hdr(blob, 0x80, 8) == 0
+    blob16 = oracle.encode(sixteen)
+    assert _hdr(blob16, 0x80, 8) > 0
+
+
+def test_hand_worked_2x2_blob():
+    # W = [[1.0, -2.0], [0.5, 3.0]] padded with +0.0 to 128 x 32.
+    # exponents: 1.0 -> 127, -2.0 -> 128, 0.5 -> 126, 3.0 -> 128, pads -> 0.
+    # counts: 0:4092, 128:2, 126:1, 127:1; ranked 0, 128, 126, 127.
+    # L = [0, 126, 127] (odd), H = [128]: sequence 0, 126, 127, 128 into the
+    # slots 7, 0, 8, 1; slot 9 copies its partner 1; the rest are 0.
+    w = np.array([[0x3F80, 0xC000], [0x3F00, 0x4040]], dtype=np.uint16)
+    blob = oracle.encode(w)
+    assert bytes(blob[:4]) == b"W12B"
+    assert _hdr(blob, 0x04, 4) == 1 and _hdr(blob, 0x10, 8) == 2 and _hdr(blob, 0x18, 8) == 2
+    assert _hdr(blob, 0x20, 8) == 128 and _hdr(blob, 0x28, 8) == 32
+    assert _hdr(blob, 0x40, 8) == 1 and _hdr(blob, 0x48, 8) == 1 and _hdr(blob, 0x50, 8) == 1
+    assert _hdr(blob, 0x58, 8) == 256 and _hdr(blob, 0x60, 8) == 32
+    assert _hdr(blob, 0x68, 8) == 512 and _hdr(blob, 0x70, 8) == 6144
+    assert _hdr(blob, 0x78, 8) == 512 + 6144 and _hdr(blob, 0x80, 8) == 0
+    assert _hdr(blob, 0x90, 8) == blob.size == 512 + 6144
+    table = list(blob[256:272])
+    assert table == [126, 128, 0, 0, 0, 0, 0, 0, 127, 128, 0, 0, 0, 0, 0, 0]
+    assert list(blob[272:304]) == [0] * 32  # no escapes: base 0, counts 0, mask 0
+    chunk = blob[512:512 + 6144]
+    # S bytes: (mantissa << 1) | sign of the pair partner
+    assert chunk[0] == 1 and chunk[1] == 0          # 1.0 takes -2.0's sign; -2.0 takes 1.0's
+    assert chunk[16] == 0 and chunk[17] == 0x80     # 3.0 has mantissa 0x40
+    assert np.count_nonzero(chunk[:4096]) == 2
+    # codes: 127 -> 8, 128 -> 1, 126 -> 0; the pad exponent 0 first appears at slot 2
+    assert chunk[4096] == 0x18 and chunk[4096 + 16] == 0x10
+    codes = np.array(chunk[4096:]).reshape(128, 16)
+    codes[0, 0] = codes[1, 0] = 0x22
+    assert np.all(codes == 0x22)
+    assert np.array_equal(oracle.decode(blob), w)
+
+
+def _check_tables(w, blob):
+    wp = _padded(w)
+    expo = (wp >> 7) & 0xFF
+    heads = _seg_headers(blob)
+    tiles, segs = wp.shape[0] // 128, -(-wp.shape[1] // 256)
+    n_esc = 0
+    for t in range(tiles):
+        for s in range(segs):
+            hd = heads[t * segs + s]
+            T = hd[:16]
+            assert T[15] == 0
+            for j in range(7):
+                assert (T[j] >> 7) == (T[j + 8] >> 7), "pair slots must share the top bit"
+            blk = expo[128 * t:128 * (t + 1), 256 * s:256 * (s + 1)]
+            hist = np.bincount(blk.reshape(-1), minlength=256)
+            present = [e for e in range(256) if hist[e] > 0]
+            ranked = sorted(present, key=lambda e: (-hist[e], e))[:15]
+            held = set(int(v) for v in T[:15])
+            assert set(ranked) <= held
+            assert held - set(ranked) <= {0}
+            esc = int(sum(hist[e] for e in range(256) if e not in held))
+            qcount = [int(hd[20 + 2 * q]) | (int(hd[21 + 2 * q]) << 8) for q in range(4)]
+            assert sum(qcount) == esc
+            for q in range(4):
+                qb = blk[32 * q:32 * (q + 1)]
+                assert qcount[q] == int(sum(np.count_nonzero(qb == e) for e in range(256) if e not in held))
+            mask = int.from_bytes(bytes(hd[28:32]), "little")
+            for q in range(4):
+                for j in range(8):
+                    cb = blk[32 * q:32 * (q + 1), 32 * j:32 * (j + 1)]
+                    has = any(np.count_nonzero(cb == e) for e in range(256) if e not in held)
+                    assert bool(mask >> (8 * q + j) & 1) == has
+            base = int.from_bytes(bytes(hd[16:20]), "little")
+            assert base == n_esc
+            n_esc += esc
+    assert n_esc == _hdr(blob, 0x80, 8)
+
+
+@pytest.mark.parametrize("kind", ["gauss", "heavy", "forced2", "forced10", "allbits"])
+def test_table_is_top15_and_escapes_are_outside_mass(kind):
+    if kind == "gauss":
+        w = wl.gaussian_weights(256, 700, seed=21)
+    elif kind == "heavy":
+        w = wl.heavy_tail_weights(256, 700, seed=22)
+    elif kind == "forced2":
+        w = wl.forced_escape_weights(200, 600, 0.02, seed=23)
+    elif kind == "forced10":
+        w = wl.forced_escape_weights(200, 600, 0.10, seed=24)
+    else:
+        w = wl.all_bf16_patterns(9)
+    _check_tables(w, oracle.encode(w))
+
+
+def _expected_size(n, k, n_esc):
+    up = lambda v, a: -(-v // a) * a
+    tiles, chunks = up(n, 128) // 128, up(k, 32) // 32
+    segs = -(-chunks // 8)
+    off_w = up(256 + 32 * tiles * segs, 256)
+    off_e = up(off_w + 6144 * tiles * chunks, 256)
+    return up(off_e + up(n_esc, 16), 256)
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (128, 32), (130, 300), (1024, 1024)])
+def test_size_closed_form(shape):
+    w = wl.forced_escape_weights(*shape, 0.01, seed=5)
+    blob = oracle.encode(w)
+    assert blob.size == oracle.encoded_size(w) == _expected_size(*shape, _hdr(blob, 0x80, 8))
+
+
+def _gaussian_bin_mass(std):
+    """P(BF16(N(0, std)) has biased exponent e), from the normal CDF; the lower
+    edge of bin e is the midpoint between 2^(e-127) and its BF16 predecessor."""
+    def cdf_abs(v):
+        return math.erf(v / (std * math.sqrt(2.0)))
+    edges = {}
+    for e in range(1, 256):
+        p2 = 2.0 ** (e - 127)
+        edges[e] = p2 - 2.0 ** (e - 127 - 9)
+    mass = {}
+    for e in range(1, 255):
+        mass[e] = cdf_abs(edges[e + 1]) - cdf_abs(edges[e])
+    mass[0] = cdf_abs(edges[1])
+    return mass
+
+
+def test_gaussian_escape_rate_matches_normal_cdf():
+    w = wl.gaussian_weights(2048, 4096, seed=31)
+    blob = oracle.encode(w)
+    n_esc = _hdr(blob, 0x80, 8)
+    mass = _gaussian_bin_mass(wl.WEIGHT_STD)
+    top = sorted(mass, key=lambda e: -mass[e])[:15]
+    expect = (1.0 - sum(mass[e] for e in top)) * w.size
+    assert abs(n_esc - expect) < 0.15 * expect + 5 * math.sqrt(expect)
+
+
+def test_bits_per_weight_near_twelve():
+    w, _ = wl.single_case()
+    bpw = 8.0 * oracle.encoded_size(w) / w.size
+    facts = FACTS["bits_per_weight_dense"]
+    assert 12.0 < bpw <= facts["high"] + 0.005
+    big = wl.gaussian_weights(2048, 4096, seed=32)
+    bpw_big = 8.0 * oracle.encoded_size(big) / big.size
+    assert 12.0 < bpw_big <= facts["high"]
+    # "cuts weight traffic by a quarter": packed bytes / BF16 bytes
+    ratio = oracle.encoded_size(big) / (2.0 * big.size)
+    assert abs(ratio - (1.0 - FACTS["weight_traffic_cut"]["value"])) < 0.002
+
+
+def test_gemm_f64_matches_numpy_float64():
+    rng = np.random.default_rng(7)
+    for m, n, k in [(1, 5, 7), (3, 33, 65), (32, 130, 257)]:
+        x = wl.activations(m, k, seed=int(rng.integers(1 << 30)))
+        w = wl.gaussian_weights(n, k, seed=int(rng.integers(1 << 30)))
+        ref = wl.bf16_bits_to_f32(x).astype(np.float64) @ wl.bf16_bits_to_f32(w).astype(np.float64).T
+        assert np.allclose(oracle.gemm_f64(x, w), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_f64_one_hot_and_small_integers():
+    w = wl.gaussian_weights(64, 48, seed=8)
+    for kk in (0, 17, 47):
+        x = np.zeros((1, 48), dtype=np.uint16)
+        x[0, kk] = 0x3F80  # 1.0
+        y = oracle.gemm_f64(x, w)
+        assert np.array_equal(y[0], wl.bf16_bits_to_f32(w[:, kk]).astype(np.float64))
+    rng = np.random.default_rng(9)
+    wi = rng.integers(-8, 9, (40, 100))
+    xi = rng.integers(-8, 9, (4, 100))
+    y = oracle.gemm_f64(wl.to_bf16_bits(xi.astype(np.float32)), wl.to_bf16_bits(wi.astype(np.float32)))
+    assert np.array_equal(y, (xi @ wi.T).astype(np.float64))
+
+
+def test_w12_gemm_equals_gemm_over_original():
+    w = wl.heavy_tail_weights(300, 520, seed=10)
+    x = wl.activations(5, 520, seed=11)
+    blob = oracle.encode(w)
+    assert np.array_equal(oracle.w12_gemm_f64(x, blob, threads=2), oracle.gemm_f64(x, w))
+
+
+def test_malformed_blobs_are_rejected():
+    w = wl.gaussian_weights(130, 70, seed=12)
+    blob = oracle.encode(w)
+    with pytest.raises(ValueError):
+        oracle.decode(blob[:-256])
+    bad = blob.copy()
+    bad[0] = ord("X")
+    with pytest.raises(ValueError):
+        oracle.decode(bad)
+    bad = blob.copy()
+    bad[0x11] ^= 1  # N grows by 256: padded geometry no longer matches
+    with pytest.raises(ValueError):
+        oracle.decode(bad)
