@@ -1,0 +1,171 @@
+/*
+ * w12.h — C ABI of the W12 library (libw12.so): lossless ~12-bit BF16 weights
+ * decoded bit-exactly inside a memory-bound GEMM on GB300 (sm_103a).
+ *
+ * What the operation is, from the SpecPilot pages:
+ *   "StargazerX0/SpecPilot" (hotrepo.ai), §What it is — W12 is a 12-bit weight
+ *     format that decodes bit-exactly inside the GEMM; it speeds up plain BF16
+ *     decoding at batch 1-32.
+ *   "SpecPilot" (fasttoolhub.com), §Differentiation — a general lossless
+ *     12-bit weight format.
+ *   "SpecPilot: an agent doubled speculative decoding speed, and the 10.87x
+ *     needs context" (ai.jakubjirak.com), §The mechanisms it found — about
+ *     12.01-12.02 bits per weight, decoded in the GEMM's registers; 12 instead
+ *     of 16 bits cuts the weight traffic of a memory-bound decode by a quarter.
+ * The pages define no byte layout; this library defines W12 v1:
+ *
+ *   tile 128 rows, quarter 32 rows, chunk 32 columns, segment 256 columns.
+ *   N is padded to a multiple of 128 and K to a multiple of 32 with +0.0.
+ *   blob = 256-byte header | segment headers (32 B per tile x segment)
+ *        | packed chunks (6144 B per tile x chunk) | escape bytes; each part
+ *          starts on a 256-byte boundary.
+ *   segment header: table T[16] (code -> exponent; T[15] = 0 and slots j, j+8
+ *     share the exponent's top bit), u32 first-escape offset, u16 escape count
+ *     per quarter, u32 mask (bit 8q+j: quarter q has an escape in chunk j).
+ *   packed chunk: three 2048-byte slabs of 128 rows x 16 bytes: S bytes of
+ *     columns 0-15, S bytes of columns 16-31, 4-bit codes (even column in the
+ *     low nibble).  S byte = (mantissa << 1) | sign of the column-xor-1 partner.
+ *   code 15 = escape: the exponent is the next byte of the escape list, ordered
+ *     by tile, segment, quarter, chunk, row, column.
+ *
+ * Conventions for every call:
+ *   - Returns a w12_status (0 = W12_OK).  Nothing throws across the ABI.  On an
+ *     error w12_last_error() (per thread) describes it.
+ *   - The caller owns every buffer.  The library allocates no memory of its
+ *     own; its only state is one status word per device in static device
+ *     memory (see w12_check_status).
+ *   - Pointers named *_dev are device pointers; *_host are host pointers.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Device calls are asynchronous on that stream and never synchronise it,
+ *     except w12_check_status.
+ */
+#ifndef W12_H
+#define W12_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W12_FORMAT_VERSION 1
+
+typedef enum w12_status {
+    W12_OK = 0,
+    W12_ERR_INVALID_ARG = 1,      /* null pointer, M out of range, ...          */
+    W12_ERR_SHAPE = 2,            /* N or K < 1, or sizes that overflow          */
+    W12_ERR_BUFFER_TOO_SMALL = 3, /* blob or workspace shorter than required     */
+    W12_ERR_ALIGNMENT = 4,        /* device pointer not aligned as documented    */
+    W12_ERR_CORRUPT_BLOB = 5,     /* header or segment headers inconsistent      */
+    W12_ERR_UNSUPPORTED_ARCH = 6, /* current device is not compute capability 10.3 */
+    W12_ERR_CUDA = 7,             /* a CUDA runtime call failed                   */
+    W12_ERR_TIMEOUT = 8           /* a kernel gave up a bounded wait (device word) */
+} w12_status;
+
+/* Geometry and plane offsets of a blob, filled by w12_blob_info. */
+typedef struct w12_info {
+    int64_t N, K;             /* original shape: W is N x K, y = x . W^T      */
+    int64_t N_pad, K_pad;     /* N rounded up to 128, K rounded up to 32       */
+    int64_t tiles;            /* N_pad / 128                                   */
+    int64_t chunks;           /* K_pad / 32 (per tile)                         */
+    int64_t segs;             /* ceil(chunks / 8) (per tile)                   */
+    uint64_t off_seghdr, bytes_seghdr;
+    uint64_t off_weights, bytes_weights;
+    uint64_t off_escapes, bytes_escapes;
+    uint64_t n_escapes;
+    uint64_t total_bytes;
+    double bits_per_weight;   /* 8 * total_bytes / (N * K)                     */
+} w12_info;
+
+/* Text of the last error on this thread ("" if none). */
+const char *w12_last_error(void);
+
+/* Name of a status code. */
+const char *w12_status_string(int status);
+
+/* Format version this library reads and writes (W12_FORMAT_VERSION). */
+int w12_format_version(void);
+
+/*
+ * Exact blob size for the N x K row-major BF16 matrix w_host (bit patterns).
+ * Runs the table and escape count of the encoder.  Errors: INVALID_ARG (null),
+ * SHAPE (N or K < 1, size overflow, more than 2^32-1 escapes).
+ */
+int w12_encoded_size_host(const uint16_t *w_host, int64_t N, int64_t K, size_t *bytes);
+
+/*
+ * Encode w_host (N x K, row-major BF16 bit patterns) into blob_host, which must
+ * hold at least w12_encoded_size_host bytes (else BUFFER_TOO_SMALL).  The
+ * output is canonical: equal inputs give equal bytes.  Uses all host cores.
+ * The caller copies the blob to the device (any 256-byte aligned address).
+ */
+int w12_encode_host(const uint16_t *w_host, int64_t N, int64_t K, void *blob_host,
+                    size_t bytes);
+
+/*
+ * Read and check the header of a host blob of `bytes` bytes and fill *out.
+ * Checks magic, version and every geometry field against N and K (CORRUPT_BLOB
+ * on mismatch, BUFFER_TOO_SMALL if the blob is shorter than its total size).
+ */
+int w12_blob_info(const void *blob_host, size_t bytes, w12_info *out);
+
+/*
+ * Full check of a host blob: the header as above, then every segment header
+ * (T[15] = 0, paired slots share the top bit, escape offsets are the running
+ * sum of the quarter counts, masks agree with the counts, the counts add up
+ * to the header's escape count).  CORRUPT_BLOB on any failure.
+ */
+int w12_blob_validate(const void *blob_host, size_t bytes);
+
+/*
+ * Decode a device-resident blob to BF16: w_out_dev[n * K + k] for n < N, k < K
+ * (row-major, N x K).  Bit-exact inverse of the encoder.  `info` comes from
+ * w12_blob_info on a host copy of the same blob.  blob_dev must be 256-byte
+ * aligned and w_out_dev 2-byte aligned (ALIGNMENT).  Asynchronous on stream.
+ */
+int w12_decode(const void *blob_dev, const w12_info *info, uint16_t *w_out_dev, void *stream);
+
+/*
+ * Workspace bytes w12_gemm needs for this blob and token count M (1..32).
+ * The workspace holds the split-K fp32 partials, one arrival counter per
+ * tile and, when x is not TMA-aligned, a padded copy of x.
+ */
+int w12_gemm_workspace_size(const w12_info *info, int M, size_t *bytes);
+
+/*
+ * y_dev[m * N + n] = BF16_rne( sum_k x_dev[m * K + k] * W[n][k] ), fp32
+ * accumulation, for 1 <= M <= 32, with W held by blob_dev.  The weights are
+ * streamed from HBM in packed form and decoded in registers; tensor cores
+ * (tcgen05, weights as the 128-row A operand, tokens as N = 16 or 32) do the
+ * products.  x_dev: M x K row-major BF16; y_dev: M x N row-major BF16, 2-byte
+ * aligned.  blob_dev must be 256-byte aligned.  workspace: at least
+ * w12_gemm_workspace_size bytes, 256-byte aligned, ZERO-FILLED BEFORE ITS
+ * FIRST USE; every successful call leaves the counters zero again (after a
+ * TIMEOUT, zero it again).  Calls sharing one workspace must be ordered on
+ * the GPU (same stream, or synchronised).  Asynchronous on stream; errors found
+ * on the device are reported by w12_check_status.
+ */
+int w12_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info *info,
+             uint16_t *y_dev, int M, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status word,
+ * which kernels set when a bounded wait gives up.  Returns TIMEOUT if it was
+ * set, CUDA on a CUDA error, else OK.
+ */
+int w12_check_status(void *stream);
+
+/*
+ * Diagnostic: launch one kernel on `stream` that waits on a barrier nothing
+ * ever completes, giving up after timeout_us microseconds and recording the
+ * timeout in the status word — the same bounded-wait path the GEMM uses, with
+ * no fault.  A following w12_check_status(stream) returns W12_ERR_TIMEOUT.
+ * (No passage of the pages covers this; it tests the library's failure path.)
+ */
+int w12_selftest_timeout(uint32_t timeout_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W12_H */

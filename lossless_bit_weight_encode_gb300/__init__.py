@@ -1,0 +1,67 @@
+"""W12: lossless ~12-bit BF16 weights decoded inside the GEMM, for GB300 (sm_103a).
+
+``w12`` is the ctypes binding of libw12.so (C ABI in include/w12.h);
+``W12Weight`` is a small convenience holder built on it (torch provides the
+device memory and the stream).  ``workloads`` draws the seeded synthetic inputs.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import w12
+from .w12 import W12Error
+
+__all__ = ["w12", "W12Error", "W12Weight"]
+
+
+class W12Weight:
+    """A weight matrix held on the device in W12 form.
+
+    ``W12Weight(bits)`` encodes the N x K BF16 bit patterns (numpy uint16) on
+    the host with the library's encoder and copies the blob to the current CUDA
+    device.  ``gemm(x)`` returns ``x . W^T`` (BF16) for x of shape [M, K],
+    1 <= M <= 32; ``decode()`` returns W (BF16) bit-exactly.
+    """
+
+    def __init__(self, bits: np.ndarray, device=None):
+        import torch
+
+        self.blob_host = w12.w12_encode_host(bits)
+        self.info = w12.w12_blob_info(self.blob_host)
+        self.N, self.K = int(self.info.N), int(self.info.K)
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.blob = torch.from_numpy(self.blob_host).to(dev)
+        self._ws = {}
+
+    @property
+    def bits_per_weight(self) -> float:
+        return float(self.info.bits_per_weight)
+
+    def workspace(self, M: int):
+        import torch
+
+        size = w12.w12_gemm_workspace_size(self.info, M)
+        ws = self._ws.get(M)
+        if ws is None or ws.numel() < size:
+            ws = torch.zeros(max(size, 256), dtype=torch.uint8, device=self.blob.device)
+            self._ws[M] = ws
+        return ws
+
+    def gemm(self, x, out=None, stream=None):
+        import torch
+
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != self.K or not x.is_contiguous():
+            raise ValueError("x must be a contiguous BF16 tensor of shape [M, K]")
+        M = int(x.shape[0])
+        if out is None:
+            out = torch.empty((M, self.N), dtype=torch.bfloat16, device=x.device)
+        w12.w12_gemm(x, self.blob, self.info, out, M, self.workspace(M), stream)
+        return out
+
+    def decode(self, out=None, stream=None):
+        import torch
+
+        if out is None:
+            out = torch.empty((self.N, self.K), dtype=torch.bfloat16, device=self.blob.device)
+        w12.w12_decode(self.blob, self.info, out, stream)
+        return out

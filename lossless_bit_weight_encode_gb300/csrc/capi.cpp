@@ -1,0 +1,160 @@
+// C ABI of the W12 library (declared in include/w12.h): argument checks,
+// error strings, and dispatch to the host encoder and the kernel launchers.
+// No exception crosses this boundary.
+#include <cstdint>
+#include <exception>
+#include <string>
+
+#include "../../include/w12.h"
+#include "w12_host.hpp"
+#include "w12_launch.hpp"
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int finish(int rc, const std::string &err) {
+    t_last_error = rc == W12_OK ? std::string() : err;
+    return rc;
+}
+
+template <class Fn>
+int guarded(Fn fn) {
+    try {
+        std::string err;
+        const int rc = fn(err);
+        return finish(rc, err);
+    } catch (const std::exception &e) {
+        return finish(W12_ERR_INVALID_ARG, std::string("internal error: ") + e.what());
+    } catch (...) {
+        return finish(W12_ERR_INVALID_ARG, "internal error");
+    }
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_info(const w12_info *info, std::string &err) {
+    if (!info) {
+        err = "info is null";
+        return W12_ERR_INVALID_ARG;
+    }
+    if (info->N < 1 || info->K < 1 || info->tiles != info->N_pad / 128 || info->chunks != info->K_pad / 32 ||
+        info->N_pad != (info->N + 127) / 128 * 128 || info->K_pad != (info->K + 31) / 32 * 32 ||
+        info->segs != (info->chunks + 7) / 8) {
+        err = "info does not describe a W12 v1 blob (fill it with w12_blob_info)";
+        return W12_ERR_INVALID_ARG;
+    }
+    return W12_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *w12_last_error(void) { return t_last_error.c_str(); }
+
+const char *w12_status_string(int status) {
+    switch (status) {
+    case W12_OK: return "W12_OK";
+    case W12_ERR_INVALID_ARG: return "W12_ERR_INVALID_ARG";
+    case W12_ERR_SHAPE: return "W12_ERR_SHAPE";
+    case W12_ERR_BUFFER_TOO_SMALL: return "W12_ERR_BUFFER_TOO_SMALL";
+    case W12_ERR_ALIGNMENT: return "W12_ERR_ALIGNMENT";
+    case W12_ERR_CORRUPT_BLOB: return "W12_ERR_CORRUPT_BLOB";
+    case W12_ERR_UNSUPPORTED_ARCH: return "W12_ERR_UNSUPPORTED_ARCH";
+    case W12_ERR_CUDA: return "W12_ERR_CUDA";
+    case W12_ERR_TIMEOUT: return "W12_ERR_TIMEOUT";
+    default: return "W12_ERR_UNKNOWN";
+    }
+}
+
+int w12_format_version(void) { return W12_FORMAT_VERSION; }
+
+int w12_encoded_size_host(const uint16_t *w_host, int64_t N, int64_t K, size_t *bytes) {
+    return guarded([&](std::string &err) {
+        uint64_t b = 0;
+        const int rc = w12::host::encoded_size(w_host, N, K, &b, &err);
+        if (rc == W12_OK) *bytes = (size_t)b;
+        return rc;
+    });
+}
+
+int w12_encode_host(const uint16_t *w_host, int64_t N, int64_t K, void *blob_host, size_t bytes) {
+    return guarded([&](std::string &err) {
+        return w12::host::encode(w_host, N, K, static_cast<uint8_t *>(blob_host), bytes, &err);
+    });
+}
+
+int w12_blob_info(const void *blob_host, size_t bytes, w12_info *out) {
+    return guarded([&](std::string &err) {
+        return w12::host::parse_header(static_cast<const uint8_t *>(blob_host), bytes, out, &err);
+    });
+}
+
+int w12_blob_validate(const void *blob_host, size_t bytes) {
+    return guarded([&](std::string &err) {
+        return w12::host::validate(static_cast<const uint8_t *>(blob_host), bytes, &err);
+    });
+}
+
+int w12_decode(const void *blob_dev, const w12_info *info, uint16_t *w_out_dev, void *stream) {
+    return guarded([&](std::string &err) {
+        int rc = check_info(info, err);
+        if (rc != W12_OK) return rc;
+        if (!blob_dev || !w_out_dev) {
+            err = "null device pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (!aligned(blob_dev, 256) || !aligned(w_out_dev, 2)) {
+            err = "blob_dev must be 256-byte aligned and w_out_dev 2-byte aligned";
+            return (int)W12_ERR_ALIGNMENT;
+        }
+        return w12::launch::decode(blob_dev, *info, w_out_dev, stream, &err);
+    });
+}
+
+int w12_gemm_workspace_size(const w12_info *info, int M, size_t *bytes) {
+    return guarded([&](std::string &err) {
+        int rc = check_info(info, err);
+        if (rc != W12_OK) return rc;
+        if (!bytes) {
+            err = "bytes is null";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        w12::launch::GemmPlan plan;
+        rc = w12::launch::plan_gemm(*info, M, &plan, &err);
+        if (rc == W12_OK) *bytes = plan.ws_bytes;
+        return rc;
+    });
+}
+
+int w12_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info *info, uint16_t *y_dev, int M,
+             void *workspace, size_t ws_bytes, void *stream) {
+    return guarded([&](std::string &err) {
+        int rc = check_info(info, err);
+        if (rc != W12_OK) return rc;
+        if (!x_dev || !blob_dev || !y_dev || !workspace) {
+            err = "null device pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (M < 1 || M > 32) {
+            err = "M must be in 1..32";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (!aligned(blob_dev, 256) || !aligned(workspace, 256) || !aligned(y_dev, 2) || !aligned(x_dev, 2)) {
+            err = "blob_dev and workspace must be 256-byte aligned, x_dev and y_dev 2-byte aligned";
+            return (int)W12_ERR_ALIGNMENT;
+        }
+        return w12::launch::gemm(x_dev, blob_dev, *info, y_dev, M, workspace, ws_bytes, stream, &err);
+    });
+}
+
+int w12_check_status(void *stream) {
+    return guarded([&](std::string &err) { return w12::launch::check_status(stream, &err); });
+}
+
+int w12_selftest_timeout(uint32_t timeout_us, void *stream) {
+    return guarded([&](std::string &err) { return w12::launch::selftest_timeout(timeout_us, stream, &err); });
+}
+
+}  // extern "C"

@@ -1,0 +1,326 @@
+// Host launchers of the W12 kernels and the per-device status word.
+//
+// One translation unit holds every kernel so that the status word
+// (g_w12_status, static device memory: no allocation) is one symbol per device.
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "decode.cuh"
+#include "gemm_tc.cuh"
+#include "w12_launch.hpp"
+
+namespace w12 {
+namespace dev {
+
+__device__ uint32_t g_w12_status;
+
+// Copies x [M][K] into a zero-padded [M][K8] buffer whose rows are 16-byte
+// aligned, for the tensor map (used only when x itself is not so aligned).
+__global__ void w12_pad_x_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ xp, int M, int64_t K,
+                                 int64_t K8) {
+    const int64_t total = (int64_t)M * K8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / K8, k = i % K8;
+        xp[i] = k < K ? x[m * K + k] : (uint16_t)0;
+    }
+}
+
+// Waits on an mbarrier that nothing arrives on, with a short deadline, and
+// records the timeout: exercises the bounded-wait path without a fault.
+__global__ void w12_selftest_timeout_kernel(uint32_t *status, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, globaltimer_ns() + timeout_ns)) atomicOr(status, kStatusTimeout);
+}
+
+}  // namespace dev
+
+namespace launch {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int status_code = W12_OK;
+    std::string error;
+    int sm_count = 0;
+    uint32_t *status = nullptr;
+    int occupancy[2][2] = {{0, 0}, {0, 0}};  // [ntok==32][a_smem]
+};
+
+DeviceState g_state[kMaxDevices];
+std::mutex g_mu;
+
+template <int NTOK, bool ASMEM>
+void *gemm_kernel_ptr() {
+    return reinterpret_cast<void *>(&dev::w12_gemm_tc_kernel<NTOK, kStages, ASMEM>);
+}
+template <int NTOK, bool ASMEM>
+int gemm_smem_bytes() {
+    return dev::GemmCfg<NTOK, kStages, ASMEM>::kSmemBytes;
+}
+
+int cuda_fail(cudaError_t e, const char *what, std::string *err) {
+    *err = std::string(what) + ": " + cudaGetErrorString(e);
+    return W12_ERR_CUDA;
+}
+
+template <int NTOK, bool ASMEM>
+int prepare_gemm(DeviceState &s, std::string *err) {
+    void *k = gemm_kernel_ptr<NTOK, ASMEM>();
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm_smem_bytes<NTOK, ASMEM>());
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", err);
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, 192, (size_t)gemm_smem_bytes<NTOK, ASMEM>());
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor", err);
+    // TMEM: each CTA holds 128 of the SM's 512 columns
+    s.occupancy[NTOK == 32][ASMEM] = occ < 4 ? occ : 4;
+    return W12_OK;
+}
+
+// Per-device set-up on first use (with that device current).
+int device_state(DeviceState **out, std::string *err) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice", err);
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = "device ordinal out of range";
+        return W12_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &s = g_state[dev];
+    if (!s.ready) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        e = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute", err);
+        if (major != 10 || minor != 3) {
+            *err = "W12 kernels are built for sm_103a (compute capability 10.3); this device is " +
+                   std::to_string(major) + "." + std::to_string(minor);
+            return W12_ERR_UNSUPPORTED_ARCH;
+        }
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), dev::g_w12_status);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)", err);
+        int rc = prepare_gemm<16, false>(s, err);
+        if (rc == W12_OK) rc = prepare_gemm<32, false>(s, err);
+        if (rc == W12_OK) rc = prepare_gemm<16, true>(s, err);
+        if (rc == W12_OK) rc = prepare_gemm<32, true>(s, err);
+        if (rc != W12_OK) return rc;
+        s.ready = true;
+    }
+    *out = &s;
+    return W12_OK;
+}
+
+bool use_smem_a_operand() {
+    const char *v = std::getenv("W12_A_OPERAND");
+    return v != nullptr && std::strcmp(v, "smem") == 0;
+}
+
+uint64_t timeout_ns() {
+    const char *v = std::getenv("W12_TIMEOUT_MS");
+    const long ms = v ? std::strtol(v, nullptr, 10) : 0;
+    return (uint64_t)(ms > 0 ? ms : 4000) * 1000000ull;
+}
+
+size_t up256(size_t v) { return (v + 255) / 256 * 256; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder(std::string *err) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!fn) *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return fn;
+}
+
+}  // namespace
+
+int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err) {
+    if (M < 1 || M > 32) {
+        *err = "M must be in 1..32";
+        return W12_ERR_INVALID_ARG;
+    }
+    DeviceState *s = nullptr;
+    int rc = device_state(&s, err);
+    if (rc != W12_OK) return rc;
+    plan->ntok = M <= 16 ? 16 : 32;
+    const int occ = s->occupancy[plan->ntok == 32][use_smem_a_operand()];
+    if (occ < 1) {
+        *err = "GEMM kernel cannot be resident on this device";
+        return W12_ERR_CUDA;
+    }
+    constexpr int64_t kMaxSegs = dev::GemmCfg<16, kStages, false>::kMaxSegs;
+    const int64_t capacity = (int64_t)s->sm_count * occ;
+    const int64_t tiles = info.tiles, segs = info.segs;
+    int64_t splits = capacity / tiles;
+    if (splits < 1) splits = 1;
+    if (splits > segs) splits = segs;
+    int64_t per = (segs + splits - 1) / splits;          // segments of the longest CTA
+    if (per > kMaxSegs) per = kMaxSegs;
+    splits = (segs + per - 1) / per;                      // fewest splits with that length
+    if (const char *v = std::getenv("W12_SPLITS")) {      // tuning override
+        const long f = std::strtol(v, nullptr, 10);
+        if (f >= 1 && f <= segs && (segs + f - 1) / f <= kMaxSegs) splits = f;
+    }
+    plan->splits = (int)splits;
+    plan->ctas = (int)(tiles * splits);
+    const int64_t k8 = (info.K + 7) / 8 * 8;
+    plan->ws_counters = 0;
+    plan->ws_partials = up256((size_t)tiles * 4);
+    const size_t partial_bytes = splits > 1 ? up256((size_t)splits * (size_t)M * (size_t)info.N_pad * 4) : 0;
+    plan->ws_x = plan->ws_partials + partial_bytes;
+    plan->ws_bytes = plan->ws_x + up256((size_t)M * (size_t)k8 * 2);
+    return W12_OK;
+}
+
+int decode(const void *blob_dev, const w12_info &info, uint16_t *out_dev, void *stream, std::string *err) {
+    DeviceState *s = nullptr;
+    int rc = device_state(&s, err);
+    if (rc != W12_OK) return rc;
+    dev::DecodeParams p;
+    p.blob = static_cast<const uint8_t *>(blob_dev);
+    p.off_seg = info.off_seghdr;
+    p.off_w = info.off_weights;
+    p.off_esc = info.off_escapes;
+    p.N = info.N;
+    p.K = info.K;
+    p.chunks = info.chunks;
+    p.segs = info.segs;
+    p.out = out_dev;
+    dim3 grid((unsigned)info.segs, (unsigned)info.tiles);
+    dev::w12_decode_kernel<<<grid, 128, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch", err);
+    return W12_OK;
+}
+
+namespace {
+template <int NTOK, bool ASMEM>
+cudaError_t launch_gemm_kernel(const dev::GemmParams &p, const CUtensorMap &tm, int splits, int64_t tiles,
+                               cudaStream_t st) {
+    dim3 grid((unsigned)splits, (unsigned)tiles);
+    dev::w12_gemm_tc_kernel<NTOK, kStages, ASMEM><<<grid, 192, gemm_smem_bytes<NTOK, ASMEM>(), st>>>(p, tm);
+    return cudaGetLastError();
+}
+}  // namespace
+
+int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,
+         void *workspace, size_t ws_bytes, void *stream, std::string *err) {
+    GemmPlan plan;
+    int rc = plan_gemm(info, M, &plan, err);
+    if (rc != W12_OK) return rc;
+    if (ws_bytes < plan.ws_bytes) {
+        *err = "workspace smaller than w12_gemm_workspace_size";
+        return W12_ERR_BUFFER_TOO_SMALL;
+    }
+    DeviceState *s = nullptr;
+    rc = device_state(&s, err);
+    if (rc != W12_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+
+    // x must be a TMA source: 16-byte aligned rows (K % 8 == 0, aligned base)
+    const uint16_t *xsrc = x_dev;
+    int64_t ld = info.K;
+    if ((reinterpret_cast<uintptr_t>(x_dev) & 15) != 0 || (info.K & 7) != 0) {
+        ld = (info.K + 7) / 8 * 8;
+        uint16_t *xp = reinterpret_cast<uint16_t *>(ws + plan.ws_x);
+        const int64_t total = (int64_t)M * ld;
+        const int blocks = (int)((total + 255) / 256 < 1024 ? (total + 255) / 256 : 1024);
+        dev::w12_pad_x_kernel<<<blocks, 256, 0, st>>>(x_dev, xp, M, info.K, ld);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "x padding launch", err);
+        xsrc = xp;
+    }
+    auto encode = tensor_map_encoder(err);
+    if (!encode) return W12_ERR_CUDA;
+    CUtensorMap tm;
+    const cuuint64_t dims[2] = {(cuuint64_t)info.K, (cuuint64_t)M};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)plan.ntok};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult cr = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(xsrc), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) {
+        *err = "cuTensorMapEncodeTiled failed for x (code " + std::to_string((int)cr) + ")";
+        return W12_ERR_CUDA;
+    }
+
+    dev::GemmParams p;
+    p.blob = static_cast<const uint8_t *>(blob_dev);
+    p.off_seg = info.off_seghdr;
+    p.off_w = info.off_weights;
+    p.off_esc = info.off_escapes;
+    p.N = info.N;
+    p.Npad = info.N_pad;
+    p.chunks = (int32_t)info.chunks;
+    p.segs = (int32_t)info.segs;
+    p.M = M;
+    p.splits = plan.splits;
+    p.partials = reinterpret_cast<float *>(ws + plan.ws_partials);
+    p.counters = reinterpret_cast<uint32_t *>(ws + plan.ws_counters);
+    p.y = y_dev;
+    p.status = s->status;
+    p.timeout_ns = timeout_ns();
+
+    cudaError_t e;
+    const bool asmem = use_smem_a_operand();
+    if (plan.ntok == 16)
+        e = asmem ? launch_gemm_kernel<16, true>(p, tm, plan.splits, info.tiles, st)
+                  : launch_gemm_kernel<16, false>(p, tm, plan.splits, info.tiles, st);
+    else
+        e = asmem ? launch_gemm_kernel<32, true>(p, tm, plan.splits, info.tiles, st)
+                  : launch_gemm_kernel<32, false>(p, tm, plan.splits, info.tiles, st);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm launch", err);
+    return W12_OK;
+}
+
+int check_status(void *stream, std::string *err) {
+    DeviceState *s = nullptr;
+    int rc = device_state(&s, err);
+    if (rc != W12_OK) return rc;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize", err);
+    uint32_t v = 0;
+    e = cudaMemcpy(&v, s->status, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the status word", err);
+    if (v != 0) {
+        const uint32_t zero = 0;
+        cudaMemcpy(s->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        *err = "a W12 kernel gave up a bounded wait (status word " + std::to_string(v) + ")";
+        return W12_ERR_TIMEOUT;
+    }
+    return W12_OK;
+}
+
+int selftest_timeout(uint32_t timeout_us, void *stream, std::string *err) {
+    DeviceState *s = nullptr;
+    int rc = device_state(&s, err);
+    if (rc != W12_OK) return rc;
+    dev::w12_selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        s->status, (uint64_t)timeout_us * 1000ull);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "selftest launch", err);
+    return W12_OK;
+}
+
+}  // namespace launch
+}  // namespace w12

@@ -1,0 +1,300 @@
+// Device building blocks of the W12 kernels (sm_103a): mbarrier / TMA /
+// tcgen05 wrappers in inline PTX, and the in-register W12 decode.
+//
+// Register decode ("decoded inside the GEMM registers": "SpecPilot: an agent
+// doubled speculative decoding speed, and the 10.87x needs context", §The
+// mechanisms it found; "decodes bit-exactly inside the GEMM":
+// "StargazerX0/SpecPilot", §What it is).  One thread owns one row of a
+// 32-column chunk and turns its 48 packed bytes into 16 words of BF16 pairs:
+//
+//   exponent lookup  PRMT selects bytes with a 4-bit selector whose top bit
+//                    means "replicate the sign of the selected byte".  With
+//                    the table in four words R0..R3 (slots 0-15) and
+//                    R0' = R0 ^ signs(R2), R1' = R1 ^ signs(R3):
+//                      e = prmt(R0', R1', c) ^ prmt(R2, R3, c ^ 8)
+//                    gives T[c] for every c < 15, because the format keeps
+//                    slots j and j + 8 on the same top bit.  2 PRMT + 1 XOR
+//                    per four weights (plus selector prep per eight).
+//   assembly         prmt(S, E) interleaves [E1 S1 E0 S0]; since each S byte
+//                    is (mantissa << 1) | partner's sign, one 32-bit rotate
+//                    right by 1 lands both signs, exponents and mantissas on
+//                    their BF16 bits: 1 PRMT + 1 SHF per two weights.
+//   escapes          code 15: the exponent byte is patched from the escape
+//                    list (flags by a carry trick, warp scan for offsets).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace w12 {
+namespace dev {
+
+// ---------------------------------------------------------------- basics
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// PRMT in its default mode: selector nibble bits 0-2 pick a byte of {b, a},
+// bit 3 replaces it by its sign replicated over 8 bits.  (Written in PTX
+// because __byte_perm is documented to use 3-bit selectors only.)
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t rotr1(uint32_t x) { return __funnelshift_r(x, x, 1); }
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: true once the phase with `parity` has completed, false when
+// `deadline_ns` (globaltimer) passes first.  Nothing here can spin forever.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t deadline_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && globaltimer_ns() > deadline_ns) return false;
+    }
+}
+
+// ---------------------------------------------------------------- TMA
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 2-D tiled tensor copy global -> shared (coordinates in elements, x first).
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int32_t x, int32_t y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16 (BF16 in, fp32 accumulate).
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_taddr),
+        "r"(a_taddr), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T.
+__device__ __forceinline__ void mma_smem_a(uint32_t d_taddr, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_taddr),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// Warp-collective store of 16 32-bit columns (lane i -> TMEM lane base + i).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Warp-collective load of 16 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Make generic-proxy writes to shared memory visible to the async proxy
+// (tensor cores reading an operand written by st.shared).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1 at bit 46, and the
+// layout type in bits 61-63 (0 none, 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)(layout & 7u) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 D, BF16 A and B, both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- W12 decode
+// The segment table in the four words the lookup uses (see the file header).
+struct Table {
+    uint32_t u0, u1, u2, u3;
+};
+
+__device__ __forceinline__ Table make_table(uint4 t) {
+    Table r;
+    r.u0 = t.x ^ prmt(t.z, 0u, 0xBA98u);  // xor with the signs of slots 8..11
+    r.u1 = t.y ^ prmt(t.w, 0u, 0xBA98u);  // xor with the signs of slots 12..15
+    r.u2 = t.z;
+    r.u3 = t.w;
+    return r;
+}
+
+// Exponent bytes of the eight weights whose codes fill word w (code k in
+// nibble k): ea gets codes 0-3, eb codes 4-7, one exponent per byte.
+__device__ __forceinline__ void lookup8(const Table &T, uint32_t w, uint32_t &ea, uint32_t &eb) {
+    const uint32_t wh = w >> 16;
+    ea = prmt(T.u0, T.u1, w) ^ prmt(T.u2, T.u3, w ^ 0x8888u);
+    eb = prmt(T.u0, T.u1, wh) ^ prmt(T.u2, T.u3, wh ^ 0x8888u);
+}
+
+// E[j] = exponents of columns 4j..4j+3 of the thread's row.
+__device__ __forceinline__ void decode_exponents(const Table &T, const uint4 &codes, uint32_t (&E)[8]) {
+    lookup8(T, codes.x, E[0], E[1]);
+    lookup8(T, codes.y, E[2], E[3]);
+    lookup8(T, codes.z, E[4], E[5]);
+    lookup8(T, codes.w, E[6], E[7]);
+}
+
+// out[i] = BF16 pair (column 2i in the low half, 2i+1 in the high half).
+__device__ __forceinline__ void assemble(const uint4 &s_lo, const uint4 &s_hi, const uint32_t (&E)[8],
+                                         uint32_t (&out)[16]) {
+    const uint32_t S[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        out[2 * j] = rotr1(prmt(S[j], E[j], 0x5140u));      // [E1 S1 E0 S0]
+        out[2 * j + 1] = rotr1(prmt(S[j], E[j], 0x7362u));  // [E3 S3 E2 S2]
+    }
+}
+
+// Bit 4p+3 set exactly where nibble p of w equals 15 (the escape code):
+// adding 7 to the low three bits of ~w carries into bit 3 unless they are 0.
+__device__ __forceinline__ uint32_t escape_flags(uint32_t w) {
+    const uint32_t t = (~w & 0x77777777u) + 0x77777777u;
+    return ~t & w & 0x88888888u;
+}
+
+// Patch the escaped exponents of one thread's row chunk, reading the escape
+// bytes in column order from src.
+__device__ __forceinline__ void patch_escapes(const uint32_t (&f)[4], const uint8_t *src, uint32_t (&E)[8]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t fj = (f[j >> 1] >> (16 * (j & 1))) & 0x8888u;
+        while (fj) {
+            const uint32_t b = (uint32_t)__ffs(fj) - 1u;  // 3, 7, 11 or 15
+            fj &= fj - 1u;
+            const uint32_t sh = (b >> 2) << 3;
+            const uint32_t e = *src++;
+            E[j] = (E[j] & ~(0xFFu << sh)) | (e << sh);
+        }
+    }
+}
+
+// Warp-wide escape step for one quarter-chunk: every lane finds its escapes,
+// an exclusive scan over the lanes gives each lane its first byte in the
+// quarter's run (rows in lane order, columns in order), and the exponents are
+// patched.  Returns the warp's escape count (to advance the run).
+__device__ __forceinline__ uint32_t warp_escapes(const uint4 &codes, const uint8_t *run, uint32_t (&E)[8]) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t f[4] = {escape_flags(codes.x), escape_flags(codes.y), escape_flags(codes.z),
+                           escape_flags(codes.w)};
+    const uint32_t cnt = __popc(f[0]) + __popc(f[1]) + __popc(f[2]) + __popc(f[3]);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= (uint32_t)d) incl += v;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (cnt) patch_escapes(f, run + (incl - cnt), E);
+    return total;
+}
+
+}  // namespace dev
+}  // namespace w12

@@ -1,0 +1,82 @@
+// W12 v1 format constants and blob geometry shared by the host encoder, the
+// C ABI and the kernels of the library.  (The test oracle keeps its own copy.)
+//
+// Format definition: see include/w12.h.  Sources for the properties the format
+// must have: "StargazerX0/SpecPilot" (hotrepo.ai) §What it is; "SpecPilot"
+// (fasttoolhub.com) §Differentiation; "SpecPilot: an agent doubled speculative
+// decoding speed, and the 10.87x needs context" (ai.jakubjirak.com) §The
+// mechanisms it found.
+#pragma once
+
+#include <cstdint>
+
+namespace w12 {
+
+constexpr int kTileRows = 128;
+constexpr int kQuarterRows = 32;
+constexpr int kChunkK = 32;
+constexpr int kSegK = 256;
+constexpr int kChunksPerSeg = kSegK / kChunkK;   // 8
+constexpr int kSlabBytes = kTileRows * 16;       // 2048
+constexpr int kChunkBytes = 3 * kSlabBytes;      // 6144
+constexpr int kSegHdrBytes = 32;
+constexpr int kHeaderBytes = 256;
+constexpr int kPlaneAlign = 256;
+constexpr uint32_t kMagic = 0x42323157u;         // "W12B" little-endian
+constexpr uint32_t kVersion = 1;
+
+// Header field offsets.
+namespace hdr {
+constexpr int kMagicOff = 0x00, kVersionOff = 0x04, kHeaderBytesOff = 0x08, kFlagsOff = 0x0C;
+constexpr int kN = 0x10, kK = 0x18, kNpad = 0x20, kKpad = 0x28;
+constexpr int kTileRowsOff = 0x30, kChunkKOff = 0x34, kSegKOff = 0x38, kQuarterOff = 0x3C;
+constexpr int kTiles = 0x40, kChunks = 0x48, kSegs = 0x50;
+constexpr int kOffSeg = 0x58, kBytesSeg = 0x60, kOffW = 0x68, kBytesW = 0x70;
+constexpr int kOffEsc = 0x78, kNEsc = 0x80, kBytesEsc = 0x88, kTotal = 0x90;
+}  // namespace hdr
+
+// Segment header layout (32 bytes).
+struct SegHeader {
+    uint8_t table[16];
+    uint32_t esc_base;
+    uint16_t qcount[4];
+    uint32_t chunk_mask;
+};
+static_assert(sizeof(SegHeader) == kSegHdrBytes, "segment header is 32 bytes");
+
+struct Geometry {
+    int64_t N = 0, K = 0, Npad = 0, Kpad = 0;
+    int64_t tiles = 0, chunks = 0, segs = 0;
+    uint64_t off_seg = 0, bytes_seg = 0, off_w = 0, bytes_w = 0, off_esc = 0;
+
+    static inline uint64_t round_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
+
+    // Fills every plane offset that does not depend on the escape count.
+    static inline Geometry of(int64_t n, int64_t k) {
+        Geometry g;
+        g.N = n;
+        g.K = k;
+        g.Npad = (int64_t)round_up((uint64_t)n, kTileRows);
+        g.Kpad = (int64_t)round_up((uint64_t)k, kChunkK);
+        g.tiles = g.Npad / kTileRows;
+        g.chunks = g.Kpad / kChunkK;
+        g.segs = (g.chunks + kChunksPerSeg - 1) / kChunksPerSeg;
+        g.off_seg = kHeaderBytes;
+        g.bytes_seg = (uint64_t)kSegHdrBytes * (uint64_t)(g.tiles * g.segs);
+        g.off_w = round_up(g.off_seg + g.bytes_seg, kPlaneAlign);
+        g.bytes_w = (uint64_t)kChunkBytes * (uint64_t)(g.tiles * g.chunks);
+        g.off_esc = round_up(g.off_w + g.bytes_w, kPlaneAlign);
+        return g;
+    }
+    inline uint64_t bytes_esc(uint64_t n_esc) const { return round_up(n_esc, 16); }
+    inline uint64_t total(uint64_t n_esc) const {
+        return round_up(off_esc + bytes_esc(n_esc), kPlaneAlign);
+    }
+    // Chunks in segment s of any tile (the last segment may be short).
+    inline int seg_chunks(int64_t s) const {
+        int64_t left = chunks - s * kChunksPerSeg;
+        return (int)(left < kChunksPerSeg ? left : kChunksPerSeg);
+    }
+};
+
+}  // namespace w12

@@ -1,0 +1,19 @@
+// Host-side pieces of the W12 library: encoder, header parsing, blob checks.
+#pragma once
+
+#include <cstdint>
+#include <string>
+
+#include "../../include/w12.h"
+#include "w12_format.hpp"
+
+namespace w12 {
+namespace host {
+
+int encoded_size(const uint16_t *w, int64_t N, int64_t K, uint64_t *bytes, std::string *err);
+int encode(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, uint64_t cap, std::string *err);
+int parse_header(const uint8_t *blob, uint64_t bytes, w12_info *out, std::string *err);
+int validate(const uint8_t *blob, uint64_t bytes, std::string *err);
+
+}  // namespace host
+}  // namespace w12

@@ -1,0 +1,34 @@
+// Launch layer between the C ABI (capi.cpp) and the CUDA kernels (kernels.cu).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include "../../include/w12.h"
+
+namespace w12 {
+namespace launch {
+
+// How w12_gemm will run a problem on the current device.
+struct GemmPlan {
+    int ntok = 16;          // MMA token width (16 or 32)
+    int splits = 1;         // CTAs per tile along K
+    int ctas = 0;           // grid size
+    size_t ws_counters = 0, ws_partials = 0, ws_x = 0;  // workspace offsets
+    size_t ws_bytes = 0;
+};
+
+int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err);
+
+int decode(const void *blob_dev, const w12_info &info, uint16_t *out_dev, void *stream, std::string *err);
+
+int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,
+         void *workspace, size_t ws_bytes, void *stream, std::string *err);
+
+int check_status(void *stream, std::string *err);
+
+int selftest_timeout(uint32_t timeout_us, void *stream, std::string *err);
+
+}  // namespace launch
+}  // namespace w12

@@ -1,0 +1,170 @@
+"""Python binding of libw12.so (ctypes).  Argument marshalling only: every step
+of the encode, decode and GEMM runs in the library; torch supplies device
+memory and streams.  Function names match the C ABI in include/w12.h.
+
+There is no fallback: if the library is missing or a call fails, an exception
+is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libw12.so")
+
+W12_OK = 0
+STATUS_NAMES = {
+    0: "W12_OK", 1: "W12_ERR_INVALID_ARG", 2: "W12_ERR_SHAPE", 3: "W12_ERR_BUFFER_TOO_SMALL",
+    4: "W12_ERR_ALIGNMENT", 5: "W12_ERR_CORRUPT_BLOB", 6: "W12_ERR_UNSUPPORTED_ARCH", 7: "W12_ERR_CUDA",
+    8: "W12_ERR_TIMEOUT",
+}
+EXPORTED = (
+    "w12_last_error", "w12_status_string", "w12_format_version", "w12_encoded_size_host", "w12_encode_host",
+    "w12_blob_info", "w12_blob_validate", "w12_decode", "w12_gemm_workspace_size", "w12_gemm",
+    "w12_check_status", "w12_selftest_timeout",
+)
+
+
+class W12Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class w12_info(ctypes.Structure):
+    _fields_ = [
+        ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("N_pad", ctypes.c_int64), ("K_pad", ctypes.c_int64),
+        ("tiles", ctypes.c_int64), ("chunks", ctypes.c_int64), ("segs", ctypes.c_int64),
+        ("off_seghdr", ctypes.c_uint64), ("bytes_seghdr", ctypes.c_uint64),
+        ("off_weights", ctypes.c_uint64), ("bytes_weights", ctypes.c_uint64),
+        ("off_escapes", ctypes.c_uint64), ("bytes_escapes", ctypes.c_uint64),
+        ("n_escapes", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64),
+        ("bits_per_weight", ctypes.c_double),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"W12 library not built ({LIB_PATH} missing): run __graft_entry__.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, sz, i64, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64, ctypes.c_int
+    L.w12_last_error.restype = ctypes.c_char_p
+    L.w12_last_error.argtypes = []
+    L.w12_status_string.restype = ctypes.c_char_p
+    L.w12_status_string.argtypes = [i32]
+    L.w12_format_version.restype = i32
+    L.w12_format_version.argtypes = []
+    L.w12_encoded_size_host.argtypes = [vp, i64, i64, ctypes.POINTER(sz)]
+    L.w12_encode_host.argtypes = [vp, i64, i64, vp, sz]
+    L.w12_blob_info.argtypes = [vp, sz, ctypes.POINTER(w12_info)]
+    L.w12_blob_validate.argtypes = [vp, sz]
+    L.w12_decode.argtypes = [vp, ctypes.POINTER(w12_info), vp, vp]
+    L.w12_gemm_workspace_size.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(sz)]
+    L.w12_gemm.argtypes = [vp, vp, ctypes.POINTER(w12_info), vp, i32, vp, sz, vp]
+    L.w12_check_status.argtypes = [vp]
+    L.w12_selftest_timeout.argtypes = [ctypes.c_uint32, vp]
+    for name in EXPORTED[3:]:
+        getattr(L, name).restype = i32
+    _lib = L
+    return L
+
+
+def _check(rc: int) -> None:
+    if rc != W12_OK:
+        raise W12Error(rc, lib().w12_last_error().decode())
+
+
+def _host_u16(w: np.ndarray) -> np.ndarray:
+    w = np.ascontiguousarray(w)
+    if w.dtype != np.uint16 or w.ndim != 2:
+        raise TypeError("weights must be a 2-D uint16 array of BF16 bit patterns")
+    return w
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---------------------------------------------------------------- host calls
+def w12_encoded_size_host(w: np.ndarray) -> int:
+    w = _host_u16(w)
+    out = ctypes.c_size_t()
+    _check(lib().w12_encoded_size_host(w.ctypes.data, w.shape[0], w.shape[1], ctypes.byref(out)))
+    return out.value
+
+
+def w12_encode_host(w: np.ndarray) -> np.ndarray:
+    """Canonical W12 blob (uint8 array) of the N x K BF16 bit patterns `w`."""
+    w = _host_u16(w)
+    size = w12_encoded_size_host(w)
+    blob = np.empty(size, dtype=np.uint8)
+    _check(lib().w12_encode_host(w.ctypes.data, w.shape[0], w.shape[1], blob.ctypes.data, size))
+    return blob
+
+
+def w12_blob_info(blob: np.ndarray) -> w12_info:
+    blob = np.ascontiguousarray(blob, dtype=np.uint8)
+    info = w12_info()
+    _check(lib().w12_blob_info(blob.ctypes.data, blob.size, ctypes.byref(info)))
+    return info
+
+
+def w12_blob_validate(blob: np.ndarray) -> None:
+    blob = np.ascontiguousarray(blob, dtype=np.uint8)
+    _check(lib().w12_blob_validate(blob.ctypes.data, blob.size))
+
+
+# ---------------------------------------------------------------- device calls
+def w12_decode(blob_dev, info: w12_info, out_dev, stream=None) -> None:
+    """Decode a device blob (torch uint8 tensor) into out_dev (torch int16/bf16 [N, K])."""
+    _check(lib().w12_decode(blob_dev.data_ptr(), ctypes.byref(info), out_dev.data_ptr(), _stream_handle(stream)))
+
+
+def w12_gemm_workspace_size(info: w12_info, M: int) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().w12_gemm_workspace_size(ctypes.byref(info), int(M), ctypes.byref(out)))
+    return out.value
+
+
+def w12_gemm(x_dev, blob_dev, info: w12_info, y_dev, M: int, workspace, stream=None) -> None:
+    """y_dev[M, N] = x_dev[M, K] . W^T on the device (torch tensors, BF16)."""
+    _check(lib().w12_gemm(x_dev.data_ptr(), blob_dev.data_ptr(), ctypes.byref(info), y_dev.data_ptr(), int(M),
+                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                          _stream_handle(stream)))
+
+
+def w12_gemm_ptr(x_ptr: int, blob_ptr: int, info: w12_info, y_ptr: int, M: int, ws_ptr: int, ws_bytes: int,
+                 stream_handle: int | None) -> int:
+    """Raw-pointer form of w12_gemm that returns the status instead of raising
+    (for timing loops that check once at the end)."""
+    return lib().w12_gemm(x_ptr, blob_ptr, ctypes.byref(info), y_ptr, int(M), ws_ptr, ws_bytes, stream_handle)
+
+
+def w12_check_status(stream=None) -> None:
+    _check(lib().w12_check_status(_stream_handle(stream)))
+
+
+def w12_selftest_timeout(timeout_us: int, stream=None) -> None:
+    _check(lib().w12_selftest_timeout(int(timeout_us), _stream_handle(stream)))
+
+
+def w12_last_error() -> str:
+    return lib().w12_last_error().decode()

@@ -1,0 +1,125 @@
+"""Host side of the library on CPU: the C ABI loads and exports every symbol
+include/w12.h declares; the library's encoder is byte-equal to the oracle's;
+header parsing and blob validation accept good blobs and reject bad ones."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from lossless_bit_weight_encode_gb300 import build as libbuild
+from lossless_bit_weight_encode_gb300 import w12
+from lossless_bit_weight_encode_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    libbuild.build()
+    oracle.build()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "w12.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w12_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = w12.lib()
+    declared = _declared_symbols()
+    assert len(declared) >= 12
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(w12.EXPORTED)
+    assert lib.w12_format_version() == 1
+    for code, name in w12.STATUS_NAMES.items():
+        assert lib.w12_status_string(code).decode() == name
+
+
+CASES = {
+    "exhaustive": lambda: wl.all_bf16_patterns(),
+    "exhaustive_shuffled": lambda: wl.all_bf16_patterns(77),
+    "single": lambda: wl.single_case()[0],
+    "ragged_small": lambda: wl.gaussian_weights(1, 1, seed=1),
+    "ragged": lambda: wl.gaussian_weights(333, 777, seed=2),
+    "heavy": lambda: wl.heavy_tail_weights(384, 2048, seed=3),
+    "forced2": lambda: wl.forced_escape_weights(256, 1024, 0.02, seed=4),
+    "forced10": lambda: wl.forced_escape_weights(130, 1000, 0.10, seed=5),
+    "forced100": lambda: wl.forced_escape_weights(128, 512, 1.0, seed=6),
+    "zeros": lambda: np.zeros((200, 300), dtype=np.uint16),
+    "big_exponents": lambda: (wl.gaussian_weights(256, 512, seed=7) | np.uint16(0x4000)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_encoder_is_byte_equal_to_oracle(case):
+    w = CASES[case]()
+    ref = oracle.encode(w)
+    assert w12.w12_encoded_size_host(w) == ref.size
+    blob = w12.w12_encode_host(w)
+    assert blob.size == ref.size
+    assert np.array_equal(blob, ref), f"first difference at byte {int(np.argmax(blob != ref))}"
+    w12.w12_blob_validate(blob)
+    assert np.array_equal(oracle.decode(blob), w)
+
+
+def test_blob_info_fields():
+    w = wl.heavy_tail_weights(300, 1000, seed=8)
+    blob = w12.w12_encode_host(w)
+    info = w12.w12_blob_info(blob)
+    assert (info.N, info.K, info.N_pad, info.K_pad) == (300, 1000, 384, 1024)
+    assert (info.tiles, info.chunks, info.segs) == (3, 32, 4)
+    assert info.off_seghdr == 256 and info.bytes_seghdr == 32 * 12
+    assert info.off_weights == 768 and info.bytes_weights == 6144 * 96  # 256 + 384 rounded up to 256
+    assert info.off_escapes == 768 + 6144 * 96
+    assert info.total_bytes == blob.size
+    assert info.bytes_escapes == -(-info.n_escapes // 16) * 16
+    assert abs(info.bits_per_weight - 8.0 * blob.size / (300 * 1000)) < 1e-12
+
+
+def _expect(status, fn, *args):
+    with pytest.raises(w12.W12Error) as ei:
+        fn(*args)
+    assert ei.value.status == status, str(ei.value)
+    assert w12.w12_last_error() != ""
+
+
+def test_rejects_bad_blobs():
+    w = wl.forced_escape_weights(256, 600, 0.05, seed=9)
+    blob = w12.w12_encode_host(w)
+    _expect(3, w12.w12_blob_info, blob[:100])          # shorter than the header
+    _expect(3, w12.w12_blob_info, blob[:-256])         # shorter than its total size
+    bad = blob.copy(); bad[1] ^= 1
+    _expect(5, w12.w12_blob_info, bad)                 # magic
+    bad = blob.copy(); bad[4] = 2
+    _expect(5, w12.w12_blob_info, bad)                 # version
+    bad = blob.copy(); bad[0x48] ^= 1
+    _expect(5, w12.w12_blob_info, bad)                 # chunk count
+    seg0 = 256
+    bad = blob.copy(); bad[seg0 + 15] = 3
+    _expect(5, w12.w12_blob_validate, bad)             # escape slot must hold 0
+    bad = blob.copy(); bad[seg0 + 0] ^= 0x80
+    _expect(5, w12.w12_blob_validate, bad)             # paired slots on different top bits
+    bad = blob.copy(); bad[seg0 + 32 + 16] ^= 1
+    _expect(5, w12.w12_blob_validate, bad)             # second segment's escape offset
+    bad = blob.copy(); bad[seg0 + 20] ^= 1
+    _expect(5, w12.w12_blob_validate, bad)             # quarter count
+    bad = blob.copy(); bad[seg0 + 28:seg0 + 32] = 0
+    _expect(5, w12.w12_blob_validate, bad)             # mask disagrees with the counts
+
+
+def test_host_argument_errors():
+    lib = w12.lib()
+    import ctypes
+    out = ctypes.c_size_t()
+    w = np.zeros((4, 4), dtype=np.uint16)
+    assert lib.w12_encoded_size_host(None, 4, 4, ctypes.byref(out)) == 1
+    assert lib.w12_encoded_size_host(w.ctypes.data, 0, 4, ctypes.byref(out)) == 2
+    assert lib.w12_encoded_size_host(w.ctypes.data, 4, -1, ctypes.byref(out)) == 2
+    size = w12.w12_encoded_size_host(w)
+    buf = np.empty(size, dtype=np.uint8)
+    assert lib.w12_encode_host(w.ctypes.data, 4, 4, buf.ctypes.data, size - 1) == 3
+    assert lib.w12_encode_host(w.ctypes.data, 4, 4, buf.ctypes.data, size) == 0
