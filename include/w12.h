@@ -134,6 +134,13 @@ int w12_decode(const void *blob_dev, const w12_info *info, uint16_t *w_out_dev, 
 int w12_gemm_workspace_size(const w12_info *info, int M, size_t *bytes);
 
 /*
+ * The launch plan w12_gemm uses for this blob and M on the current device:
+ * out[0] token tile of the MMA (16 or 32), out[1] CTAs per 128-row tile along
+ * K (split-K), out[2] total CTAs, out[3] resident CTAs per SM assumed.
+ */
+int w12_gemm_launch_info(const w12_info *info, int M, int32_t out[4]);
+
+/*
  * y_dev[m * N + n] = BF16_rne( sum_k x_dev[m * K + k] * W[n][k] ), fp32
  * accumulation, for 1 <= M <= 32, with W held by blob_dev.  The weights are
  * streamed from HBM in packed form and decoded in registers; tensor cores

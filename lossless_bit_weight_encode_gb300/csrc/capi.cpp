@@ -5,7 +5,7 @@
 #include <exception>
 #include <string>
 
-#include "../../include/w12.h"
+#include "w12.h"
 #include "w12_host.hpp"
 #include "w12_launch.hpp"
 
@@ -124,6 +124,26 @@ int w12_gemm_workspace_size(const w12_info *info, int M, size_t *bytes) {
         w12::launch::GemmPlan plan;
         rc = w12::launch::plan_gemm(*info, M, &plan, &err);
         if (rc == W12_OK) *bytes = plan.ws_bytes;
+        return rc;
+    });
+}
+
+int w12_gemm_launch_info(const w12_info *info, int M, int32_t out[4]) {
+    return guarded([&](std::string &err) {
+        int rc = check_info(info, err);
+        if (rc != W12_OK) return rc;
+        if (!out) {
+            err = "out is null";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        w12::launch::GemmPlan plan;
+        rc = w12::launch::plan_gemm(*info, M, &plan, &err);
+        if (rc == W12_OK) {
+            out[0] = plan.ntok;
+            out[1] = plan.splits;
+            out[2] = plan.ctas;
+            out[3] = plan.ctas_per_sm;
+        }
         return rc;
     });
 }

@@ -52,6 +52,7 @@ struct DeviceState {
     bool ready = false;
     int status_code = W12_OK;
     std::string error;
+    int device = 0;
     int sm_count = 0;
     uint32_t *status = nullptr;
     int occupancy[2][2] = {{0, 0}, {0, 0}};  // [ntok==32][a_smem]
@@ -79,9 +80,18 @@ int prepare_gemm(DeviceState &s, std::string *err) {
     void *k = gemm_kernel_ptr<NTOK, ASMEM>();
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm_smem_bytes<NTOK, ASMEM>());
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", err);
+    // all of the unified L1/shared storage as shared memory, so that several
+    // CTAs fit on an SM
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(carveout)", err);
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, 192, (size_t)gemm_smem_bytes<NTOK, ASMEM>());
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor", err);
+    // shared memory per SM bounds it as well (the query is not trusted alone)
+    int smem_sm = 0;
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, s.device);
+    const int by_smem = smem_sm / (gemm_smem_bytes<NTOK, ASMEM>() + 1024);
+    if (by_smem > occ) occ = by_smem;
     // TMEM: each CTA holds 128 of the SM's 512 columns
     s.occupancy[NTOK == 32][ASMEM] = occ < 4 ? occ : 4;
     return W12_OK;
@@ -99,6 +109,7 @@ int device_state(DeviceState **out, std::string *err) {
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState &s = g_state[dev];
     if (!s.ready) {
+        s.device = dev;
         int major = 0, minor = 0;
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
@@ -181,6 +192,7 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err) {
     }
     plan->splits = (int)splits;
     plan->ctas = (int)(tiles * splits);
+    plan->ctas_per_sm = occ;
     const int64_t k8 = (info.K + 7) / 8 * 8;
     plan->ws_counters = 0;
     plan->ws_partials = up256((size_t)tiles * 4);

@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <string>
 
-#include "../../include/w12.h"
+#include "w12.h"
 #include "w12_format.hpp"
 
 namespace w12 {

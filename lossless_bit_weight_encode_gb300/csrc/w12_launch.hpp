@@ -5,7 +5,7 @@
 #include <cstdint>
 #include <string>
 
-#include "../../include/w12.h"
+#include "w12.h"
 
 namespace w12 {
 namespace launch {
@@ -15,6 +15,7 @@ struct GemmPlan {
     int ntok = 16;          // MMA token width (16 or 32)
     int splits = 1;         // CTAs per tile along K
     int ctas = 0;           // grid size
+    int ctas_per_sm = 0;    // resident CTAs per SM the plan assumed
     size_t ws_counters = 0, ws_partials = 0, ws_x = 0;  // workspace offsets
     size_t ws_bytes = 0;
 };

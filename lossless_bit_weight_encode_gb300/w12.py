@@ -23,7 +23,8 @@ STATUS_NAMES = {
 }
 EXPORTED = (
     "w12_last_error", "w12_status_string", "w12_format_version", "w12_encoded_size_host", "w12_encode_host",
-    "w12_blob_info", "w12_blob_validate", "w12_decode", "w12_gemm_workspace_size", "w12_gemm",
+    "w12_blob_info", "w12_blob_validate", "w12_decode", "w12_gemm_workspace_size", "w12_gemm_launch_info",
+    "w12_gemm",
     "w12_check_status", "w12_selftest_timeout",
 )
 
@@ -73,6 +74,7 @@ def lib() -> ctypes.CDLL:
     L.w12_blob_validate.argtypes = [vp, sz]
     L.w12_decode.argtypes = [vp, ctypes.POINTER(w12_info), vp, vp]
     L.w12_gemm_workspace_size.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(sz)]
+    L.w12_gemm_launch_info.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(ctypes.c_int32)]
     L.w12_gemm.argtypes = [vp, vp, ctypes.POINTER(w12_info), vp, i32, vp, sz, vp]
     L.w12_check_status.argtypes = [vp]
     L.w12_selftest_timeout.argtypes = [ctypes.c_uint32, vp]
@@ -142,6 +144,12 @@ def w12_gemm_workspace_size(info: w12_info, M: int) -> int:
     out = ctypes.c_size_t()
     _check(lib().w12_gemm_workspace_size(ctypes.byref(info), int(M), ctypes.byref(out)))
     return out.value
+
+
+def w12_gemm_launch_info(info: w12_info, M: int) -> dict:
+    out = (ctypes.c_int32 * 4)()
+    _check(lib().w12_gemm_launch_info(ctypes.byref(info), int(M), out))
+    return {"ntok": out[0], "splits": out[1], "ctas": out[2], "ctas_per_sm": out[3]}
 
 
 def w12_gemm(x_dev, blob_dev, info: w12_info, y_dev, M: int, workspace, stream=None) -> None:

@@ -1,0 +1,168 @@
+"""GPU W12 GEMM through the C ABI against the fp64 oracle over the original
+BF16 weights: tolerance on every tested output, bit-exact where the arithmetic
+is exact (one-hot x, small integers), reproducible run to run, and the failure
+path (bounded wait -> W12_ERR_TIMEOUT) without a fault."""
+import numpy as np
+import pytest
+
+import oracle
+from lossless_bit_weight_encode_gb300 import W12Weight, w12
+from lossless_bit_weight_encode_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+A_OPERANDS = ["tmem", "smem"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from gpu_util import ensure_built
+    ensure_built()
+
+
+@pytest.fixture(params=A_OPERANDS)
+def a_operand(request, monkeypatch):
+    monkeypatch.setenv("W12_A_OPERAND", request.param)
+    return request.param
+
+
+def _gemm(mat, x_bits):
+    import torch
+    from gpu_util import dev_to_bits, to_dev_bf16
+    y = mat.gemm(to_dev_bf16(x_bits))
+    w12.w12_check_status()
+    torch.cuda.synchronize()
+    return dev_to_bits(y)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 16, 17, 31, 32])
+def test_small_gemm_all_m(M, a_operand):
+    from gpu_util import check_tolerance
+    w = wl.gaussian_weights(384, 2048, seed=M)
+    x = wl.activations(M, 2048, seed=100 + M)
+    mat = W12Weight(w)
+    check_tolerance(_gemm(mat, x), oracle.gemm_f64(x, w), f"M={M} {a_operand}")
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (1, 32), (129, 33), (300, 1000), (300, 1001), (130, 7000)])
+@pytest.mark.parametrize("M", [1, 5, 32])
+def test_ragged_gemm(shape, M):
+    from gpu_util import check_tolerance
+    n, k = shape
+    w = wl.heavy_tail_weights(n, k, seed=n + k)
+    x = wl.activations(M, k, seed=n * k + M)
+    check_tolerance(_gemm(W12Weight(w), x), oracle.gemm_f64(x, w), f"{shape} M={M}")
+
+
+@pytest.mark.parametrize("frac", [0.02, 0.10, 1.0])
+@pytest.mark.parametrize("M", [1, 16])
+def test_forced_escape_gemm(frac, M, a_operand):
+    from gpu_util import check_tolerance
+    w = wl.forced_escape_weights(256, 4096, frac, seed=int(frac * 1000) + M)
+    # huge exponents overflow the sum; keep the weights finite and moderate
+    e = (w >> 7) & 0xFF
+    w = np.where((e > 140) | (e == 255), (w & 0x807F) | np.uint16(130 << 7), w).astype(np.uint16)
+    x = wl.activations(M, 4096, seed=7 + M)
+    check_tolerance(_gemm(W12Weight(w), x), oracle.gemm_f64(x, w), f"escapes {frac} M={M}")
+
+
+def test_one_hot_is_exact(a_operand):
+    from gpu_util import bits_to_f64
+    w = wl.heavy_tail_weights(256, 1024, seed=11)
+    ks = [0, 1, 31, 32, 500, 1023]
+    x = np.zeros((len(ks), 1024), dtype=np.uint16)
+    for i, k in enumerate(ks):
+        x[i, k] = 0x3F80  # 1.0
+    y = bits_to_f64(_gemm(W12Weight(w), x))
+    for i, k in enumerate(ks):
+        assert np.array_equal(y[i], bits_to_f64(w[:, k])), f"column {k}"
+
+
+def test_small_integers_are_exact():
+    from gpu_util import bits_to_f64
+    rng = np.random.default_rng(12)
+    wi = rng.integers(-8, 9, (256, 1536)).astype(np.float32)
+    xi = rng.integers(-8, 9, (7, 1536)).astype(np.float32)
+    y = bits_to_f64(_gemm(W12Weight(wl.to_bf16_bits(wi)), wl.to_bf16_bits(xi)))
+    ref = (xi.astype(np.int64) @ wi.astype(np.int64).T).astype(np.float64)
+    ref_bf16 = bits_to_f64(wl.to_bf16_bits(ref.astype(np.float32)))
+    assert np.array_equal(y, ref_bf16)
+
+
+def test_reproducible_and_workspace_restored():
+    import torch
+    from gpu_util import dev_to_bits, to_dev_bf16
+    w = wl.gaussian_weights(1024, 17408, seed=13)
+    x = to_dev_bf16(wl.activations(16, 17408, seed=14))
+    mat = W12Weight(w)
+    y1 = dev_to_bits(mat.gemm(x))
+    ws = mat.workspace(16)
+    w12.w12_check_status()
+    tiles = int(mat.info.tiles)
+    assert int(ws[: tiles * 4].view(torch.int32).abs().sum().item()) == 0, "split-K counters not reset"
+    y2 = dev_to_bits(mat.gemm(x))
+    w12.w12_check_status()
+    assert np.array_equal(y1, y2)
+
+
+def test_unaligned_x_is_handled():
+    import torch
+    from gpu_util import check_tolerance, dev_to_bits, to_dev_bf16
+    w = wl.gaussian_weights(256, 1024, seed=15)
+    x = wl.activations(3, 1024, seed=16)
+    buf = torch.zeros(3 * 1024 + 1, dtype=torch.bfloat16, device="cuda")
+    xv = buf[1:].view(3, 1024)
+    xv.copy_(to_dev_bf16(x))
+    mat = W12Weight(w)
+    y = torch.empty((3, 256), dtype=torch.bfloat16, device="cuda")
+    w12.w12_gemm(xv, mat.blob, mat.info, y, 3, mat.workspace(3))
+    w12.w12_check_status()
+    check_tolerance(dev_to_bits(y), oracle.gemm_f64(x, w), "unaligned x")
+
+
+def test_argument_errors():
+    import torch
+    w = wl.gaussian_weights(128, 256, seed=17)
+    mat = W12Weight(w)
+    x = torch.zeros((33, 256), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((33, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(w12.W12Error) as ei:
+        w12.w12_gemm(x, mat.blob, mat.info, y, 33, mat.workspace(1))
+    assert ei.value.status == 1
+    # workspace too small: rejected on the host before any launch
+    big = W12Weight(wl.gaussian_weights(128, 8192, seed=18))
+    xb = torch.zeros((1, 8192), dtype=torch.bfloat16, device="cuda")
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    assert w12.w12_gemm_workspace_size(big.info, 1) > 256
+    with pytest.raises(w12.W12Error) as ei:
+        w12.w12_gemm(xb, big.blob, big.info, y[:1], 1, small)
+    assert ei.value.status == 3
+    bad_blob = torch.zeros(mat.blob.numel() + 16, dtype=torch.uint8, device="cuda")[16:]
+    with pytest.raises(w12.W12Error) as ei:
+        w12.w12_gemm(x[:1], bad_blob, mat.info, y[:1], 1, mat.workspace(1))
+    assert ei.value.status == 4
+
+
+def test_bounded_wait_reports_timeout():
+    w12.w12_check_status()
+    w12.w12_selftest_timeout(2000)
+    with pytest.raises(w12.W12Error) as ei:
+        w12.w12_check_status()
+    assert ei.value.status == 8
+    w12.w12_check_status()  # cleared; the context is still usable
+
+
+@pytest.mark.parametrize("workload,Ms", [("layer", (1, 2, 4, 8, 16, 32)), ("heavy", (1, 16))])
+def test_layer_shapes_sampled_rows(workload, Ms):
+    """Every layer matrix at full size, in the launch configuration the
+    benchmark uses; the oracle checks 512 seeded rows of y per matrix and M."""
+    from gpu_util import check_tolerance
+    rng = np.random.default_rng(19)
+    for name, w in wl.layer_weights(workload):
+        mat = W12Weight(w)
+        rows = np.sort(rng.choice(w.shape[0], size=512, replace=False))
+        for M in Ms:
+            x = wl.activations(M, w.shape[1], seed=wl.activation_seed(workload, M))
+            y = _gemm(mat, x)
+            ref = oracle.gemm_f64(x, np.ascontiguousarray(w[rows]))
+            check_tolerance(y[:, rows], ref, f"{workload} {name} M={M}")
