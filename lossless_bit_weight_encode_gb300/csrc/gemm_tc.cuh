@@ -13,18 +13,26 @@
 // owns one tile and a range of whole segments along K (split-K); partial sums
 // go to an fp32 workspace and the last CTA of a tile adds them in split order.
 //
-// Warp roles (192 threads):
-//   warps 0-3  decode: warp q handles rows 32q..32q+31 (TMEM lanes of quarter
-//              q); per chunk it reads 48 B per row from SMEM, decodes 32
-//              weights per thread, patches escapes, stores 16 columns of BF16
-//              pairs into a TMEM A slot (or SMEM A slot), and later runs the
-//              epilogue;
-//   warp 4     producer: one lane issues cp.async.bulk for the segment
-//              headers, for every stage of 2 packed chunks (12 KB) and for each
-//              segment's escape bytes, plus cp.async.bulk.tensor for the
-//              stage's 64-column x tile (128-byte swizzle);
-//   warp 5     allocates TMEM; one lane issues tcgen05.mma (2 per chunk) and
+// Warp roles (320 threads):
+//   warps 0-7  decode: warp w handles rows 32q..32q+31 (q = w mod 4, the TMEM
+//              lanes of quarter q) and columns 16h..16h+15 of every chunk
+//              (h = w / 4); per weight stage (2 chunks) a thread reads its
+//              row's S bytes and codes from SMEM, decodes 2 x 16 weights,
+//              patches escapes and stores 2 x 8 columns of BF16 pairs into a
+//              TMEM A slot (or SMEM A slot); one handshake with the MMA warp
+//              per stage; afterwards the warp runs the epilogue for half of
+//              the token columns;
+//   warp 8     producer: one lane issues cp.async.bulk for the segment
+//              headers and for every weight stage (2 packed chunks, 12 KB), and
+//              per segment cp.async.bulk.tensor for the segment's 256-column x
+//              tile (four 64-column boxes, 128-byte swizzle) plus
+//              cp.async.bulk for the segment's escape bytes;
+//   warp 9     allocates TMEM; one lane issues tcgen05.mma (2 per chunk) and
 //              tcgen05.commit.
+// Rings: weight stages are released by the decode warps as soon as they have
+// read them (no MMA latency in that loop); the per-segment x tile and escape
+// bytes are released when the segment's MMAs have completed and its decoders
+// are done.  Waits are made by one lane per warp; __syncwarp orders the rest.
 // Every wait is bounded (deadline from %globaltimer); on expiry the kernel
 // records W12_ERR_TIMEOUT in the status word, lets in-flight copies land and
 // MMAs finish, frees TMEM and returns.
@@ -56,59 +64,50 @@ struct GemmParams {
 
 template <int NTOK, int STAGES, bool A_SMEM>
 struct GemmCfg {
-    static constexpr int kThreads = 192;
+    static constexpr int kThreads = 320;
+    static constexpr int kDecWarps = 8;
     static constexpr int kStages = STAGES;
     static constexpr bool kASmem = A_SMEM;
     static constexpr int kNtok = NTOK;
-    static constexpr int kStageChunks = 2;
-    static constexpr int kWBytes = kStageChunks * kChunkBytes;  // 12288
-    static constexpr int kXBytes = NTOK * 64 * 2;               // NTOK rows x 64 columns BF16
-    static constexpr int kStageBytes = kWBytes + kXBytes;       // multiple of 1024
-    static constexpr int kASlots = 4;
-    static constexpr int kASlotBytes = kTileRows * kChunkK * 2;  // 8 KB (SMEM A variant)
-    static constexpr int kEscSlots = 2;
+    static constexpr int kWBytes = 2 * kChunkBytes;             // weight stage: 2 chunks
+    static constexpr int kXBoxBytes = NTOK * 128;               // one 64-column x box
+    static constexpr int kXBytes = 4 * kXBoxBytes;              // x tile of one segment
+    static constexpr int kSegSlots = 2;                         // x + escapes per segment
+    static constexpr int kASlots = 3;                             // one weight stage (2 chunks) each
+    static constexpr int kASlotBytes = 2 * kTileRows * kChunkK * 2;  // 16 KB (SMEM A variant)
+    static constexpr int kAChunkBytes = kTileRows * kChunkK * 2;     // 8 KB per chunk
     static constexpr int kEscCap = 2048;
     static constexpr int kMaxSegs = 96;   // segments per CTA (K range <= 24576)
     static constexpr int kTmemCols = 128;
     static constexpr int kDCol = 0;
     static constexpr int kACol = 32;
-    static constexpr int kOffStages = 0;
-    static constexpr int kOffA = kOffStages + STAGES * kStageBytes;
+    static constexpr int kOffX = 0;                                         // 1024-aligned
+    static constexpr int kOffW = kOffX + kSegSlots * kXBytes;
+    static constexpr int kOffA = kOffW + STAGES * kWBytes;
     static constexpr int kOffEsc = kOffA + (A_SMEM ? kASlots * kASlotBytes : 0);
-    static constexpr int kOffHdr = kOffEsc + kEscSlots * kEscCap;
+    static constexpr int kOffHdr = kOffEsc + kSegSlots * kEscCap;
     static constexpr int kOffBars = kOffHdr + kMaxSegs * kSegHdrBytes;
-    // full[S], empty[S], afull[4], aempty[4], escfull[2], escempty[2], hdr, accum, drain,
-    // epi_in (partials written), epi_out (arrival counted)
-    static constexpr int kNumBars = 2 * STAGES + 2 * kASlots + 2 * kEscSlots + 5;
+    // wfull[S], wempty[S], sfull[2], sempty[2], afull[4], aempty[4],
+    // hdr, accum, drain, epi_in, epi_out
+    static constexpr int kNumBars = 2 * STAGES + 2 * kSegSlots + 2 * kASlots + 5;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024
-    static_assert(kStageBytes % 1024 == 0, "x tiles must stay 1024-byte aligned for the 128-byte swizzle");
+    static_assert(kXBoxBytes % 1024 == 0, "x boxes must stay 1024-byte aligned for the 128-byte swizzle");
     static_assert(NTOK == 16 || NTOK == 32, "token tile is 16 or 32");
 };
 
 struct Bars {
-    uint64_t *full, *empty, *afull, *aempty, *escfull, *escempty, *hdr, *accum, *drain, *epi_in, *epi_out;
+    uint64_t *wfull, *wempty, *sfull, *sempty, *afull, *aempty, *hdr, *accum, *drain, *epi_in, *epi_out;
 };
 
-// Wait by lane 0 with a deadline, result broadcast to the warp; on success
-// every lane then observes the completed phase itself.
+// One lane waits (bounded); the result is broadcast and __syncwarp orders the
+// other lanes after the completed phase.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t deadline) {
-    const uint32_t lane = threadIdx.x & 31u;
     uint32_t ok = 0;
-    if (lane == 0) ok = mbar_wait(bar, parity, deadline) ? 1u : 0u;
+    if ((threadIdx.x & 31u) == 0) ok = mbar_wait(bar, parity, deadline) ? 1u : 0u;
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    // The phase cannot move on before this warp arrives elsewhere, so the
-    // other lanes' checks succeed at once; the bound is only a safeguard.
-    for (int i = 0; ok && i < (1 << 20) && !mbar_try_wait(bar, parity); ++i) {
-    }
+    __syncwarp();
     return ok != 0;
-}
-
-// The abort flag as lane 0 sees it, so that a warp always decides as one.
-__device__ __forceinline__ bool warp_aborted(volatile uint32_t *abort_flag) {
-    uint32_t a = 0;
-    if ((threadIdx.x & 31u) == 0) a = *abort_flag;
-    return __shfl_sync(0xFFFFFFFFu, a, 0) != 0;
 }
 
 __device__ __forceinline__ void raise_timeout(uint32_t *status, volatile uint32_t *abort_flag) {
@@ -120,119 +119,136 @@ __device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+__device__ __forceinline__ uint32_t seg_escape_total(const uint4 &meta) {
+    return (meta.y & 0xFFFFu) + (meta.y >> 16) + (meta.z & 0xFFFFu) + (meta.z >> 16);
+}
+
+template <class C>
+__device__ __forceinline__ bool escapes_staged(uint32_t total) {
+    return total > 0 && total + 30u <= (uint32_t)C::kEscCap;
+}
+
 // ------------------------------------------------------------------ producer
 template <class C>
 __device__ void gemm_producer(const GemmParams &p, const CUtensorMap *tmap, uint8_t *smem, const Bars &b,
                               volatile uint32_t *abort_flag, int64_t tile, int s0, int c0, int c1,
                               uint64_t deadline) {
-    const int nsegs_cta = (c1 - c0 + kChunksPerSeg - 1) / kChunksPerSeg;
     const int nchunks = c1 - c0;
+    const int nsegs_cta = (nchunks + kChunksPerSeg - 1) / kChunksPerSeg;
     const int nstages = (nchunks + 1) / 2;
     uint8_t *hdr = smem + C::kOffHdr;
     prefetch_tmap(tmap);
 
-    // this CTA's segment headers, one copy
     const uint32_t hbytes = (uint32_t)nsegs_cta * kSegHdrBytes;
     mbar_arrive_expect_tx(b.hdr, hbytes);
     bulk_g2s(hdr, p.blob + p.off_seg + (uint64_t)(tile * p.segs + s0) * kSegHdrBytes, hbytes, b.hdr);
     bool hdr_ready = false;
-    int issued = 0, esc_issued = 0;
+    int issued = 0, seg_issued = 0;
     bool failed = false;
 
     for (int st = 0; st < nstages; ++st) {
-        if (*abort_flag) break;
         const int chunk = c0 + 2 * st;
         if ((chunk & (kChunksPerSeg - 1)) == 0) {
-            // first stage of a segment: stage its escape bytes
+            // a segment starts: its x tile and its escape bytes
             const int ls = chunk / kChunksPerSeg - s0;
-            const int eslot = ls & 1;
+            const int sslot = ls & 1;
             if (!hdr_ready) {
                 if (!mbar_wait(b.hdr, 0, deadline)) { failed = true; break; }
                 hdr_ready = true;
             }
-            if (ls >= 2 && !mbar_wait(b.escempty + eslot, (uint32_t)((ls >> 1) - 1) & 1u, deadline)) {
+            if (ls >= 2 && !mbar_wait(b.sempty + sslot, (uint32_t)((ls >> 1) - 1) & 1u, deadline)) {
                 failed = true;
                 break;
             }
             const uint4 meta = *reinterpret_cast<const uint4 *>(hdr + ls * kSegHdrBytes + 16);
             const uint32_t base = meta.x;
-            const uint32_t total = (meta.y & 0xFFFFu) + (meta.y >> 16) + (meta.z & 0xFFFFu) + (meta.z >> 16);
-            if (total > 0 && total + 30u <= (uint32_t)C::kEscCap) {
-                const uint32_t src0 = base & ~15u;
-                const uint32_t bytes = ((base + total + 15u) & ~15u) - src0;
-                mbar_arrive_expect_tx(b.escfull + eslot, bytes);
-                bulk_g2s(smem + C::kOffEsc + eslot * C::kEscCap, p.blob + p.off_esc + src0, bytes, b.escfull + eslot);
-            } else {
-                mbar_arrive(b.escfull + eslot);  // nothing to stage (none, or read from global)
+            const uint32_t total = seg_escape_total(meta);
+            uint32_t ebytes = 0, src0 = 0;
+            if (escapes_staged<C>(total)) {
+                src0 = base & ~15u;
+                ebytes = ((base + total + 15u) & ~15u) - src0;
             }
-            esc_issued = ls + 1;
+            mbar_arrive_expect_tx(b.sfull + sslot, (uint32_t)C::kXBytes + ebytes);
+            uint8_t *xs = smem + C::kOffX + sslot * C::kXBytes;
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx)
+                tma_load_2d(xs + bx * C::kXBoxBytes, tmap, chunk * kChunkK + bx * 64, 0, b.sfull + sslot);
+            if (ebytes)
+                bulk_g2s(smem + C::kOffEsc + sslot * C::kEscCap, p.blob + p.off_esc + src0, ebytes, b.sfull + sslot);
+            seg_issued = ls + 1;
         }
         const int slot = st % C::kStages;
         if (st >= C::kStages &&
-            !mbar_wait(b.empty + slot, (uint32_t)(st / C::kStages - 1) & 1u, deadline)) {
+            !mbar_wait(b.wempty + slot, (uint32_t)(st / C::kStages - 1) & 1u, deadline)) {
             failed = true;
             break;
         }
         const int nch = min(2, c1 - chunk);
-        uint8_t *stage = smem + C::kOffStages + slot * C::kStageBytes;
-        mbar_arrive_expect_tx(b.full + slot, (uint32_t)(nch * kChunkBytes + C::kXBytes));
-        bulk_g2s(stage, p.blob + p.off_w + (uint64_t)(tile * p.chunks + chunk) * kChunkBytes,
-                 (uint32_t)(nch * kChunkBytes), b.full + slot);
-        tma_load_2d(stage + C::kWBytes, tmap, chunk * kChunkK, 0, b.full + slot);
+        mbar_arrive_expect_tx(b.wfull + slot, (uint32_t)(nch * kChunkBytes));
+        bulk_g2s(smem + C::kOffW + slot * C::kWBytes,
+                 p.blob + p.off_w + (uint64_t)(tile * p.chunks + chunk) * kChunkBytes, (uint32_t)(nch * kChunkBytes),
+                 b.wfull + slot);
         issued = st + 1;
+        if (*abort_flag) break;
     }
     if (failed) raise_timeout(p.status, abort_flag);
     if (*abort_flag) {
         // let every copy still in flight land before the CTA can exit
         const uint64_t drain_deadline = globaltimer_ns() + 1000000000ull;
         for (int st = max(0, issued - C::kStages); st < issued; ++st)
-            mbar_wait(b.full + st % C::kStages, (uint32_t)(st / C::kStages) & 1u, drain_deadline);
-        for (int ls = max(0, esc_issued - 2); ls < esc_issued; ++ls)
-            mbar_wait(b.escfull + (ls & 1), (uint32_t)(ls >> 1) & 1u, drain_deadline);
+            mbar_wait(b.wfull + st % C::kStages, (uint32_t)(st / C::kStages) & 1u, drain_deadline);
+        for (int ls = max(0, seg_issued - 2); ls < seg_issued; ++ls)
+            mbar_wait(b.sfull + (ls & 1), (uint32_t)(ls >> 1) & 1u, drain_deadline);
         mbar_wait(b.hdr, 0, drain_deadline);
     }
 }
 
 // ------------------------------------------------------------------ MMA issuer
-// A chunk of 32 columns is two MMAs of K = 16.  B (x) sits in the stage's
-// 128-byte-swizzled tile: K-major, rows of 128 bytes, 8-row atoms of 1024 B;
-// the MMA for columns 16u..16u+15 of the stage starts 32u bytes into it.
+// A chunk of 32 columns is two MMAs of K = 16.  B (x) sits in the segment's
+// x tile: four 128-byte-swizzled boxes of 64 columns, K-major, 8-row atoms of
+// 1024 B; columns 16u..16u+15 of a box start 32u bytes into it.
 template <class C>
 __device__ void gemm_mma(const GemmParams &p, uint8_t *smem, const Bars &b, volatile uint32_t *abort_flag,
-                         uint32_t tmem_base, int nchunks, uint64_t deadline) {
+                         uint32_t tmem_base, int c0, int nchunks, uint64_t deadline) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, C::kNtok);
+    const int nstages = (nchunks + 1) / 2;
     bool failed = false;
-    int i = 0;
-    for (; i < nchunks; ++i) {
-        if (*abort_flag) break;
-        const int st = i >> 1, slot = st % C::kStages;
-        if ((i & 1) == 0 && !mbar_wait(b.full + slot, (uint32_t)(st / C::kStages) & 1u, deadline)) {
-            failed = true;
-            break;
+    uint32_t xs = 0;
+    for (int st = 0; st < nstages; ++st) {
+        const int chunk0 = c0 + 2 * st;
+        const int jj0 = chunk0 & (kChunksPerSeg - 1);
+        const int ls = st / (kChunksPerSeg / 2);
+        const int nch = min(2, c0 + nchunks - chunk0);
+        if (jj0 == 0) {
+            if (!mbar_wait(b.sfull + (ls & 1), (uint32_t)(ls >> 1) & 1u, deadline)) { failed = true; break; }
+            xs = smem_u32(smem + C::kOffX + (ls & 1) * C::kXBytes);
         }
-        const int aslot = i % C::kASlots;
-        if (!mbar_wait(b.afull + aslot, (uint32_t)(i / C::kASlots) & 1u, deadline)) {
-            failed = true;
-            break;
-        }
+        const int aslot = st % C::kASlots;
+        if (!mbar_wait(b.afull + aslot, (uint32_t)(st / C::kASlots) & 1u, deadline)) { failed = true; break; }
         tc_fence_after();
-        const uint32_t xs = smem_u32(smem + C::kOffStages + slot * C::kStageBytes + C::kWBytes);
+        for (int e = 0; e < nch; ++e) {
+            const int jj = jj0 + e;
+            const uint32_t xbox = xs + (uint32_t)(jj >> 1) * C::kXBoxBytes + (uint32_t)(jj & 1) * 64u;
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t bdesc = smem_desc(xs + (uint32_t)((i & 1) * 2 + kk) * 32u, 16u, 1024u, 2u);
-            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-            if constexpr (C::kASmem) {
-                // K-major, no swizzle: 8x16-byte core matrices, 128 B apart
-                // along K, 512 B apart along rows; MMA kk starts 256 B in.
-                const uint32_t as = smem_u32(smem + C::kOffA + aslot * C::kASlotBytes) + (uint32_t)kk * 256u;
-                mma_smem_a(tmem_base + C::kDCol, smem_desc(as, 128u, 512u, 0u), bdesc, idesc, acc);
-            } else {
-                mma_tmem_a(tmem_base + C::kDCol, tmem_base + C::kACol + (uint32_t)(16 * aslot + 8 * kk), bdesc,
-                           idesc, acc);
+            for (int kk = 0; kk < 2; ++kk) {
+                const uint64_t bdesc = smem_desc(xbox + (uint32_t)kk * 32u, 16u, 1024u, 2u);
+                const uint32_t acc = (st > 0 || e > 0 || kk > 0) ? 1u : 0u;
+                if constexpr (C::kASmem) {
+                    // K-major, no swizzle: 8x16-byte core matrices, 128 B apart
+                    // along K, 512 B apart along rows; MMA kk starts 256 B in.
+                    const uint32_t as = smem_u32(smem + C::kOffA + aslot * C::kASlotBytes + e * C::kAChunkBytes) +
+                                        (uint32_t)kk * 256u;
+                    mma_smem_a(tmem_base + C::kDCol, smem_desc(as, 128u, 512u, 0u), bdesc, idesc, acc);
+                } else {
+                    // slot columns: [k-half kk][chunk e] x 8 (one decode warp's 16 columns are contiguous)
+                    mma_tmem_a(tmem_base + C::kDCol,
+                               tmem_base + C::kACol + (uint32_t)(32 * aslot + 16 * kk + 8 * e), bdesc, idesc, acc);
+                }
             }
         }
         mma_commit(b.aempty + aslot);
-        if ((i & 1) == 1 || i == nchunks - 1) mma_commit(b.empty + slot);
+        if (jj0 + nch == kChunksPerSeg || st == nstages - 1) mma_commit(b.sempty + (ls & 1));
+        if (*abort_flag) break;
     }
     if (failed) raise_timeout(p.status, abort_flag);
     mma_commit(b.accum);  // also fires when nothing was issued
@@ -242,15 +258,31 @@ __device__ void gemm_mma(const GemmParams &p, uint8_t *smem, const Bars &b, vola
 }
 
 // ------------------------------------------------------------------ decoders
+// One chunk's half-row: decode 16 weights of row r, columns 16h..16h+15.
+__device__ __forceinline__ void decode_half_chunk(const Table &T, const uint4 &sb, const uint4 &codes, int h,
+                                                  bool has_escapes, const uint8_t *&run, uint32_t (&out)[8]) {
+    uint32_t E[4];
+    decode_exponents_half(T, h ? codes.z : codes.x, h ? codes.w : codes.y, E);
+    if (has_escapes) run += warp_escapes_half(codes, h, run, E);
+    assemble_half(sb, E, out);
+}
+
 template <class C>
 __device__ void gemm_decode(const GemmParams &p, uint8_t *smem, const Bars &b, volatile uint32_t *abort_flag,
                             uint32_t tmem_base, int s0, int c0, int c1, uint64_t deadline) {
-    const int q = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int q = warp & 3;       // TMEM lane quarter = rows 32q..32q+31
+    const int h = warp >> 2;      // columns 16h..16h+15 of each chunk
     const int lane = threadIdx.x & 31;
-    const int r = threadIdx.x;  // row in the tile
+    const int r = 32 * q + lane;  // row in the tile
     const int nchunks = c1 - c0;
+    const int nstages = (nchunks + 1) / 2;
     const uint8_t *hdr = smem + C::kOffHdr;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    // this thread's S bytes (half h of its row) in weight stage 0; codes are
+    // c_off further on
+    const uint32_t s_row = smem_u32(smem + C::kOffW) + (uint32_t)(h * kSlabBytes + 16 * r);
+    const uint32_t c_off = (uint32_t)((2 - h) * kSlabBytes);
 
     if (!warp_wait(b.hdr, 0, deadline)) {
         if (lane == 0) raise_timeout(p.status, abort_flag);
@@ -259,72 +291,118 @@ __device__ void gemm_decode(const GemmParams &p, uint8_t *smem, const Bars &b, v
     Table T{};
     uint32_t mask_q = 0;
     const uint8_t *run = nullptr;
-    int eslot = 0;
-    for (int i = 0; i < nchunks; ++i) {
-        if (warp_aborted(abort_flag)) return;
-        const int chunk = c0 + i;
-        const int jj = chunk & (kChunksPerSeg - 1);
-        if (jj == 0) {
-            const int ls = chunk / kChunksPerSeg - s0;
-            const uint8_t *h = hdr + ls * kSegHdrBytes;
-            T = make_table(*reinterpret_cast<const uint4 *>(h));
-            const uint4 meta = *reinterpret_cast<const uint4 *>(h + 16);
-            const uint32_t qc0 = meta.y & 0xFFFFu, qc1 = meta.y >> 16, qc2 = meta.z & 0xFFFFu, qc3 = meta.z >> 16;
-            const uint32_t total = qc0 + qc1 + qc2 + qc3;
+    // The handshake for stage st (wait for its TMEM stores, tell the MMA warp)
+    // is made one stage later, so that the store latency overlaps the next
+    // stage's decode.
+    int pend_slot = -1;
+    bool pend_seg_end = false;
+    int pend_ls = 0;
+    for (int st = 0; st < nstages; ++st) {
+        const int chunk0 = c0 + 2 * st;
+        const int jj0 = chunk0 & (kChunksPerSeg - 1);
+        const int ls = st / (kChunksPerSeg / 2);
+        const int nch = min(2, c1 - chunk0);
+        if (jj0 == 0) {
+            const uint8_t *hp = hdr + (chunk0 / kChunksPerSeg - s0) * kSegHdrBytes;
+            T = make_table(*reinterpret_cast<const uint4 *>(hp));
+            const uint4 meta = *reinterpret_cast<const uint4 *>(hp + 16);
+            const uint32_t qc0 = meta.y & 0xFFFFu, qc1 = meta.y >> 16, qc2 = meta.z & 0xFFFFu;
             const uint32_t qoff = (q > 0 ? qc0 : 0u) + (q > 1 ? qc1 : 0u) + (q > 2 ? qc2 : 0u);
             mask_q = (meta.w >> (8 * q)) & 0xFFu;
-            eslot = ls & 1;
-            if (!warp_wait(b.escfull + eslot, (uint32_t)(ls >> 1) & 1u, deadline)) {
+            if (!warp_wait(b.sfull + (ls & 1), (uint32_t)(ls >> 1) & 1u, deadline)) {
                 if (lane == 0) raise_timeout(p.status, abort_flag);
                 return;
             }
-            if (total > 0 && total + 30u <= (uint32_t)C::kEscCap)
-                run = smem + C::kOffEsc + eslot * C::kEscCap + (meta.x & 15u) + qoff;
+            if (escapes_staged<C>(seg_escape_total(meta)))
+                run = smem + C::kOffEsc + (ls & 1) * C::kEscCap + (meta.x & 15u) + qoff;
             else
                 run = p.blob + p.off_esc + meta.x + qoff;
         }
-        const int st = i >> 1, slot = st % C::kStages;
-        if ((i & 1) == 0 && !warp_wait(b.full + slot, (uint32_t)(st / C::kStages) & 1u, deadline)) {
+        const int slot = st % C::kStages;
+        if (!warp_wait(b.wfull + slot, (uint32_t)(st / C::kStages) & 1u, deadline)) {
             if (lane == 0) raise_timeout(p.status, abort_flag);
             return;
         }
-        const uint8_t *cp = smem + C::kOffStages + slot * C::kStageBytes + (i & 1) * kChunkBytes;
-        const uint4 s_lo = *reinterpret_cast<const uint4 *>(cp + 16 * r);
-        const uint4 s_hi = *reinterpret_cast<const uint4 *>(cp + kSlabBytes + 16 * r);
-        const uint4 codes = *reinterpret_cast<const uint4 *>(cp + 2 * kSlabBytes + 16 * r);
-        if ((i & 1) == 1 || i == nchunks - 1) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b.empty + slot);  // this warp is done with the stage's bytes
+        const uint32_t sa = s_row + (uint32_t)(slot * C::kWBytes);
+        const uint4 sb0 = lds128(sa);
+        const uint4 cd0 = lds128(sa + c_off);
+        uint4 sb1 = make_uint4(0, 0, 0, 0), cd1 = make_uint4(0, 0, 0, 0);
+        if (nch == 2) {
+            sb1 = lds128(sa + kChunkBytes);
+            cd1 = lds128(sa + kChunkBytes + c_off);
         }
-        uint32_t E[8];
-        decode_exponents(T, codes, E);
-        if ((mask_q >> jj) & 1u) run += warp_escapes(codes, run, E);
-        uint32_t out[16];
-        assemble(s_lo, s_hi, E, out);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b.wempty + slot);  // this warp is done with the stage's bytes
 
-        const int aslot = i % C::kASlots;
-        if (i >= C::kASlots &&
-            !warp_wait(b.aempty + aslot, (uint32_t)(i / C::kASlots - 1) & 1u, deadline)) {
+        uint32_t out0[8], out1[8];
+        decode_half_chunk(T, sb0, cd0, h, (mask_q >> jj0) & 1u, run, out0);
+        if (nch == 2) {
+            decode_half_chunk(T, sb1, cd1, h, (mask_q >> (jj0 + 1)) & 1u, run, out1);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) out1[i] = 0u;
+        }
+
+        if constexpr (!C::kASmem) {
+            if (pend_slot >= 0) {
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(b.afull + pend_slot);
+                    if (pend_seg_end) mbar_arrive(b.sempty + (pend_ls & 1));
+                }
+                pend_slot = -1;
+            }
+        }
+        const int aslot = st % C::kASlots;
+        if (st >= C::kASlots &&
+            !warp_wait(b.aempty + aslot, (uint32_t)(st / C::kASlots - 1) & 1u, deadline)) {
             if (lane == 0) raise_timeout(p.status, abort_flag);
             return;
         }
         if constexpr (C::kASmem) {
-            uint8_t *ap = smem + C::kOffA + aslot * C::kASlotBytes + (r >> 3) * 512 + (r & 7) * 16;
+            uint8_t *ap = smem + C::kOffA + aslot * C::kASlotBytes + (r >> 3) * 512 + (r & 7) * 16 + h * 256;
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
+            for (int g = 0; g < 2; ++g)
                 *reinterpret_cast<uint4 *>(ap + g * 128) =
-                    make_uint4(out[4 * g], out[4 * g + 1], out[4 * g + 2], out[4 * g + 3]);
+                    make_uint4(out0[4 * g], out0[4 * g + 1], out0[4 * g + 2], out0[4 * g + 3]);
+            if (nch == 2) {
+#pragma unroll
+                for (int g = 0; g < 2; ++g)
+                    *reinterpret_cast<uint4 *>(ap + C::kAChunkBytes + g * 128) =
+                        make_uint4(out1[4 * g], out1[4 * g + 1], out1[4 * g + 2], out1[4 * g + 3]);
+            }
             fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(b.afull + aslot);
+                if (jj0 + nch == kChunksPerSeg || st == nstages - 1) mbar_arrive(b.sempty + (ls & 1));
+            }
         } else {
             tc_fence_after();
-            tmem_st16(tmem_base + lane_base + (uint32_t)(C::kACol + 16 * aslot), out);
+            const uint32_t ta = tmem_base + lane_base + (uint32_t)(C::kACol + 32 * aslot + 16 * h);
+            uint32_t v[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[i] = out0[i];
+                v[8 + i] = out1[i];  // a short last stage leaves these columns unread
+            }
+            tmem_st16(ta, v);
+            pend_slot = aslot;
+            pend_seg_end = (jj0 + nch == kChunksPerSeg || st == nstages - 1);
+            pend_ls = ls;
+        }
+    }
+    if constexpr (!C::kASmem) {
+        if (pend_slot >= 0) {
             tmem_wait_st();
             tc_fence_before();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b.afull + aslot);
-        if (jj == kChunksPerSeg - 1 || i == nchunks - 1) {
-            if (lane == 0) mbar_arrive(b.escempty + eslot);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(b.afull + pend_slot);
+                if (pend_seg_end) mbar_arrive(b.sempty + (pend_ls & 1));
+            }
         }
     }
 }
@@ -336,43 +414,49 @@ template <class C>
 __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint32_t *abort_flag,
                               volatile uint32_t *last_flag, uint32_t tmem_base, int64_t tile, int split,
                               uint64_t deadline) {
-    const int q = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int q = warp & 3;
+    const int h = warp >> 2;
     const int lane = threadIdx.x & 31;
-    if (warp_aborted(abort_flag)) return;
+    constexpr int kHalf = C::kNtok / 2;  // this warp's tokens: h*kHalf .. h*kHalf + kHalf - 1
+    const int m0 = h * kHalf;
     if (!warp_wait(b.accum, 0, deadline)) {
         if (lane == 0) raise_timeout(p.status, abort_flag);
         return;
     }
     tc_fence_after();
-    float acc[C::kNtok];
+    float acc[kHalf];
     {
-        uint32_t v[16];
-        tmem_ld16(tmem_base + ((uint32_t)(32 * q) << 16) + C::kDCol, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int m = 0; m < 16; ++m) acc[m] = __uint_as_float(v[m]);
-        if constexpr (C::kNtok == 32) {
-            tmem_ld16(tmem_base + ((uint32_t)(32 * q) << 16) + C::kDCol + 16u, v);
+        const uint32_t ta = tmem_base + ((uint32_t)(32 * q) << 16) + C::kDCol + (uint32_t)m0;
+        if constexpr (kHalf == 8) {
+            uint32_t v[8];
+            tmem_ld8(ta, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc[16 + m] = __uint_as_float(v[m]);
+            for (int m = 0; m < 8; ++m) acc[m] = __uint_as_float(v[m]);
+        } else {
+            uint32_t v[16];
+            tmem_ld16(ta, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc[m] = __uint_as_float(v[m]);
         }
     }
     const int64_t n = tile * kTileRows + 32 * q + lane;
     if (p.splits == 1) {
         if (n < p.N) {
 #pragma unroll
-            for (int m = 0; m < C::kNtok; ++m)
-                if (m < p.M) p.y[(int64_t)m * p.N + n] = bf16_bits_rn(acc[m]);
+            for (int m = 0; m < kHalf; ++m)
+                if (m0 + m < p.M) p.y[(int64_t)(m0 + m) * p.N + n] = bf16_bits_rn(acc[m]);
         }
         return;
     }
     float *part = p.partials + (int64_t)split * p.M * p.Npad + n;
 #pragma unroll
-    for (int m = 0; m < C::kNtok; ++m)
-        if (m < p.M) __stcg(part + (int64_t)m * p.Npad, acc[m]);
+    for (int m = 0; m < kHalf; ++m)
+        if (m0 + m < p.M) __stcg(part + (int64_t)(m0 + m) * p.Npad, acc[m]);
     __threadfence();
-    // the four decode warps meet on mbarriers (bounded waits, no bar.sync that
+    // the decode warps meet on mbarriers (bounded waits, no bar.sync that
     // a warp which gave up could leave the others stuck in)
     __syncwarp();
     if (lane == 0) mbar_arrive(b.epi_in);
@@ -394,7 +478,7 @@ __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint3
     __threadfence();
     if (n < p.N) {
 #pragma unroll
-        for (int m = 0; m < C::kNtok; ++m) {
+        for (int m = m0; m < m0 + kHalf; ++m) {
             if (m < p.M) {
                 float s = 0.0f;
                 for (int sp = 0; sp < p.splits; ++sp)
@@ -408,20 +492,20 @@ __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint3
 
 // ------------------------------------------------------------------ kernel
 template <int NTOK, int STAGES, bool A_SMEM>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, NTOK == 16 ? 3 : 2)
     w12_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_x) {
     using C = GemmCfg<NTOK, STAGES, A_SMEM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBars);
     Bars b;
-    b.full = bars;
-    b.empty = b.full + STAGES;
-    b.afull = b.empty + STAGES;
+    b.wfull = bars;
+    b.wempty = b.wfull + STAGES;
+    b.sfull = b.wempty + STAGES;
+    b.sempty = b.sfull + C::kSegSlots;
+    b.afull = b.sempty + C::kSegSlots;
     b.aempty = b.afull + C::kASlots;
-    b.escfull = b.aempty + C::kASlots;
-    b.escempty = b.escfull + C::kEscSlots;
-    b.hdr = b.escempty + C::kEscSlots;
+    b.hdr = b.aempty + C::kASlots;
     b.accum = b.hdr + 1;
     b.drain = b.accum + 1;
     b.epi_in = b.drain + 1;
@@ -442,27 +526,27 @@ __global__ void __launch_bounds__(192, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(b.full + i, 1);
-            mbar_init(b.empty + i, 4 + 1);
+            mbar_init(b.wfull + i, 1);
+            mbar_init(b.wempty + i, C::kDecWarps);
+        }
+        for (int i = 0; i < C::kSegSlots; ++i) {
+            mbar_init(b.sfull + i, 1);
+            mbar_init(b.sempty + i, C::kDecWarps + 1);
         }
         for (int i = 0; i < C::kASlots; ++i) {
-            mbar_init(b.afull + i, 4);
+            mbar_init(b.afull + i, C::kDecWarps);
             mbar_init(b.aempty + i, 1);
-        }
-        for (int i = 0; i < C::kEscSlots; ++i) {
-            mbar_init(b.escfull + i, 1);
-            mbar_init(b.escempty + i, 4);
         }
         mbar_init(b.hdr, 1);
         mbar_init(b.accum, 1);
         mbar_init(b.drain, 1);
-        mbar_init(b.epi_in, 4);
+        mbar_init(b.epi_in, C::kDecWarps);
         mbar_init(b.epi_out, 1);
         *abort_flag = 0u;
         *last_flag = 0u;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(tmem_slot, C::kTmemCols);
         tmem_relinquish();
     }
@@ -471,10 +555,10 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == 8) {
         if ((threadIdx.x & 31) == 0) gemm_producer<C>(p, &tmap_x, smem, b, abort_flag, tile, s0, c0, c1, deadline);
-    } else if (warp == 5) {
-        if ((threadIdx.x & 31) == 0) gemm_mma<C>(p, smem, b, abort_flag, tmem_base, c1 - c0, deadline);
+    } else if (warp == 9) {
+        if ((threadIdx.x & 31) == 0) gemm_mma<C>(p, smem, b, abort_flag, tmem_base, c0, c1 - c0, deadline);
         __syncwarp();
     } else {
         gemm_decode<C>(p, smem, b, abort_flag, tmem_base, s0, c0, c1, deadline);
@@ -483,7 +567,7 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem_base, C::kTmemCols);
+    if (warp == 9) tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
 }  // namespace dev

@@ -85,7 +85,8 @@ int prepare_gemm(DeviceState &s, std::string *err) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(carveout)", err);
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, 192, (size_t)gemm_smem_bytes<NTOK, ASMEM>());
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, dev::GemmCfg<NTOK, kStages, ASMEM>::kThreads,
+                                                      (size_t)gemm_smem_bytes<NTOK, ASMEM>());
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor", err);
     // shared memory per SM bounds it as well (the query is not trusted alone)
     int smem_sm = 0;
@@ -228,7 +229,8 @@ template <int NTOK, bool ASMEM>
 cudaError_t launch_gemm_kernel(const dev::GemmParams &p, const CUtensorMap &tm, int splits, int64_t tiles,
                                cudaStream_t st) {
     dim3 grid((unsigned)splits, (unsigned)tiles);
-    dev::w12_gemm_tc_kernel<NTOK, kStages, ASMEM><<<grid, 192, gemm_smem_bytes<NTOK, ASMEM>(), st>>>(p, tm);
+    dev::w12_gemm_tc_kernel<NTOK, kStages, ASMEM>
+        <<<grid, dev::GemmCfg<NTOK, kStages, ASMEM>::kThreads, gemm_smem_bytes<NTOK, ASMEM>(), st>>>(p, tm);
     return cudaGetLastError();
 }
 }  // namespace

@@ -51,6 +51,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// 16-byte shared-memory load through a 32-bit shared address.
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(saddr));
+    return v;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -81,13 +90,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As above, but a thread whose phase is not complete may sleep in hardware
+// for up to `hint_ns` (it wakes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait: true once the phase with `parity` has completed, false when
 // `deadline_ns` (globaltimer) passes first.  Nothing here can spin forever.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t deadline_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && globaltimer_ns() > deadline_ns) return false;
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if ((i & 7u) == 0 && globaltimer_ns() > deadline_ns) return false;
     }
 }
 
@@ -172,6 +195,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
         "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(v[0]),
+        "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+        : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Warp-collective load of 16 32-bit columns.
@@ -183,6 +212,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
           "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
         : "r"(taddr)
         : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr)
+                 : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -277,22 +312,119 @@ __device__ __forceinline__ void patch_escapes(const uint32_t (&f)[4], const uint
 }
 
 // Warp-wide escape step for one quarter-chunk: every lane finds its escapes,
-// an exclusive scan over the lanes gives each lane its first byte in the
+// an exclusive prefix over the lanes gives each lane its first byte in the
 // quarter's run (rows in lane order, columns in order), and the exponents are
-// patched.  Returns the warp's escape count (to advance the run).
+// patched.  Returns the warp's escape count (to advance the run).  When few
+// lanes hold escapes (the common case) the prefix is gathered from those lanes
+// only; otherwise a shuffle scan runs.
 __device__ __forceinline__ uint32_t warp_escapes(const uint4 &codes, const uint8_t *run, uint32_t (&E)[8]) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t f[4] = {escape_flags(codes.x), escape_flags(codes.y), escape_flags(codes.z),
                            escape_flags(codes.w)};
     const uint32_t cnt = __popc(f[0]) + __popc(f[1]) + __popc(f[2]) + __popc(f[3]);
+    const uint32_t holders = __ballot_sync(0xFFFFFFFFu, cnt != 0);
+    uint32_t excl = 0, total = 0;
+    if (__popc(holders) <= 4) {
+        uint32_t h = holders;
+        while (h) {
+            const uint32_t l = (uint32_t)__ffs(h) - 1u;
+            h &= h - 1u;
+            const uint32_t c = __shfl_sync(0xFFFFFFFFu, cnt, l);
+            total += c;
+            if (l < lane) excl += c;
+        }
+    } else {
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= (uint32_t)d) incl += v;
+        }
+        total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        excl = incl - cnt;
+    }
+    if (cnt) patch_escapes(f, run + excl, E);
+    return total;
+}
+
+// ---- half-chunk forms: one thread, one row, 16 columns (half h of a chunk)
+
+// E[j] = exponents of columns 16h + 4j .. 16h + 4j + 3 (codes in words w0, w1).
+__device__ __forceinline__ void decode_exponents_half(const Table &T, uint32_t w0, uint32_t w1, uint32_t (&E)[4]) {
+    lookup8(T, w0, E[0], E[1]);
+    lookup8(T, w1, E[2], E[3]);
+}
+
+// out[i] = BF16 pair of columns 16h + 2i, 16h + 2i + 1.
+__device__ __forceinline__ void assemble_half(const uint4 &s, const uint32_t (&E)[4], uint32_t (&out)[8]) {
+    const uint32_t S[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        out[2 * j] = rotr1(prmt(S[j], E[j], 0x5140u));
+        out[2 * j + 1] = rotr1(prmt(S[j], E[j], 0x7362u));
+    }
+}
+
+// Exclusive prefix over the lanes of `cnt` and the warp total.  When no lane
+// holds more than one escape (the common case) a ballot gives both; else a
+// shuffle scan.
+__device__ __forceinline__ void lane_prefix(uint32_t cnt, uint32_t &excl, uint32_t &total) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t holders = __ballot_sync(0xFFFFFFFFu, cnt != 0);
+    if (__all_sync(0xFFFFFFFFu, cnt <= 1u)) {
+        excl = __popc(holders & ((1u << lane) - 1u));
+        total = __popc(holders);
+        return;
+    }
     uint32_t incl = cnt;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
         if (lane >= (uint32_t)d) incl += v;
     }
-    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    if (cnt) patch_escapes(f, run + (incl - cnt), E);
+    total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    excl = incl - cnt;
+}
+
+// Patch escaped exponents into E[0..3] (16 columns) from src, in column
+// order, with a warp-uniform loop and predicated selects (no divergent
+// branches): fh[0], fh[1] are the escape flags of the 16 columns.
+__device__ __forceinline__ void patch_half(uint32_t f0, uint32_t f1, const uint8_t *src, uint32_t (&E)[4]) {
+    const uint32_t mine = __popc(f0) + __popc(f1);
+    const uint32_t rounds = __reduce_max_sync(0xFFFFFFFFu, mine);
+    for (uint32_t t = 0; t < rounds; ++t) {
+        const bool have = t < mine;
+        const bool lo = f0 != 0u;
+        const uint32_t fw = lo ? f0 : f1;
+        const uint32_t b = (uint32_t)__ffs(fw) - 1u;    // 4p + 3 within the word
+        const uint32_t k = (lo ? 0u : 8u) + (b >> 2);    // column 0..15
+        const uint32_t clear = fw & (fw - 1u);
+        f0 = lo ? clear : f0;
+        f1 = lo ? f1 : clear;
+        const uint32_t e = have ? (uint32_t)src[t] : 0u;
+        const uint32_t sh = (k & 3u) << 3;
+        const uint32_t j = k >> 2;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t patched = (E[jj] & ~(0xFFu << sh)) | (e << sh);
+            E[jj] = (have && j == (uint32_t)jj) ? patched : E[jj];
+        }
+    }
+}
+
+// Escape step for half h of a quarter-chunk.  The escape run orders a row's
+// 32 columns together, so the lane prefix is taken over whole-row counts and
+// the second half starts after the row's first-half escapes.  Returns the
+// warp's escape count over the whole chunk (both halves).
+__device__ __forceinline__ uint32_t warp_escapes_half(const uint4 &codes, int h, const uint8_t *run,
+                                                      uint32_t (&E)[4]) {
+    const uint32_t f[4] = {escape_flags(codes.x), escape_flags(codes.y), escape_flags(codes.z),
+                           escape_flags(codes.w)};
+    const uint32_t c0 = __popc(f[0]) + __popc(f[1]);
+    const uint32_t cnt = c0 + __popc(f[2]) + __popc(f[3]);
+    uint32_t excl, total;
+    lane_prefix(cnt, excl, total);
+    patch_half(h ? f[2] : f[0], h ? f[3] : f[1], run + excl + (h ? c0 : 0u), E);
     return total;
 }
 
