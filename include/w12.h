@@ -157,6 +157,38 @@ int w12_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info *info,
              uint16_t *y_dev, int M, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Size of the fixed scratch array behind w12_gemm_noalloc (16 MiB).
+ */
+#define W12_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * The same product as w12_gemm, for callers that cannot allocate device
+ * memory.  No passage of the SpecPilot pages has a counterpart; this entry
+ * point exists for integration.  Callers that cannot call cudaMalloc include
+ * serving engines whose allocator has reserved all free HBM up front (for
+ * weights and KV cache) and would fail or fragment on a new allocation,
+ * plug-ins that must not allocate behind their host framework's memory
+ * accounting, and latency-critical paths where cudaMalloc's implicit device
+ * synchronisation is not acceptable.
+ *
+ * The split-K partials, arrival counters and padded x copy live in one array
+ * of W12_NOALLOC_SCRATCH_BYTES in static device memory inside the library;
+ * every device that loads the library keeps that array until the process
+ * exits.  The call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine): it clears the counters with cudaMemsetAsync on `stream`
+ * and launches the GEMM.  The first call on each device looks up the array's
+ * device address (with that device current); make that first call before any
+ * stream capture.  A problem whose scratch need (w12_gemm_workspace_size)
+ * exceeds W12_NOALLOC_SCRATCH_BYTES is rejected with W12_ERR_BUFFER_TOO_SMALL
+ * before anything is launched.  All calls share the one array, which keeps
+ * the last call's contents: calls that overlap on the GPU (different streams
+ * without ordering, or several host threads) race and give wrong results;
+ * order them on one stream.  Arguments and errors otherwise as w12_gemm.
+ */
+int w12_gemm_noalloc(const uint16_t *x_dev, const void *blob_dev, const w12_info *info,
+                     uint16_t *y_dev, int M, void *stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's status word,
  * which kernels set when a bounded wait gives up.  Returns TIMEOUT if it was
  * set, CUDA on a CUDA error, else OK.

@@ -169,6 +169,27 @@ int w12_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info *info, 
     });
 }
 
+int w12_gemm_noalloc(const uint16_t *x_dev, const void *blob_dev, const w12_info *info, uint16_t *y_dev, int M,
+                     void *stream) {
+    return guarded([&](std::string &err) {
+        int rc = check_info(info, err);
+        if (rc != W12_OK) return rc;
+        if (!x_dev || !blob_dev || !y_dev) {
+            err = "null device pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (M < 1 || M > 32) {
+            err = "M must be in 1..32";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (!aligned(blob_dev, 256) || !aligned(y_dev, 2) || !aligned(x_dev, 2)) {
+            err = "blob_dev must be 256-byte aligned, x_dev and y_dev 2-byte aligned";
+            return (int)W12_ERR_ALIGNMENT;
+        }
+        return w12::launch::gemm_noalloc(x_dev, blob_dev, *info, y_dev, M, stream, &err);
+    });
+}
+
 int w12_check_status(void *stream) {
     return guarded([&](std::string &err) { return w12::launch::check_status(stream, &err); });
 }

@@ -325,6 +325,61 @@ int check_status(void *stream, std::string *err) {
     return W12_OK;
 }
 
+// ---------------------------------------------------------------- no-alloc
+// Scratch for w12_gemm_noalloc: a fixed array in static device memory, so
+// that call never allocates.  Every device that loads the library holds it
+// until the process exits.  All calls share it and it keeps the last call's
+// contents, so calls that overlap on the GPU race.
+static __device__ __align__(256) uint8_t g_w12_noalloc_scratch[W12_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+uint8_t *g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current): in host code the array's name is
+// only a host-side stand-in, never a device address.
+int noalloc_scratch(uint8_t **out, std::string *err) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice", err);
+    if (dev < 0 || dev >= kMaxDevices) {
+        *err = "device ordinal out of range";
+        return W12_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_w12_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)", err);
+        g_noalloc_ptr[dev] = static_cast<uint8_t *>(ptr);
+    }
+    *out = g_noalloc_ptr[dev];
+    return W12_OK;
+}
+}  // namespace
+
+int gemm_noalloc(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,
+                 void *stream, std::string *err) {
+    GemmPlan plan;
+    int rc = plan_gemm(info, M, &plan, err);
+    if (rc != W12_OK) return rc;
+    if (plan.ws_bytes > (size_t)W12_NOALLOC_SCRATCH_BYTES) {
+        *err = "w12_gemm_noalloc: this matrix and M need " + std::to_string(plan.ws_bytes) +
+               " bytes of scratch, more than the fixed " + std::to_string((size_t)W12_NOALLOC_SCRATCH_BYTES) +
+               " bytes the library reserves; use w12_gemm with a caller-provided workspace";
+        return W12_ERR_BUFFER_TOO_SMALL;
+    }
+    uint8_t *scratch = nullptr;
+    rc = noalloc_scratch(&scratch, err);
+    if (rc != W12_OK) return rc;
+    // the split-K arrival counters must start at zero on every call
+    cudaError_t e = cudaMemsetAsync(scratch + plan.ws_counters, 0, plan.ws_partials - plan.ws_counters,
+                                    static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(no-alloc counters)", err);
+    return gemm(x_dev, blob_dev, info, y_dev, M, scratch, (size_t)W12_NOALLOC_SCRATCH_BYTES, stream, err);
+}
+
 int selftest_timeout(uint32_t timeout_us, void *stream, std::string *err) {
     DeviceState *s = nullptr;
     int rc = device_state(&s, err);

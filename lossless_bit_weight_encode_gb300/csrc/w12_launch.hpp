@@ -27,6 +27,9 @@ int decode(const void *blob_dev, const w12_info &info, uint16_t *out_dev, void *
 int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,
          void *workspace, size_t ws_bytes, void *stream, std::string *err);
 
+int gemm_noalloc(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,
+                 void *stream, std::string *err);
+
 int check_status(void *stream, std::string *err);
 
 int selftest_timeout(uint32_t timeout_us, void *stream, std::string *err);

@@ -16,6 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libw12.so")
 
 W12_OK = 0
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # W12_NOALLOC_SCRATCH_BYTES in include/w12.h
 STATUS_NAMES = {
     0: "W12_OK", 1: "W12_ERR_INVALID_ARG", 2: "W12_ERR_SHAPE", 3: "W12_ERR_BUFFER_TOO_SMALL",
     4: "W12_ERR_ALIGNMENT", 5: "W12_ERR_CORRUPT_BLOB", 6: "W12_ERR_UNSUPPORTED_ARCH", 7: "W12_ERR_CUDA",
@@ -24,7 +25,7 @@ STATUS_NAMES = {
 EXPORTED = (
     "w12_last_error", "w12_status_string", "w12_format_version", "w12_encoded_size_host", "w12_encode_host",
     "w12_blob_info", "w12_blob_validate", "w12_decode", "w12_gemm_workspace_size", "w12_gemm_launch_info",
-    "w12_gemm",
+    "w12_gemm", "w12_gemm_noalloc",
     "w12_check_status", "w12_selftest_timeout",
 )
 
@@ -76,6 +77,7 @@ def lib() -> ctypes.CDLL:
     L.w12_gemm_workspace_size.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(sz)]
     L.w12_gemm_launch_info.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(ctypes.c_int32)]
     L.w12_gemm.argtypes = [vp, vp, ctypes.POINTER(w12_info), vp, i32, vp, sz, vp]
+    L.w12_gemm_noalloc.argtypes = [vp, vp, ctypes.POINTER(w12_info), vp, i32, vp]
     L.w12_check_status.argtypes = [vp]
     L.w12_selftest_timeout.argtypes = [ctypes.c_uint32, vp]
     for name in EXPORTED[3:]:
@@ -164,6 +166,13 @@ def w12_gemm_ptr(x_ptr: int, blob_ptr: int, info: w12_info, y_ptr: int, M: int, 
     """Raw-pointer form of w12_gemm that returns the status instead of raising
     (for timing loops that check once at the end)."""
     return lib().w12_gemm(x_ptr, blob_ptr, ctypes.byref(info), y_ptr, int(M), ws_ptr, ws_bytes, stream_handle)
+
+
+def w12_gemm_noalloc(x_dev, blob_dev, info: w12_info, y_dev, M: int, stream=None) -> None:
+    """w12_gemm without a workspace argument: the library's fixed static
+    scratch is used (see include/w12.h); nothing is allocated."""
+    _check(lib().w12_gemm_noalloc(x_dev.data_ptr(), blob_dev.data_ptr(), ctypes.byref(info), y_dev.data_ptr(),
+                                  int(M), _stream_handle(stream)))
 
 
 def w12_check_status(stream=None) -> None:
