@@ -128,6 +128,26 @@ __device__ __forceinline__ bool escapes_staged(uint32_t total) {
     return total > 0 && total + 30u <= (uint32_t)C::kEscCap;
 }
 
+
+// Before waiting for the previous kernel in the stream: pull this CTA's first
+// weight bytes (its segment headers and up to kPrefetchBytes of packed chunks)
+// into L2.  Only L2 is warmed here; every load that lands in shared memory is
+// issued after griddepcontrol.wait, so a blob written by that previous kernel
+// is still read correctly.
+constexpr uint32_t kPrefetchBytes = 96 * 1024;
+__device__ __forceinline__ void prefetch_cta_weights(const GemmParams &p, int64_t tile, int s0, int c0, int c1) {
+    const int nsegs_cta = (c1 - c0 + kChunksPerSeg - 1) / kChunksPerSeg;
+    prefetch_l2(p.blob + p.off_seg + (uint64_t)(tile * p.segs + s0) * kSegHdrBytes,
+                (uint32_t)nsegs_cta * kSegHdrBytes);
+    const uint8_t *w = p.blob + p.off_w + (uint64_t)(tile * p.chunks + c0) * kChunkBytes;
+    uint32_t left = (uint32_t)(c1 - c0) * kChunkBytes;
+    if (left > kPrefetchBytes) left = kPrefetchBytes;
+    for (uint32_t off = 0; off < left; off += 4 * kChunkBytes) {
+        const uint32_t n = left - off < 4u * kChunkBytes ? left - off : 4u * kChunkBytes;
+        prefetch_l2(w + off, n);
+    }
+}
+
 // ------------------------------------------------------------------ producer
 template <class C>
 __device__ void gemm_producer(const GemmParams &p, const CUtensorMap *tmap, uint8_t *smem, const Bars &b,
@@ -554,6 +574,9 @@ __global__ void __launch_bounds__(320, NTOK == 16 ? 3 : 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    if (warp == 8 && (threadIdx.x & 31) == 0) prefetch_cta_weights(p, tile, s0, c0, c1);
+    pdl_wait();
 
     if (warp == 8) {
         if ((threadIdx.x & 31) == 0) gemm_producer<C>(p, &tmap_x, smem, b, abort_flag, tile, s0, c0, c1, deadline);

@@ -1,0 +1,352 @@
+// W12 GEMV on CUDA cores (one token, M = 1): y = x . W^T with W streamed from
+// HBM in W12 form and decoded in registers ("decoded inside the GEMM
+// registers", "SpecPilot: an agent doubled speculative decoding speed, and
+// the 10.87x needs context", §The mechanisms it found; bit-exact weights,
+// "StargazerX0/SpecPilot", §What it is).
+//
+// With one token the product is 2 flops per weight, far below what needs the
+// tensor cores; what bounds this path is streaming the packed bytes and the
+// integer decode.  So the decoded BF16 pairs go straight into fp32 fused
+// multiply-adds (fma.rn.f32x2: two weights per instruction) with no TMEM
+// store and no handshake with an MMA warp.
+//
+// Warp roles (288 threads):
+//   warps 0-7  decode: warp w handles rows 32q..32q+31 (q = w mod 4) and
+//              columns 16h..16h+15 of every chunk (h = w / 4); per weight
+//              stage (2 chunks) a thread reads its row's S bytes and codes from
+//              SMEM, decodes 2 x 16 weights, patches escapes and accumulates
+//              them against x (fp32 in SMEM, converted once per segment);
+//   warp 8     producer: cp.async.bulk for the segment headers and every
+//              weight stage (12 KB); per segment cp.async.bulk.tensor for the
+//              256 x values and cp.async.bulk for the escape bytes.
+// The two column halves of a row are added in fixed order at the end, then
+// the split-K partials as in the tensor-core kernel.  Every wait is bounded.
+#pragma once
+
+#include "gemm_tc.cuh"
+
+namespace w12 {
+namespace dev {
+
+template <int STAGES, int SCHUNKS>
+struct GemvCfg {
+    static constexpr int kThreads = 288;
+    static constexpr int kDecWarps = 8;
+    static constexpr int kStages = STAGES;
+    static constexpr int kStageChunks = SCHUNKS;                // chunks per weight stage
+    static constexpr int kStagesPerSeg = kChunksPerSeg / SCHUNKS;
+    static constexpr int kWBytes = SCHUNKS * kChunkBytes;
+    static constexpr int kXbBytes = kSegK * 2;        // one segment of x, BF16 (TMA destination)
+    static constexpr int kXfBytes = kSegK * 4;        // the same as fp32
+    static constexpr int kSegSlots = 2;
+    static constexpr int kEscCap = 2048;
+    static constexpr int kMaxSegs = 96;
+    static constexpr int kOffW = 0;
+    static constexpr int kOffXb = kOffW + STAGES * kWBytes;  // 128-byte aligned
+    static constexpr int kOffXf = kOffXb + kSegSlots * kXbBytes;
+    static constexpr int kOffEsc = kOffXf + kSegSlots * kXfBytes;
+    static constexpr int kOffHdr = kOffEsc + kSegSlots * kEscCap;
+    static constexpr int kOffRed = kOffHdr + kMaxSegs * kSegHdrBytes;  // 128 fp32
+    static constexpr int kOffBars = kOffRed + kTileRows * 4;
+    // wfull[S], wempty[S], sfull[2], sempty[2], xconv[2], hdr, red, epi_in, epi_out
+    static constexpr int kNumBars = 2 * STAGES + 3 * kSegSlots + 4;
+    static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 64 + 128;  // + slack to align the base to 128
+    static_assert(kOffXb % 128 == 0, "TMA destination alignment");
+    static_assert(kChunksPerSeg % SCHUNKS == 0, "stages must tile a segment");
+};
+
+struct GemvBars {
+    uint64_t *wfull, *wempty, *sfull, *sempty, *xconv, *hdr, *red, *epi_in, *epi_out;
+};
+
+// two fp32 values as one 64-bit operand of the packed instructions
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+    uint64_t v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(lo), "r"(hi));
+    return v;
+}
+
+__device__ __forceinline__ void fma2(uint64_t &acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+// acc += w . x over 16 columns: w as 8 BF16 pairs (even column low), x as
+// 16 fp32 at shared address xs.  Exact widening: BF16 -> fp32 is a shift.
+__device__ __forceinline__ void dot16(const uint32_t (&w)[8], uint32_t xs, uint64_t &acc0, uint64_t &acc1) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint4 xv = lds128(xs + 16u * (uint32_t)g);
+        const uint32_t w0 = w[2 * g], w1 = w[2 * g + 1];
+        fma2(acc0, pack2(w0 << 16, w0 & 0xFFFF0000u), pack2(xv.x, xv.y));
+        fma2(acc1, pack2(w1 << 16, w1 & 0xFFFF0000u), pack2(xv.z, xv.w));
+    }
+}
+
+__device__ __forceinline__ float unpack_sum(uint64_t a, uint64_t b) {
+    const float a0 = __uint_as_float((uint32_t)a), a1 = __uint_as_float((uint32_t)(a >> 32));
+    const float b0 = __uint_as_float((uint32_t)b), b1 = __uint_as_float((uint32_t)(b >> 32));
+    return (a0 + a1) + (b0 + b1);
+}
+
+// ------------------------------------------------------------------ producer
+template <class C>
+__device__ void gemv_producer(const GemmParams &p, const CUtensorMap *tmap, uint8_t *smem, const GemvBars &b,
+                              volatile uint32_t *abort_flag, int64_t tile, int s0, int c0, int c1,
+                              uint64_t deadline) {
+    const int nchunks = c1 - c0;
+    const int nsegs_cta = (nchunks + kChunksPerSeg - 1) / kChunksPerSeg;
+    const int nstages = (nchunks + C::kStageChunks - 1) / C::kStageChunks;
+    uint8_t *hdr = smem + C::kOffHdr;
+    prefetch_tmap(tmap);
+
+    const uint32_t hbytes = (uint32_t)nsegs_cta * kSegHdrBytes;
+    mbar_arrive_expect_tx(b.hdr, hbytes);
+    bulk_g2s(hdr, p.blob + p.off_seg + (uint64_t)(tile * p.segs + s0) * kSegHdrBytes, hbytes, b.hdr);
+    bool hdr_ready = false;
+    int issued = 0, seg_issued = 0;
+    bool failed = false;
+
+    for (int st = 0; st < nstages; ++st) {
+        const int chunk = c0 + C::kStageChunks * st;
+        if ((chunk & (kChunksPerSeg - 1)) == 0) {
+            const int ls = chunk / kChunksPerSeg - s0;
+            const int sslot = ls & 1;
+            if (!hdr_ready) {
+                if (!mbar_wait(b.hdr, 0, deadline)) { failed = true; break; }
+                hdr_ready = true;
+            }
+            if (ls >= 2 && !mbar_wait(b.sempty + sslot, (uint32_t)((ls >> 1) - 1) & 1u, deadline)) {
+                failed = true;
+                break;
+            }
+            const uint4 meta = *reinterpret_cast<const uint4 *>(hdr + ls * kSegHdrBytes + 16);
+            const uint32_t base = meta.x;
+            const uint32_t total = seg_escape_total(meta);
+            uint32_t ebytes = 0, src0 = 0;
+            if (escapes_staged<C>(total)) {
+                src0 = base & ~15u;
+                ebytes = ((base + total + 15u) & ~15u) - src0;
+            }
+            mbar_arrive_expect_tx(b.sfull + sslot, (uint32_t)C::kXbBytes + ebytes);
+            tma_load_2d(smem + C::kOffXb + sslot * C::kXbBytes, tmap, chunk * kChunkK, 0, b.sfull + sslot);
+            if (ebytes)
+                bulk_g2s(smem + C::kOffEsc + sslot * C::kEscCap, p.blob + p.off_esc + src0, ebytes, b.sfull + sslot);
+            seg_issued = ls + 1;
+        }
+        const int slot = st % C::kStages;
+        if (st >= C::kStages &&
+            !mbar_wait(b.wempty + slot, (uint32_t)(st / C::kStages - 1) & 1u, deadline)) {
+            failed = true;
+            break;
+        }
+        const int nch = min(C::kStageChunks, c1 - chunk);
+        mbar_arrive_expect_tx(b.wfull + slot, (uint32_t)(nch * kChunkBytes));
+        bulk_g2s(smem + C::kOffW + slot * C::kWBytes,
+                 p.blob + p.off_w + (uint64_t)(tile * p.chunks + chunk) * kChunkBytes, (uint32_t)(nch * kChunkBytes),
+                 b.wfull + slot);
+        issued = st + 1;
+        if (*abort_flag) break;
+    }
+    if (failed) raise_timeout(p.status, abort_flag);
+    if (*abort_flag) {
+        const uint64_t drain_deadline = globaltimer_ns() + 1000000000ull;
+        for (int st = max(0, issued - C::kStages); st < issued; ++st)
+            mbar_wait(b.wfull + st % C::kStages, (uint32_t)(st / C::kStages) & 1u, drain_deadline);
+        for (int ls = max(0, seg_issued - 2); ls < seg_issued; ++ls)
+            mbar_wait(b.sfull + (ls & 1), (uint32_t)(ls >> 1) & 1u, drain_deadline);
+        mbar_wait(b.hdr, 0, drain_deadline);
+    }
+}
+
+// ------------------------------------------------------------------ decoders
+template <class C>
+__device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &b, volatile uint32_t *abort_flag,
+                            volatile uint32_t *last_flag, int64_t tile, int split, int s0, int c0, int c1,
+                            uint64_t deadline) {
+    const int warp = threadIdx.x >> 5;
+    const int q = warp & 3;       // rows 32q..32q+31
+    const int h = warp >> 2;      // columns 16h..16h+15 of each chunk
+    const int lane = threadIdx.x & 31;
+    const int r = 32 * q + lane;  // row in the tile
+    const int t = threadIdx.x;    // 0..255: the x element this thread widens per segment
+    const int nchunks = c1 - c0;
+    const int nstages = (nchunks + C::kStageChunks - 1) / C::kStageChunks;
+    const uint8_t *hdr = smem + C::kOffHdr;
+    const uint32_t s_row = smem_u32(smem + C::kOffW) + (uint32_t)(h * kSlabBytes + 16 * r);
+    const uint32_t c_off = (uint32_t)((2 - h) * kSlabBytes);
+    const uint32_t xf0 = smem_u32(smem + C::kOffXf) + (uint32_t)(16 * h) * 4u;
+
+    uint64_t acc0 = 0, acc1 = 0;  // two fp32 pairs each, +0.0
+    bool ok = warp_wait(b.hdr, 0, deadline);
+    Table T{};
+    uint32_t mask_q = 0, xseg = 0;
+    const uint8_t *run = nullptr;
+    for (int st = 0; ok && st < nstages; ++st) {
+        const int chunk0 = c0 + C::kStageChunks * st;
+        const int jj0 = chunk0 & (kChunksPerSeg - 1);
+        const int ls = st / C::kStagesPerSeg;
+        const int sslot = ls & 1;
+        const int nch = min(C::kStageChunks, c1 - chunk0);
+        if (jj0 == 0) {
+            const uint8_t *hp = hdr + (chunk0 / kChunksPerSeg - s0) * kSegHdrBytes;
+            T = make_table(*reinterpret_cast<const uint4 *>(hp));
+            const uint4 meta = *reinterpret_cast<const uint4 *>(hp + 16);
+            const uint32_t qc0 = meta.y & 0xFFFFu, qc1 = meta.y >> 16, qc2 = meta.z & 0xFFFFu;
+            const uint32_t qoff = (q > 0 ? qc0 : 0u) + (q > 1 ? qc1 : 0u) + (q > 2 ? qc2 : 0u);
+            mask_q = (meta.w >> (8 * q)) & 0xFFu;
+            if (!(ok = warp_wait(b.sfull + sslot, (uint32_t)(ls >> 1) & 1u, deadline))) break;
+            if (escapes_staged<C>(seg_escape_total(meta)))
+                run = smem + C::kOffEsc + sslot * C::kEscCap + (meta.x & 15u) + qoff;
+            else
+                run = p.blob + p.off_esc + meta.x + qoff;
+            // widen this segment's 256 x values to fp32, one per thread
+            const uint16_t xb = reinterpret_cast<const uint16_t *>(smem + C::kOffXb + sslot * C::kXbBytes)[t];
+            reinterpret_cast<float *>(smem + C::kOffXf + sslot * C::kXfBytes)[t] = __uint_as_float((uint32_t)xb << 16);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b.xconv + sslot);
+            if (!(ok = warp_wait(b.xconv + sslot, (uint32_t)(ls >> 1) & 1u, deadline))) break;
+            xseg = xf0 + (uint32_t)(sslot * C::kXfBytes);
+        }
+        const int slot = st % C::kStages;
+        if (!(ok = warp_wait(b.wfull + slot, (uint32_t)(st / C::kStages) & 1u, deadline))) break;
+        // read the whole stage first so that its slot is freed early
+        const uint32_t sa = s_row + (uint32_t)(slot * C::kWBytes);
+        uint4 sb[C::kStageChunks], cd[C::kStageChunks];
+#pragma unroll
+        for (int e = 0; e < C::kStageChunks; ++e) {
+            if (e < nch) {
+                sb[e] = lds128(sa + (uint32_t)(e * kChunkBytes));
+                cd[e] = lds128(sa + (uint32_t)(e * kChunkBytes) + c_off);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b.wempty + slot);
+
+#pragma unroll
+        for (int e = 0; e < C::kStageChunks; ++e) {
+            if (e < nch) {
+                uint32_t out[8];
+                decode_half_chunk(T, sb[e], cd[e], h, (mask_q >> (jj0 + e)) & 1u, run, out);
+                dot16(out, xseg + (uint32_t)((jj0 + e) * kChunkK * 4), acc0, acc1);
+            }
+        }
+        if (jj0 + nch == kChunksPerSeg || st == nstages - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b.sempty + sslot);  // done with this segment's x and escapes
+        }
+    }
+    if (!ok) {
+        if (lane == 0) raise_timeout(p.status, abort_flag);
+        return;
+    }
+
+    // ---- epilogue: add the two column halves of each row in fixed order
+    const float mine = unpack_sum(acc0, acc1);
+    float *red = reinterpret_cast<float *>(smem + C::kOffRed);
+    if (h == 1) {
+        red[r] = mine;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b.red);
+        return;
+    }
+    if (!warp_wait(b.red, 0, deadline)) {
+        if (lane == 0) raise_timeout(p.status, abort_flag);
+        return;
+    }
+    const float total = mine + red[r];
+    const int64_t n = tile * kTileRows + r;
+    if (p.splits == 1) {
+        if (n < p.N) p.y[n] = bf16_bits_rn(total);
+        return;
+    }
+    __stcg(p.partials + (int64_t)split * p.Npad + n, total);
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b.epi_in);
+    if (threadIdx.x == 0) {
+        if (mbar_wait(b.epi_in, 0, deadline)) {
+            __threadfence();
+            const uint32_t old = atomicAdd(p.counters + tile, 1u);
+            *last_flag = (old == (uint32_t)(p.splits - 1)) ? 1u : 0u;
+            mbar_arrive(b.epi_out);
+        } else {
+            raise_timeout(p.status, abort_flag);
+        }
+    }
+    if (!warp_wait(b.epi_out, 0, deadline)) {
+        if (lane == 0) raise_timeout(p.status, abort_flag);
+        return;
+    }
+    if (*last_flag == 0) return;
+    __threadfence();
+    if (n < p.N) {
+        float s = 0.0f;
+        for (int sp = 0; sp < p.splits; ++sp) s += __ldcg(p.partials + (int64_t)sp * p.Npad + n);
+        p.y[n] = bf16_bits_rn(s);
+    }
+    if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next call
+}
+
+// ------------------------------------------------------------------ kernel
+template <int STAGES, int SCHUNKS>
+__global__ void __launch_bounds__(288, 2)
+    w12_gemv_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_x) {
+    using C = GemvCfg<STAGES, SCHUNKS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBars);
+    GemvBars b;
+    b.wfull = bars;
+    b.wempty = b.wfull + STAGES;
+    b.sfull = b.wempty + STAGES;
+    b.sempty = b.sfull + C::kSegSlots;
+    b.xconv = b.sempty + C::kSegSlots;
+    b.hdr = b.xconv + C::kSegSlots;
+    b.red = b.hdr + 1;
+    b.epi_in = b.red + 1;
+    b.epi_out = b.epi_in + 1;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile uint32_t *abort_flag = misc + 1;
+    volatile uint32_t *last_flag = misc + 2;
+
+    const int warp = threadIdx.x >> 5;
+    const int split = blockIdx.x;
+    const int64_t tile = blockIdx.y;
+    const int s0 = (int)((int64_t)split * p.segs / p.splits);
+    const int s1 = (int)((int64_t)(split + 1) * p.segs / p.splits);
+    const int c0 = s0 * kChunksPerSeg;
+    const int c1 = min(s1 * kChunksPerSeg, p.chunks);
+    const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(b.wfull + i, 1);
+            mbar_init(b.wempty + i, C::kDecWarps);
+        }
+        for (int i = 0; i < C::kSegSlots; ++i) {
+            mbar_init(b.sfull + i, 1);
+            mbar_init(b.sempty + i, C::kDecWarps);
+            mbar_init(b.xconv + i, C::kDecWarps);
+        }
+        mbar_init(b.hdr, 1);
+        mbar_init(b.red, 4);
+        mbar_init(b.epi_in, 4);
+        mbar_init(b.epi_out, 1);
+        *abort_flag = 0u;
+        *last_flag = 0u;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    if (warp == 8 && (threadIdx.x & 31) == 0) prefetch_cta_weights(p, tile, s0, c0, c1);
+    pdl_wait();
+    if (warp == 8) {
+        if ((threadIdx.x & 31) == 0) gemv_producer<C>(p, &tmap_x, smem, b, abort_flag, tile, s0, c0, c1, deadline);
+    } else {
+        gemv_decode<C>(p, smem, b, abort_flag, last_flag, tile, split, s0, c0, c1, deadline);
+    }
+}
+
+}  // namespace dev
+}  // namespace w12

@@ -7,9 +7,11 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "decode.cuh"
 #include "gemm_tc.cuh"
+#include "gemv.cuh"
 #include "w12_launch.hpp"
 
 namespace w12 {
@@ -56,6 +58,7 @@ struct DeviceState {
     int sm_count = 0;
     uint32_t *status = nullptr;
     int occupancy[2][2] = {{0, 0}, {0, 0}};  // [ntok==32][a_smem]
+    int gemv_occupancy = 0;
 };
 
 DeviceState g_state[kMaxDevices];
@@ -88,13 +91,25 @@ int prepare_gemm(DeviceState &s, std::string *err) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, dev::GemmCfg<NTOK, kStages, ASMEM>::kThreads,
                                                       (size_t)gemm_smem_bytes<NTOK, ASMEM>());
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor", err);
-    // shared memory per SM bounds it as well (the query is not trusted alone)
-    int smem_sm = 0;
-    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, s.device);
-    const int by_smem = smem_sm / (gemm_smem_bytes<NTOK, ASMEM>() + 1024);
-    if (by_smem > occ) occ = by_smem;
     // TMEM: each CTA holds 128 of the SM's 512 columns
     s.occupancy[NTOK == 32][ASMEM] = occ < 4 ? occ : 4;
+    return W12_OK;
+}
+
+constexpr int kGemvStages = 4;
+constexpr int kGemvChunks = 4;  // chunks per weight stage
+using GemvC = dev::GemvCfg<kGemvStages, kGemvChunks>;
+
+int prepare_gemv(DeviceState &s, std::string *err) {
+    void *k = reinterpret_cast<void *>(&dev::w12_gemv_kernel<kGemvStages, kGemvChunks>);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GemvC::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemv)", err);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemv carveout)", err);
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, GemvC::kThreads, (size_t)GemvC::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(gemv)", err);
+    s.gemv_occupancy = occ < 8 ? occ : 8;
     return W12_OK;
 }
 
@@ -123,7 +138,8 @@ int device_state(DeviceState **out, std::string *err) {
         }
         e = cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), dev::g_w12_status);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)", err);
-        int rc = prepare_gemm<16, false>(s, err);
+        int rc = prepare_gemv(s, err);
+        if (rc == W12_OK) rc = prepare_gemm<16, false>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<32, false>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<16, true>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<32, true>(s, err);
@@ -132,6 +148,14 @@ int device_state(DeviceState **out, std::string *err) {
     }
     *out = &s;
     return W12_OK;
+}
+
+// One token runs on CUDA cores unless W12_M1_PATH=tc asks for the tensor-core
+// kernel (kept selectable so both stay tested).
+bool use_gemv(int M) {
+    if (M != 1) return false;
+    const char *v = std::getenv("W12_M1_PATH");
+    return !(v != nullptr && std::strcmp(v, "tc") == 0);
 }
 
 bool use_smem_a_operand() {
@@ -172,8 +196,9 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err) {
     DeviceState *s = nullptr;
     int rc = device_state(&s, err);
     if (rc != W12_OK) return rc;
+    plan->gemv = use_gemv(M);
     plan->ntok = M <= 16 ? 16 : 32;
-    const int occ = s->occupancy[plan->ntok == 32][use_smem_a_operand()];
+    const int occ = plan->gemv ? s->gemv_occupancy : s->occupancy[plan->ntok == 32][use_smem_a_operand()];
     if (occ < 1) {
         *err = "GEMM kernel cannot be resident on this device";
         return W12_ERR_CUDA;
@@ -225,13 +250,38 @@ int decode(const void *blob_dev, const w12_info &info, uint16_t *out_dev, void *
 }
 
 namespace {
+// GEMM launches carry the programmatic-stream-serialization attribute: the
+// kernel may start while the previous kernel in the stream finishes; it warms
+// L2 with its first weights and then waits (griddepcontrol.wait) before any
+// other memory access.  W12_PDL=0 turns the attribute off.
+bool use_pdl() {
+    const char *v = std::getenv("W12_PDL");
+    return !(v != nullptr && std::strcmp(v, "0") == 0);
+}
+
+template <class... KArgs, class... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = use_pdl() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <int NTOK, bool ASMEM>
 cudaError_t launch_gemm_kernel(const dev::GemmParams &p, const CUtensorMap &tm, int splits, int64_t tiles,
                                cudaStream_t st) {
     dim3 grid((unsigned)splits, (unsigned)tiles);
-    dev::w12_gemm_tc_kernel<NTOK, kStages, ASMEM>
-        <<<grid, dev::GemmCfg<NTOK, kStages, ASMEM>::kThreads, gemm_smem_bytes<NTOK, ASMEM>(), st>>>(p, tm);
-    return cudaGetLastError();
+    return launch_overlapped(dev::w12_gemm_tc_kernel<NTOK, kStages, ASMEM>, grid,
+                             dim3(dev::GemmCfg<NTOK, kStages, ASMEM>::kThreads),
+                             (size_t)gemm_smem_bytes<NTOK, ASMEM>(), st, p, tm);
 }
 }  // namespace
 
@@ -268,10 +318,13 @@ int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint
     CUtensorMap tm;
     const cuuint64_t dims[2] = {(cuuint64_t)info.K, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)plan.ntok};
+    // tensor cores: 64-column boxes of NTOK token rows, 128-byte swizzle;
+    // GEMV: one 256-column box of the single row, no swizzle
+    const cuuint32_t box[2] = {plan.gemv ? (cuuint32_t)kSegK : 64u, plan.gemv ? 1u : (cuuint32_t)plan.ntok};
     const cuuint32_t estr[2] = {1u, 1u};
     CUresult cr = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(xsrc), dims, strides, box,
-                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         plan.gemv ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) {
         *err = "cuTensorMapEncodeTiled failed for x (code " + std::to_string((int)cr) + ")";
@@ -297,7 +350,11 @@ int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint
 
     cudaError_t e;
     const bool asmem = use_smem_a_operand();
-    if (plan.ntok == 16)
+    if (plan.gemv) {
+        dim3 grid((unsigned)plan.splits, (unsigned)info.tiles);
+        e = launch_overlapped(dev::w12_gemv_kernel<kGemvStages, kGemvChunks>, grid, dim3(GemvC::kThreads),
+                              (size_t)GemvC::kSmemBytes, st, p, tm);
+    } else if (plan.ntok == 16)
         e = asmem ? launch_gemm_kernel<16, true>(p, tm, plan.splits, info.tiles, st)
                   : launch_gemm_kernel<16, false>(p, tm, plan.splits, info.tiles, st);
     else

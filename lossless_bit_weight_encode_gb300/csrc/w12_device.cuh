@@ -134,6 +134,19 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int32_t
         : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching, and wait until the previous one has completed and its writes are
+// visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Warm L2 with `bytes` (a multiple of 16) from a 16-byte aligned address.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -166,3 +166,43 @@ def test_layer_shapes_sampled_rows(workload, Ms):
             y = _gemm(mat, x)
             ref = oracle.gemm_f64(x, np.ascontiguousarray(w[rows]))
             check_tolerance(y[:, rows], ref, f"{workload} {name} M={M}")
+
+
+@pytest.fixture(params=["gemv", "tc"])
+def m1_path(request, monkeypatch):
+    monkeypatch.setenv("W12_M1_PATH", request.param)
+    return request.param
+
+
+@pytest.mark.parametrize("case", ["gauss", "ragged", "forced2", "forced10", "forced100", "heavy_long"])
+def test_one_token_paths(case, m1_path):
+    """M = 1 runs on CUDA cores by default and on tensor cores on request;
+    both must meet the tolerance, including ragged tiles and every escape
+    regime (staged in SMEM, or read from global memory when a segment holds
+    too many)."""
+    from gpu_util import check_tolerance
+    if case == "gauss":
+        w = wl.gaussian_weights(512, 5120, seed=31)
+    elif case == "ragged":
+        w = wl.heavy_tail_weights(301, 1001, seed=32)
+    elif case == "heavy_long":
+        w = wl.heavy_tail_weights(256, 17408, seed=33)
+    else:
+        frac = {"forced2": 0.02, "forced10": 0.10, "forced100": 1.0}[case]
+        w = wl.forced_escape_weights(256, 4096, frac, seed=34)
+        e = (w >> 7) & 0xFF
+        w = np.where((e > 140) | (e == 255), (w & 0x807F) | np.uint16(130 << 7), w).astype(np.uint16)
+    x = wl.activations(1, w.shape[1], seed=35)
+    mat = W12Weight(w)
+    assert w12.w12_gemm_launch_info(mat.info, 1)["ntok"] in (16, 32)
+    check_tolerance(_gemm(mat, x), oracle.gemm_f64(x, w), f"{case} {m1_path}")
+
+
+def test_one_token_one_hot_exact(m1_path):
+    from gpu_util import bits_to_f64
+    w = wl.heavy_tail_weights(256, 1024, seed=36)
+    for k in (0, 17, 1023):
+        x = np.zeros((1, 1024), dtype=np.uint16)
+        x[0, k] = 0x3F80
+        y = bits_to_f64(_gemm(W12Weight(w), x))
+        assert np.array_equal(y[0], bits_to_f64(w[:, k])), f"{m1_path} column {k}"
