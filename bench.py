@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "W12 decode-GEMM effective weight GB/s & µs/layer at M=1–32; % of HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("lossless_bit_weight_encode_gb300/csrc/gemm_tc.cuh",
+                  "lossless_bit_weight_encode_gb300/csrc/gemv.cuh",
                   "lossless_bit_weight_encode_gb300/csrc/w12_device.cuh",
                   "lossless_bit_weight_encode_gb300/csrc/kernels.cu")
 
@@ -335,6 +336,8 @@ def run_w12(args):
     w12.w12_check_status()
     launch_ms = [statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(kp)) for i in range(nl)]
 
+    kernel_name = "w12_gemv_kernel" if w12.w12_gemm_launch_info(mats[0].info, M).get("ntok") and M == 1 \
+        and os.environ.get("W12_M1_PATH", "") != "tc" else "w12_gemm_tc_kernel"
     layer_weights = sum(m.N * m.K for m in mats)
     packed = sum(int(m.info.total_bytes) for m in mats)
     alg = [int(m.info.total_bytes) + 2 * M * m.K + 2 * M * m.N for m in mats]
@@ -429,7 +432,7 @@ def run_w12(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": traffic,
                      "algorithmic_bytes_per_launch": round(sum(alg) / nl),
-                     "kernel": "w12_gemm_tc_kernel", "launch_us": [round(v * 1e3, 2) for v in launch_ms]},
+                     "kernel": kernel_name, "launch_us": [round(v * 1e3, 2) for v in launch_ms]},
         "cpu_baseline": cpu,
         "clocks": csum,
         "e2e": e2e,

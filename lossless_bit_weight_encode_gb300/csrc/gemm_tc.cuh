@@ -168,35 +168,7 @@ __device__ void gemm_producer(const GemmParams &p, const CUtensorMap *tmap, uint
 
     for (int st = 0; st < nstages; ++st) {
         const int chunk = c0 + 2 * st;
-        if ((chunk & (kChunksPerSeg - 1)) == 0) {
-            // a segment starts: its x tile and its escape bytes
-            const int ls = chunk / kChunksPerSeg - s0;
-            const int sslot = ls & 1;
-            if (!hdr_ready) {
-                if (!mbar_wait(b.hdr, 0, deadline)) { failed = true; break; }
-                hdr_ready = true;
-            }
-            if (ls >= 2 && !mbar_wait(b.sempty + sslot, (uint32_t)((ls >> 1) - 1) & 1u, deadline)) {
-                failed = true;
-                break;
-            }
-            const uint4 meta = *reinterpret_cast<const uint4 *>(hdr + ls * kSegHdrBytes + 16);
-            const uint32_t base = meta.x;
-            const uint32_t total = seg_escape_total(meta);
-            uint32_t ebytes = 0, src0 = 0;
-            if (escapes_staged<C>(total)) {
-                src0 = base & ~15u;
-                ebytes = ((base + total + 15u) & ~15u) - src0;
-            }
-            mbar_arrive_expect_tx(b.sfull + sslot, (uint32_t)C::kXBytes + ebytes);
-            uint8_t *xs = smem + C::kOffX + sslot * C::kXBytes;
-#pragma unroll
-            for (int bx = 0; bx < 4; ++bx)
-                tma_load_2d(xs + bx * C::kXBoxBytes, tmap, chunk * kChunkK + bx * 64, 0, b.sfull + sslot);
-            if (ebytes)
-                bulk_g2s(smem + C::kOffEsc + sslot * C::kEscCap, p.blob + p.off_esc + src0, ebytes, b.sfull + sslot);
-            seg_issued = ls + 1;
-        }
+        // the stage's packed chunks first: they need nothing from the header
         const int slot = st % C::kStages;
         if (st >= C::kStages &&
             !mbar_wait(b.wempty + slot, (uint32_t)(st / C::kStages - 1) & 1u, deadline)) {
@@ -209,6 +181,36 @@ __device__ void gemm_producer(const GemmParams &p, const CUtensorMap *tmap, uint
                  p.blob + p.off_w + (uint64_t)(tile * p.chunks + chunk) * kChunkBytes, (uint32_t)(nch * kChunkBytes),
                  b.wfull + slot);
         issued = st + 1;
+        if ((chunk & (kChunksPerSeg - 1)) == 0) {
+            // a segment starts: its x tile (no header needed), then its escape
+            // bytes; the one arrival comes last so the phase cannot complete early
+            const int ls = chunk / kChunksPerSeg - s0;
+            const int sslot = ls & 1;
+            if (ls >= 2 && !mbar_wait(b.sempty + sslot, (uint32_t)((ls >> 1) - 1) & 1u, deadline)) {
+                failed = true;
+                break;
+            }
+            mbar_expect_tx(b.sfull + sslot, (uint32_t)C::kXBytes);
+            uint8_t *xs = smem + C::kOffX + sslot * C::kXBytes;
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx)
+                tma_load_2d(xs + bx * C::kXBoxBytes, tmap, chunk * kChunkK + bx * 64, 0, b.sfull + sslot);
+            seg_issued = ls + 1;
+            if (!hdr_ready) {
+                if (!mbar_wait(b.hdr, 0, deadline)) { failed = true; break; }
+                hdr_ready = true;
+            }
+            const uint4 meta = *reinterpret_cast<const uint4 *>(hdr + ls * kSegHdrBytes + 16);
+            const uint32_t base = meta.x;
+            const uint32_t total = seg_escape_total(meta);
+            if (escapes_staged<C>(total)) {
+                const uint32_t src0 = base & ~15u;
+                const uint32_t ebytes = ((base + total + 15u) & ~15u) - src0;
+                mbar_expect_tx(b.sfull + sslot, ebytes);
+                bulk_g2s(smem + C::kOffEsc + sslot * C::kEscCap, p.blob + p.off_esc + src0, ebytes, b.sfull + sslot);
+            }
+            mbar_arrive(b.sfull + sslot);
+        }
         if (*abort_flag) break;
     }
     if (failed) raise_timeout(p.status, abort_flag);
@@ -355,12 +357,22 @@ __device__ void gemm_decode(const GemmParams &p, uint8_t *smem, const Bars &b, v
         if (lane == 0) mbar_arrive(b.wempty + slot);  // this warp is done with the stage's bytes
 
         uint32_t out0[8], out1[8];
-        decode_half_chunk(T, sb0, cd0, h, (mask_q >> jj0) & 1u, run, out0);
-        if (nch == 2) {
-            decode_half_chunk(T, sb1, cd1, h, (mask_q >> (jj0 + 1)) & 1u, run, out1);
+        if (nch == 2 && ((mask_q >> jj0) & 3u) == 0) {
+            // common case, decided once per stage for the whole warp: two
+            // chunks without escapes
+            uint32_t E[4];
+            decode_exponents_half(T, h ? cd0.z : cd0.x, h ? cd0.w : cd0.y, E);
+            assemble_half(sb0, E, out0);
+            decode_exponents_half(T, h ? cd1.z : cd1.x, h ? cd1.w : cd1.y, E);
+            assemble_half(sb1, E, out1);
         } else {
+            decode_half_chunk(T, sb0, cd0, h, (mask_q >> jj0) & 1u, run, out0);
+            if (nch == 2) {
+                decode_half_chunk(T, sb1, cd1, h, (mask_q >> (jj0 + 1)) & 1u, run, out1);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) out1[i] = 0u;
+                for (int i = 0; i < 8; ++i) out1[i] = 0u;
+            }
         }
 
         if constexpr (!C::kASmem) {

@@ -109,31 +109,7 @@ __device__ void gemv_producer(const GemmParams &p, const CUtensorMap *tmap, uint
 
     for (int st = 0; st < nstages; ++st) {
         const int chunk = c0 + C::kStageChunks * st;
-        if ((chunk & (kChunksPerSeg - 1)) == 0) {
-            const int ls = chunk / kChunksPerSeg - s0;
-            const int sslot = ls & 1;
-            if (!hdr_ready) {
-                if (!mbar_wait(b.hdr, 0, deadline)) { failed = true; break; }
-                hdr_ready = true;
-            }
-            if (ls >= 2 && !mbar_wait(b.sempty + sslot, (uint32_t)((ls >> 1) - 1) & 1u, deadline)) {
-                failed = true;
-                break;
-            }
-            const uint4 meta = *reinterpret_cast<const uint4 *>(hdr + ls * kSegHdrBytes + 16);
-            const uint32_t base = meta.x;
-            const uint32_t total = seg_escape_total(meta);
-            uint32_t ebytes = 0, src0 = 0;
-            if (escapes_staged<C>(total)) {
-                src0 = base & ~15u;
-                ebytes = ((base + total + 15u) & ~15u) - src0;
-            }
-            mbar_arrive_expect_tx(b.sfull + sslot, (uint32_t)C::kXbBytes + ebytes);
-            tma_load_2d(smem + C::kOffXb + sslot * C::kXbBytes, tmap, chunk * kChunkK, 0, b.sfull + sslot);
-            if (ebytes)
-                bulk_g2s(smem + C::kOffEsc + sslot * C::kEscCap, p.blob + p.off_esc + src0, ebytes, b.sfull + sslot);
-            seg_issued = ls + 1;
-        }
+        // the stage's packed chunks first: they need nothing from the header
         const int slot = st % C::kStages;
         if (st >= C::kStages &&
             !mbar_wait(b.wempty + slot, (uint32_t)(st / C::kStages - 1) & 1u, deadline)) {
@@ -146,6 +122,33 @@ __device__ void gemv_producer(const GemmParams &p, const CUtensorMap *tmap, uint
                  p.blob + p.off_w + (uint64_t)(tile * p.chunks + chunk) * kChunkBytes, (uint32_t)(nch * kChunkBytes),
                  b.wfull + slot);
         issued = st + 1;
+        if ((chunk & (kChunksPerSeg - 1)) == 0) {
+            // a segment starts: its x (no header needed), then its escapes;
+            // the one arrival comes last so the phase cannot complete early
+            const int ls = chunk / kChunksPerSeg - s0;
+            const int sslot = ls & 1;
+            if (ls >= 2 && !mbar_wait(b.sempty + sslot, (uint32_t)((ls >> 1) - 1) & 1u, deadline)) {
+                failed = true;
+                break;
+            }
+            mbar_expect_tx(b.sfull + sslot, (uint32_t)C::kXbBytes);
+            tma_load_2d(smem + C::kOffXb + sslot * C::kXbBytes, tmap, chunk * kChunkK, 0, b.sfull + sslot);
+            seg_issued = ls + 1;
+            if (!hdr_ready) {
+                if (!mbar_wait(b.hdr, 0, deadline)) { failed = true; break; }
+                hdr_ready = true;
+            }
+            const uint4 meta = *reinterpret_cast<const uint4 *>(hdr + ls * kSegHdrBytes + 16);
+            const uint32_t base = meta.x;
+            const uint32_t total = seg_escape_total(meta);
+            if (escapes_staged<C>(total)) {
+                const uint32_t src0 = base & ~15u;
+                const uint32_t ebytes = ((base + total + 15u) & ~15u) - src0;
+                mbar_expect_tx(b.sfull + sslot, ebytes);
+                bulk_g2s(smem + C::kOffEsc + sslot * C::kEscCap, p.blob + p.off_esc + src0, ebytes, b.sfull + sslot);
+            }
+            mbar_arrive(b.sfull + sslot);
+        }
         if (*abort_flag) break;
     }
     if (failed) raise_timeout(p.status, abort_flag);
@@ -223,12 +226,25 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
         __syncwarp();
         if (lane == 0) mbar_arrive(b.wempty + slot);
 
+        const uint32_t stage_esc = (mask_q >> jj0) & ((1u << C::kStageChunks) - 1u);
+        if (nch == C::kStageChunks && stage_esc == 0) {
+            // common case, decided once per stage for the whole warp: a full
+            // stage without escapes
 #pragma unroll
-        for (int e = 0; e < C::kStageChunks; ++e) {
-            if (e < nch) {
-                uint32_t out[8];
-                decode_half_chunk(T, sb[e], cd[e], h, (mask_q >> (jj0 + e)) & 1u, run, out);
+            for (int e = 0; e < C::kStageChunks; ++e) {
+                uint32_t E[4], out[8];
+                decode_exponents_half(T, h ? cd[e].z : cd[e].x, h ? cd[e].w : cd[e].y, E);
+                assemble_half(sb[e], E, out);
                 dot16(out, xseg + (uint32_t)((jj0 + e) * kChunkK * 4), acc0, acc1);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < C::kStageChunks; ++e) {
+                if (e < nch) {
+                    uint32_t out[8];
+                    decode_half_chunk(T, sb[e], cd[e], h, (stage_esc >> e) & 1u, run, out);
+                    dot16(out, xseg + (uint32_t)((jj0 + e) * kChunkK * 4), acc0, acc1);
+                }
             }
         }
         if (jj0 + nch == kChunksPerSeg || st == nstages - 1) {

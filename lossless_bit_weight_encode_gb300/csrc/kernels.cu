@@ -4,6 +4,7 @@
 // (g_w12_status, static device memory: no allocation) is one symbol per device.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -78,6 +79,29 @@ int cuda_fail(cudaError_t e, const char *what, std::string *err) {
     return W12_ERR_CUDA;
 }
 
+// Resident CTAs per SM from the kernel's own limits: registers (allocated per
+// warp in units of 256), dynamic shared memory (+1 KB reserved per CTA) and
+// threads.  The runtime's occupancy query is taken when it reports more.
+int resident_ctas(const void *kernel, int threads, int smem_bytes, int device, std::string *err, int *out) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes", err);
+    int regs_sm = 0, smem_sm = 0, threads_sm = 0;
+    cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, device);
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device);
+    cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, device);
+    const int warps = (threads + 31) / 32;
+    const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+    int occ = regs_warp > 0 ? regs_sm / (warps * regs_warp) : 1;
+    occ = std::min(occ, smem_sm / (smem_bytes + 1024));
+    occ = std::min(occ, threads_sm / threads);
+    int api = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&api, kernel, threads, (size_t)smem_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor", err);
+    *out = std::max(std::max(occ, api), 1);
+    return W12_OK;
+}
+
 template <int NTOK, bool ASMEM>
 int prepare_gemm(DeviceState &s, std::string *err) {
     void *k = gemm_kernel_ptr<NTOK, ASMEM>();
@@ -88,9 +112,9 @@ int prepare_gemm(DeviceState &s, std::string *err) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(carveout)", err);
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, dev::GemmCfg<NTOK, kStages, ASMEM>::kThreads,
-                                                      (size_t)gemm_smem_bytes<NTOK, ASMEM>());
-    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor", err);
+    const int rc = resident_ctas(k, dev::GemmCfg<NTOK, kStages, ASMEM>::kThreads, gemm_smem_bytes<NTOK, ASMEM>(),
+                                 s.device, err, &occ);
+    if (rc != W12_OK) return rc;
     // TMEM: each CTA holds 128 of the SM's 512 columns
     s.occupancy[NTOK == 32][ASMEM] = occ < 4 ? occ : 4;
     return W12_OK;
@@ -107,8 +131,8 @@ int prepare_gemv(DeviceState &s, std::string *err) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemv carveout)", err);
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, GemvC::kThreads, (size_t)GemvC::kSmemBytes);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(gemv)", err);
+    const int rc = resident_ctas(k, GemvC::kThreads, GemvC::kSmemBytes, s.device, err, &occ);
+    if (rc != W12_OK) return rc;
     s.gemv_occupancy = occ < 8 ? occ : 8;
     return W12_OK;
 }
