@@ -87,7 +87,7 @@ def hbm_peak_gbs():
 def recorded_traffic():
     """Per-launch DRAM bytes of the GEMM kernel from the committed ncu summary,
     only while the kernel sources still hash to what was profiled."""
-    path = os.path.join(ROOT, "profiles", "gemm_tc_traffic.json")
+    path = os.path.join(ROOT, "profiles", "w12_layer_m1_traffic.json")
     if not os.path.exists(path):
         return None
     try:
