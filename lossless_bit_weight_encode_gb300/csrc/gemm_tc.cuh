@@ -100,9 +100,12 @@ struct Bars {
     uint64_t *wfull, *wempty, *sfull, *sempty, *afull, *aempty, *hdr, *accum, *drain, *epi_in, *epi_out;
 };
 
-// One lane waits (bounded); the result is broadcast and __syncwarp orders the
-// other lanes after the completed phase.
+// Whole-warp wait.  Usually the phase has already completed and one try_wait
+// by every lane settles it (no branch, no shuffle); otherwise one lane waits
+// (bounded), the result is broadcast and __syncwarp orders the other lanes
+// after the completed phase.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t deadline) {
+    if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
     uint32_t ok = 0;
     if ((threadIdx.x & 31u) == 0) ok = mbar_wait(bar, parity, deadline) ? 1u : 0u;
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -284,8 +287,10 @@ __device__ void gemm_mma(const GemmParams &p, uint8_t *smem, const Bars &b, vola
 __device__ __forceinline__ void decode_half_chunk(const Table &T, const uint4 &sb, const uint4 &codes, int h,
                                                   bool has_escapes, const uint8_t *&run, uint32_t (&out)[8]) {
     uint32_t E[4];
-    decode_exponents_half(T, h ? codes.z : codes.x, h ? codes.w : codes.y, E);
-    if (has_escapes) run += warp_escapes_half(codes, h, run, E);
+    if (has_escapes)
+        run += decode_exponents_half_esc(T, codes, h, run, E);
+    else
+        decode_exponents_half(T, h ? codes.z : codes.x, h ? codes.w : codes.y, E);
     assemble_half(sb, E, out);
 }
 
@@ -353,8 +358,7 @@ __device__ void gemm_decode(const GemmParams &p, uint8_t *smem, const Bars &b, v
             sb1 = lds128(sa + kChunkBytes);
             cd1 = lds128(sa + kChunkBytes + c_off);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b.wempty + slot);  // this warp is done with the stage's bytes
+        warp_arrive(b.wempty + slot);  // this warp is done with the stage's bytes
 
         uint32_t out0[8], out1[8];
         if (nch == 2 && ((mask_q >> jj0) & 3u) == 0) {

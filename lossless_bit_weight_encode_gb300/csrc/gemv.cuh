@@ -223,8 +223,7 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
                 cd[e] = lds128(sa + (uint32_t)(e * kChunkBytes) + c_off);
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b.wempty + slot);
+        warp_arrive(b.wempty + slot);
 
         const uint32_t stage_esc = (mask_q >> jj0) & ((1u << C::kStageChunks) - 1u);
         if (nch == C::kStageChunks && stage_esc == 0) {
@@ -248,8 +247,7 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
             }
         }
         if (jj0 + nch == kChunksPerSeg || st == nstages - 1) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b.sempty + sslot);  // done with this segment's x and escapes
+            warp_arrive(b.sempty + sslot);  // done with this segment's x and escapes
         }
     }
     if (!ok) {

@@ -431,20 +431,54 @@ __device__ __forceinline__ void patch_half(uint32_t f0, uint32_t f1, const uint8
     }
 }
 
-// Escape step for half h of a quarter-chunk.  The escape run orders a row's
-// 32 columns together, so the lane prefix is taken over whole-row counts and
-// the second half starts after the row's first-half escapes.  Returns the
-// warp's escape count over the whole chunk (both halves).
-__device__ __forceinline__ uint32_t warp_escapes_half(const uint4 &codes, int h, const uint8_t *run,
-                                                      uint32_t (&E)[4]) {
+// Escape step for half h of a quarter-chunk, before the exponent lookup.  The
+// escape run orders a row's 32 columns together, so the lane prefix is taken
+// over whole-row counts and the second half starts after the row's first-half
+// escapes.  Common case: no lane holds more than one escape in its 16 columns.
+// Then a lane with one escape puts that exponent into slot 15 of its own copy
+// of the table, and the ordinary lookup decodes it.  Slot 15 is looked up as
+// sign(slot 7) ^ slot 15, and slot 7 as slot 7 ^ sign(slot 15), so this holds
+// when the escaped exponent has the same top bit as T[7].  Otherwise the
+// exponents are patched after the lookup.  Returns the warp's escape count
+// over the whole chunk (to advance the run).
+__device__ __forceinline__ uint32_t decode_exponents_half_esc(const Table &T, const uint4 &codes, int h,
+                                                             const uint8_t *run, uint32_t (&E)[4]) {
     const uint32_t f[4] = {escape_flags(codes.x), escape_flags(codes.y), escape_flags(codes.z),
                            escape_flags(codes.w)};
     const uint32_t c0 = __popc(f[0]) + __popc(f[1]);
     const uint32_t cnt = c0 + __popc(f[2]) + __popc(f[3]);
     uint32_t excl, total;
     lane_prefix(cnt, excl, total);
-    patch_half(h ? f[2] : f[0], h ? f[3] : f[1], run + excl + (h ? c0 : 0u), E);
+    const uint32_t fh0 = h ? f[2] : f[0], fh1 = h ? f[3] : f[1];
+    const uint32_t mine = __popc(fh0) + __popc(fh1);
+    const uint8_t *src = run + excl + (h ? c0 : 0u);
+    Table Tl = T;
+    bool ok = mine <= 1u;
+    if (mine == 1u) {
+        const uint32_t e = *src;
+        const uint32_t sign7 = (T.u1 & 0x80000000u) ? 0xFFu : 0u;  // top bit of slot 7
+        ok = ((e ^ sign7) & 0x80u) == 0u;
+        Tl.u3 = (T.u3 & 0x00FFFFFFu) | ((e ^ sign7) << 24);
+    }
+    const uint32_t w0 = h ? codes.z : codes.x, w1 = h ? codes.w : codes.y;
+    if (__all_sync(0xFFFFFFFFu, ok)) {
+        decode_exponents_half(Tl, w0, w1, E);
+    } else {
+        decode_exponents_half(T, w0, w1, E);
+        patch_half(fh0, fh1, src, E);
+    }
     return total;
+}
+
+// Arrive on an mbarrier once for the whole warp (after ordering every lane's
+// earlier accesses), without a divergent branch.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+    __syncwarp();
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
 }
 
 }  // namespace dev
