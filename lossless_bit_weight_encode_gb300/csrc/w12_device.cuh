@@ -438,8 +438,9 @@ __device__ __forceinline__ void patch_half(uint32_t f0, uint32_t f1, const uint8
 // Then a lane with one escape puts that exponent into slot 15 of its own copy
 // of the table, and the ordinary lookup decodes it.  Slot 15 is looked up as
 // sign(slot 7) ^ slot 15, and slot 7 as slot 7 ^ sign(slot 15), so this holds
-// when the escaped exponent has the same top bit as T[7].  Otherwise the
-// exponents are patched after the lookup.  Returns the warp's escape count
+// when the escaped exponent has the same top bit as T[7], or when the lane has
+// no code 7 to get wrong.  Otherwise the exponents are patched after the
+// lookup.  Returns the warp's escape count
 // over the whole chunk (to advance the run).
 __device__ __forceinline__ uint32_t decode_exponents_half_esc(const Table &T, const uint4 &codes, int h,
                                                              const uint8_t *run, uint32_t (&E)[4]) {
@@ -453,14 +454,17 @@ __device__ __forceinline__ uint32_t decode_exponents_half_esc(const Table &T, co
     const uint32_t mine = __popc(fh0) + __popc(fh1);
     const uint8_t *src = run + excl + (h ? c0 : 0u);
     Table Tl = T;
+    const uint32_t w0 = h ? codes.z : codes.x, w1 = h ? codes.w : codes.y;
     bool ok = mine <= 1u;
     if (mine == 1u) {
         const uint32_t e = *src;
         const uint32_t sign7 = (T.u1 & 0x80000000u) ? 0xFFu : 0u;  // top bit of slot 7
-        ok = ((e ^ sign7) & 0x80u) == 0u;
+        // a top-bit mismatch only breaks code 7, which is harmless when none of
+        // this lane's 16 codes is 7 (code ^ 8 == 15)
+        const bool no_code7 = (escape_flags(w0 ^ 0x88888888u) | escape_flags(w1 ^ 0x88888888u)) == 0u;
+        ok = ((e ^ sign7) & 0x80u) == 0u || no_code7;
         Tl.u3 = (T.u3 & 0x00FFFFFFu) | ((e ^ sign7) << 24);
     }
-    const uint32_t w0 = h ? codes.z : codes.x, w1 = h ? codes.w : codes.y;
     if (__all_sync(0xFFFFFFFFu, ok)) {
         decode_exponents_half(Tl, w0, w1, E);
     } else {
