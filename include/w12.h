@@ -107,6 +107,8 @@ int w12_encode_host(const uint16_t *w_host, int64_t N, int64_t K, void *blob_hos
  * Read and check the header of a host blob of `bytes` bytes and fill *out.
  * Checks magic, version and every geometry field against N and K (CORRUPT_BLOB
  * on mismatch, BUFFER_TOO_SMALL if the blob is shorter than its total size).
+ * Only the first 256 bytes are read: for a blob held on the device, a host
+ * copy of its header with `bytes` = the device blob's length is enough.
  */
 int w12_blob_info(const void *blob_host, size_t bytes, w12_info *out);
 
@@ -189,9 +191,44 @@ int w12_gemm_noalloc(const uint16_t *x_dev, const void *blob_dev, const w12_info
                      uint16_t *y_dev, int M, void *stream);
 
 /*
+ * Device encoder: the same canonical bytes as w12_encode_host, computed on the
+ * GPU from weights already in device memory (for example a whole model
+ * checkpoint loaded to HBM, encoded without a round trip through the host).
+ * It produces the format the pages call lossless and bit-exact ("SpecPilot"
+ * (fasttoolhub.com) §Differentiation; "StargazerX0/SpecPilot" §What it is);
+ * the pages do not say where the encoding runs.
+ *
+ * w12_encode_workspace_size: scratch bytes both calls below need for N x K
+ *   (one 32-byte plan record and one 8-byte offset per 128 x 256 segment, plus
+ *   256).  SHAPE as for w12_encoded_size_host.
+ * w12_encoded_size_device: runs the encoder's table and escape-count passes on
+ *   `stream` over w_dev (N x K row-major BF16 bit patterns, 2-byte aligned;
+ *   16-byte aligned with K % 8 == 0 reads faster), then SYNCHRONISES `stream`
+ *   and stores the exact blob size (equal to w12_encoded_size_host's) in
+ *   *bytes.  SHAPE if the matrix has more than 2^32-1 escapes.
+ * w12_encode_device: writes the whole blob into blob_dev (256-byte aligned,
+ *   `bytes` long), asynchronously on `stream`; it repeats the table pass, so
+ *   it needs no state from the size call.  A buffer shorter than the packed
+ *   planes is refused on the host (BUFFER_TOO_SMALL); a buffer too short for
+ *   the escape bytes is found on the device: nothing is written past `bytes`,
+ *   the header is not written and w12_check_status returns BUFFER_TOO_SMALL
+ *   (SHAPE for more than 2^32-1 escapes).  workspace: 256-byte aligned, at
+ *   least w12_encode_workspace_size bytes, no initial contents; calls sharing
+ *   one workspace must be ordered on the GPU.
+ */
+int w12_encode_workspace_size(int64_t N, int64_t K, size_t *bytes);
+
+int w12_encoded_size_device(const uint16_t *w_dev, int64_t N, int64_t K, void *workspace,
+                            size_t ws_bytes, size_t *bytes, void *stream);
+
+int w12_encode_device(const uint16_t *w_dev, int64_t N, int64_t K, void *blob_dev, size_t bytes,
+                      void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's status word,
- * which kernels set when a bounded wait gives up.  Returns TIMEOUT if it was
- * set, CUDA on a CUDA error, else OK.
+ * which kernels set when a bounded wait gives up (TIMEOUT) or the device
+ * encoder finds its output buffer too short (BUFFER_TOO_SMALL) or too many
+ * escapes (SHAPE).  Returns that status, CUDA on a CUDA error, else OK.
  */
 int w12_check_status(void *stream);
 

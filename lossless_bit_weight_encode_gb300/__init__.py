@@ -33,6 +33,26 @@ class W12Weight:
         self.blob = torch.from_numpy(self.blob_host).to(dev)
         self._ws = {}
 
+    @classmethod
+    def from_device(cls, w, stream=None) -> "W12Weight":
+        """Encode a BF16 device tensor [N, K] on its GPU (same bytes as the
+        host encoder); only the 256-byte header comes back to the host."""
+        import torch
+
+        N, K = int(w.shape[0]), int(w.shape[1])
+        ws = torch.empty(w12.w12_encode_workspace_size(N, K), dtype=torch.uint8, device=w.device)
+        size = w12.w12_encoded_size_device(w, ws, stream)
+        blob = torch.empty(size, dtype=torch.uint8, device=w.device)
+        w12.w12_encode_device(w, blob, ws, stream)
+        w12.w12_check_status(stream)
+        self = cls.__new__(cls)
+        self.blob_host = None
+        self.info = w12.w12_blob_info(blob[:256].cpu().numpy(), size)
+        self.N, self.K = int(self.info.N), int(self.info.K)
+        self.blob = blob
+        self._ws = {}
+        return self
+
     @property
     def bits_per_weight(self) -> float:
         return float(self.info.bits_per_weight)

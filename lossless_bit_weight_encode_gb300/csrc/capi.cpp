@@ -190,6 +190,46 @@ int w12_gemm_noalloc(const uint16_t *x_dev, const void *blob_dev, const w12_info
     });
 }
 
+int w12_encode_workspace_size(int64_t N, int64_t K, size_t *bytes) {
+    return guarded([&](std::string &err) {
+        if (!bytes) {
+            err = "null pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        return w12::launch::encode_workspace_size(N, K, bytes, &err);
+    });
+}
+
+int w12_encoded_size_device(const uint16_t *w_dev, int64_t N, int64_t K, void *workspace, size_t ws_bytes,
+                            size_t *bytes, void *stream) {
+    return guarded([&](std::string &err) {
+        if (!w_dev || !workspace || !bytes) {
+            err = "null pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (!aligned(w_dev, 2) || !aligned(workspace, 256)) {
+            err = "w_dev must be 2-byte aligned and workspace 256-byte aligned";
+            return (int)W12_ERR_ALIGNMENT;
+        }
+        return w12::launch::encoded_size_device(w_dev, N, K, workspace, ws_bytes, bytes, stream, &err);
+    });
+}
+
+int w12_encode_device(const uint16_t *w_dev, int64_t N, int64_t K, void *blob_dev, size_t bytes, void *workspace,
+                      size_t ws_bytes, void *stream) {
+    return guarded([&](std::string &err) {
+        if (!w_dev || !blob_dev || !workspace) {
+            err = "null device pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (!aligned(w_dev, 2) || !aligned(blob_dev, 256) || !aligned(workspace, 256)) {
+            err = "w_dev must be 2-byte aligned, blob_dev and workspace 256-byte aligned";
+            return (int)W12_ERR_ALIGNMENT;
+        }
+        return w12::launch::encode_device(w_dev, N, K, blob_dev, bytes, workspace, ws_bytes, stream, &err);
+    });
+}
+
 int w12_check_status(void *stream) {
     return guarded([&](std::string &err) { return w12::launch::check_status(stream, &err); });
 }

@@ -209,6 +209,8 @@ void write_segment(const uint16_t *w, const Geometry &g, int64_t tile, int64_t s
     }
 }
 
+}  // namespace
+
 bool check_shape(int64_t N, int64_t K, std::string *err) {
     // Keeps every offset well inside 63 bits and N*K representable.
     if (N < 1 || K < 1 || N > (int64_t(1) << 31) || K > (int64_t(1) << 31) ||
@@ -218,8 +220,6 @@ bool check_shape(int64_t N, int64_t K, std::string *err) {
     }
     return true;
 }
-
-}  // namespace
 
 int encoded_size(const uint16_t *w, int64_t N, int64_t K, uint64_t *bytes, std::string *err) {
     if (!w || !bytes) {

@@ -11,8 +11,10 @@
 #include <utility>
 
 #include "decode.cuh"
+#include "encode_gpu.cuh"
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
+#include "w12_host.hpp"
 #include "w12_launch.hpp"
 
 namespace w12 {
@@ -400,10 +402,122 @@ int check_status(void *stream, std::string *err) {
     if (v != 0) {
         const uint32_t zero = 0;
         cudaMemcpy(s->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
-        *err = "a W12 kernel gave up a bounded wait (status word " + std::to_string(v) + ")";
-        return W12_ERR_TIMEOUT;
+        const std::string word = " (status word " + std::to_string(v) + ")";
+        if (v & dev::kStatusTimeout) {
+            *err = "a W12 kernel gave up a bounded wait" + word;
+            return W12_ERR_TIMEOUT;
+        }
+        if (v & dev::kStatusEncodeOverflow) {
+            *err = "w12_encode_device: the blob buffer is shorter than the encoding" + word;
+            return W12_ERR_BUFFER_TOO_SMALL;
+        }
+        *err = "w12_encode_device: more than 2^32-1 escapes, split the matrix" + word;
+        return W12_ERR_SHAPE;
     }
     return W12_OK;
+}
+
+// ---------------------------------------------------------------- encoder
+namespace {
+
+struct EncodeLayout {
+    size_t plan = 0, base = 0, n_esc = 0, bytes = 0;
+};
+
+EncodeLayout encode_layout(const Geometry &g) {
+    const size_t nseg = (size_t)(g.tiles * g.segs);
+    EncodeLayout l;
+    l.plan = 0;
+    l.base = up256(nseg * 32);
+    l.n_esc = l.base + up256(nseg * sizeof(uint64_t));
+    l.bytes = l.n_esc + 256;
+    return l;
+}
+
+int encode_launch(const uint16_t *w_dev, int64_t N, int64_t K, uint8_t *blob_dev, size_t cap, void *workspace,
+                  size_t ws_bytes, bool write, void *stream, std::string *err) {
+    if (!host::check_shape(N, K, err)) return W12_ERR_SHAPE;
+    DeviceState *s = nullptr;
+    int rc = device_state(&s, err);
+    if (rc != W12_OK) return rc;
+    const Geometry g = Geometry::of(N, K);
+    const EncodeLayout l = encode_layout(g);
+    if (ws_bytes < l.bytes) {
+        *err = "encoder workspace smaller than w12_encode_workspace_size";
+        return W12_ERR_BUFFER_TOO_SMALL;
+    }
+    if (write && cap < g.off_esc) {
+        *err = "blob buffer smaller than the encoded size";
+        return W12_ERR_BUFFER_TOO_SMALL;
+    }
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    dev::EncodeParams p;
+    p.w = w_dev;
+    p.N = g.N;
+    p.K = g.K;
+    p.Kp = g.Kpad;
+    p.tiles = g.tiles;
+    p.chunks = g.chunks;
+    p.segs = g.segs;
+    p.vec = ((reinterpret_cast<uintptr_t>(w_dev) & 15) == 0 && K % 8 == 0) ? 1 : 0;
+    p.plan = ws + l.plan;
+    p.base = reinterpret_cast<uint64_t *>(ws + l.base);
+    p.n_esc = reinterpret_cast<uint64_t *>(ws + l.n_esc);
+    p.blob = blob_dev;
+    p.blob_bytes = cap;
+    p.off_seg = g.off_seg;
+    p.off_w = g.off_w;
+    p.off_esc = g.off_esc;
+    p.status = s->status;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t nseg = g.tiles * g.segs;
+    // plan: 34 KB of shared memory per CTA, several CTAs per SM
+    const int grid = (int)std::min<int64_t>(nseg, (int64_t)s->sm_count * 6);
+    dev::w12_encode_plan_kernel<<<grid, 256, 0, st>>>(p);
+    dev::w12_encode_scan_kernel<<<1, 1024, 0, st>>>(p);
+    if (write) {
+        const int wgrid = (int)std::min<int64_t>(nseg, (int64_t)s->sm_count * 16);
+        dev::w12_encode_write_kernel<<<wgrid, 128, 0, st>>>(p);
+        dev::w12_encode_header_kernel<<<1, 256, 0, st>>>(p);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "encoder launch", err);
+    return W12_OK;
+}
+
+}  // namespace
+
+int encode_workspace_size(int64_t N, int64_t K, size_t *bytes, std::string *err) {
+    if (!host::check_shape(N, K, err)) return W12_ERR_SHAPE;
+    *bytes = encode_layout(Geometry::of(N, K)).bytes;
+    return W12_OK;
+}
+
+int encoded_size_device(const uint16_t *w_dev, int64_t N, int64_t K, void *workspace, size_t ws_bytes,
+                        size_t *bytes, void *stream, std::string *err) {
+    int rc = encode_launch(w_dev, N, K, nullptr, 0, workspace, ws_bytes, false, stream, err);
+    if (rc != W12_OK) return rc;
+    const Geometry g = Geometry::of(N, K);
+    const EncodeLayout l = encode_layout(g);
+    uint64_t n_esc = 0;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&n_esc, static_cast<uint8_t *>(workspace) + l.n_esc, sizeof n_esc,
+                                    cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the escape count", err);
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize", err);
+    if (n_esc > 0xFFFFFFFFull) {
+        *err = "more than 2^32-1 escapes: split the matrix";
+        return W12_ERR_SHAPE;
+    }
+    *bytes = (size_t)g.total(n_esc);
+    return W12_OK;
+}
+
+int encode_device(const uint16_t *w_dev, int64_t N, int64_t K, void *blob_dev, size_t cap, void *workspace,
+                  size_t ws_bytes, void *stream, std::string *err) {
+    return encode_launch(w_dev, N, K, static_cast<uint8_t *>(blob_dev), cap, workspace, ws_bytes, true, stream,
+                         err);
 }
 
 // ---------------------------------------------------------------- no-alloc

@@ -33,6 +33,14 @@ int gemm_noalloc(const uint16_t *x_dev, const void *blob_dev, const w12_info &in
 
 int check_status(void *stream, std::string *err);
 
+int encode_workspace_size(int64_t N, int64_t K, size_t *bytes, std::string *err);
+
+int encoded_size_device(const uint16_t *w_dev, int64_t N, int64_t K, void *workspace, size_t ws_bytes,
+                        size_t *bytes, void *stream, std::string *err);
+
+int encode_device(const uint16_t *w_dev, int64_t N, int64_t K, void *blob_dev, size_t cap, void *workspace,
+                  size_t ws_bytes, void *stream, std::string *err);
+
 int selftest_timeout(uint32_t timeout_us, void *stream, std::string *err);
 
 }  // namespace launch

@@ -25,7 +25,7 @@ STATUS_NAMES = {
 EXPORTED = (
     "w12_last_error", "w12_status_string", "w12_format_version", "w12_encoded_size_host", "w12_encode_host",
     "w12_blob_info", "w12_blob_validate", "w12_decode", "w12_gemm_workspace_size", "w12_gemm_launch_info",
-    "w12_gemm", "w12_gemm_noalloc",
+    "w12_gemm", "w12_gemm_noalloc", "w12_encode_workspace_size", "w12_encoded_size_device", "w12_encode_device",
     "w12_check_status", "w12_selftest_timeout",
 )
 
@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
     L.w12_gemm_launch_info.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(ctypes.c_int32)]
     L.w12_gemm.argtypes = [vp, vp, ctypes.POINTER(w12_info), vp, i32, vp, sz, vp]
     L.w12_gemm_noalloc.argtypes = [vp, vp, ctypes.POINTER(w12_info), vp, i32, vp]
+    L.w12_encode_workspace_size.argtypes = [i64, i64, ctypes.POINTER(sz)]
+    L.w12_encoded_size_device.argtypes = [vp, i64, i64, vp, sz, ctypes.POINTER(sz), vp]
+    L.w12_encode_device.argtypes = [vp, i64, i64, vp, sz, vp, sz, vp]
     L.w12_check_status.argtypes = [vp]
     L.w12_selftest_timeout.argtypes = [ctypes.c_uint32, vp]
     for name in EXPORTED[3:]:
@@ -124,10 +127,15 @@ def w12_encode_host(w: np.ndarray) -> np.ndarray:
     return blob
 
 
-def w12_blob_info(blob: np.ndarray) -> w12_info:
+def w12_blob_info(blob: np.ndarray, blob_bytes: int | None = None) -> w12_info:
+    """Header of a host blob; `blob` may be just the 256-byte header of a
+    device blob when `blob_bytes` gives that blob's length."""
     blob = np.ascontiguousarray(blob, dtype=np.uint8)
+    if blob_bytes is not None and blob.size < 256:
+        raise ValueError("the header copy must hold 256 bytes")
     info = w12_info()
-    _check(lib().w12_blob_info(blob.ctypes.data, blob.size, ctypes.byref(info)))
+    _check(lib().w12_blob_info(blob.ctypes.data, blob.size if blob_bytes is None else int(blob_bytes),
+                               ctypes.byref(info)))
     return info
 
 
@@ -173,6 +181,38 @@ def w12_gemm_noalloc(x_dev, blob_dev, info: w12_info, y_dev, M: int, stream=None
     scratch is used (see include/w12.h); nothing is allocated."""
     _check(lib().w12_gemm_noalloc(x_dev.data_ptr(), blob_dev.data_ptr(), ctypes.byref(info), y_dev.data_ptr(),
                                   int(M), _stream_handle(stream)))
+
+
+def _dev_u16(w) -> tuple[int, int]:
+    import torch
+    if w.dim() != 2 or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16) or not w.is_contiguous():
+        raise TypeError("weights must be a contiguous 2-D BF16 (or 16-bit integer) device tensor")
+    return int(w.shape[0]), int(w.shape[1])
+
+
+def w12_encode_workspace_size(N: int, K: int) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().w12_encode_workspace_size(int(N), int(K), ctypes.byref(out)))
+    return out.value
+
+
+def w12_encoded_size_device(w_dev, workspace, stream=None) -> int:
+    """Exact blob size of the device weights `w_dev` (synchronises the stream)."""
+    N, K = _dev_u16(w_dev)
+    out = ctypes.c_size_t()
+    _check(lib().w12_encoded_size_device(w_dev.data_ptr(), N, K, workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(), ctypes.byref(out),
+                                         _stream_handle(stream)))
+    return out.value
+
+
+def w12_encode_device(w_dev, blob_dev, workspace, stream=None, nbytes: int | None = None) -> None:
+    """Encode `w_dev` into the uint8 device tensor `blob_dev` (asynchronous;
+    device-side errors surface through w12_check_status)."""
+    N, K = _dev_u16(w_dev)
+    cap = blob_dev.numel() if nbytes is None else int(nbytes)
+    _check(lib().w12_encode_device(w_dev.data_ptr(), N, K, blob_dev.data_ptr(), cap, workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), _stream_handle(stream)))
 
 
 def w12_check_status(stream=None) -> None:

@@ -94,6 +94,34 @@ def all_bf16_patterns(shuffle_seed: int | None = None) -> np.ndarray:
     return v.reshape(256, 256)
 
 
+def table_rule_weights(seed: int) -> np.ndarray:
+    """2048 x 4096 BF16 patterns: the 128 x 256 block at (tile t, segment s)
+    draws its exponents from t distinct values below 128 and s distinct values
+    from 128 up, so the blocks cover every split of the table between the two
+    halves, more than 15 distinct exponents, and (every other block) exactly
+    equal counts, where the ranking falls to the smaller exponent.  Signs and
+    mantissas are uniform."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    w = np.empty((2048, 4096), dtype=np.uint16)
+    cells = 128 * 256
+    for t in range(16):
+        for s in range(16):
+            low = rng.choice(np.arange(0, 128), size=t, replace=False)
+            high = rng.choice(np.arange(128, 256), size=s, replace=False)
+            exps = np.concatenate([low, high]).astype(np.uint16)
+            if exps.size == 0:
+                exps = np.array([0], dtype=np.uint16)
+            if (t + s) % 2 == 0:
+                counts = np.full(exps.size, cells // exps.size)
+                counts[: cells % exps.size] += 1
+            else:
+                counts = rng.multinomial(cells, rng.dirichlet(np.ones(exps.size)))
+            e = rng.permutation(np.repeat(exps, counts)).reshape(128, 256)
+            sm = rng.integers(0, 1 << 16, size=(128, 256), dtype=np.uint32).astype(np.uint16) & np.uint16(0x807F)
+            w[128 * t:128 * (t + 1), 256 * s:256 * (s + 1)] = sm | (e << np.uint16(7))
+    return w
+
+
 def weight_seed(workload: str, index: int) -> int:
     wid = WORKLOAD_IDS[workload]
     if workload == "layer_sweep":

@@ -51,6 +51,7 @@ CASES = {
     "forced100": lambda: wl.forced_escape_weights(128, 512, 1.0, seed=6),
     "zeros": lambda: np.zeros((200, 300), dtype=np.uint16),
     "big_exponents": lambda: (wl.gaussian_weights(256, 512, seed=7) | np.uint16(0x4000)),
+    "table_rule": lambda: wl.table_rule_weights(8),
 }
 
 
