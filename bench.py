@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
     ap.add_argument("--m", type=int, default=1, help="tokens per GEMM (1..32)")
-    ap.add_argument("--workload", default="layer", choices=["layer", "heavy"])
+    ap.add_argument("--workload", default="layer", choices=["layer", "heavy", "model64"])
     ap.add_argument("--graph", action="store_true", help="replay the step as a CUDA graph")
     ap.add_argument("--no-bf16", action="store_true", help="skip the cuBLAS BF16 comparator")
     ap.add_argument("--no-e2e", action="store_true")
@@ -157,6 +157,15 @@ class ClockSampler:
                                                      if r[3].replace(".", "").isdigit()] or [0.0])}
 
 
+WORKLOAD_TEXT = {
+    "layer": "layer: 27B-class decoder layer (q 6144x5120, k/v 1024x5120, o 5120x6144, gate/up 17408x5120, "
+             "down 5120x17408; 340.8 M weights), weights N(0,0.02)",
+    "heavy": "heavy: layer shapes, Student-t(3)*0.02 weights with 0.5% x100 outliers",
+    "model64": "model64: 64 layers of the 27B-class shapes chained in layer order (448 GEMMs, 21.8 G weights, "
+               "32.7 GB of W12 resident), weights N(0,0.02) drawn and encoded on the GPU",
+}
+
+
 # ------------------------------------------------------------------ CPU oracle
 class OracleSample:
     """The oracle (its own encoder for the blobs, then decode + fp64 dot
@@ -202,6 +211,10 @@ def run_reference(args):
         return
     from lossless_bit_weight_encode_gb300 import workloads as wl
 
+    if args.workload == "model64":
+        # its weights come from the GPU's generator; the host-only arm times
+        # the oracle on the layer workload's matrices of the same shapes
+        args.workload = "layer"
     weights = list(wl.layer_weights(args.workload))
     xs = [wl.activations(args.m, w.shape[1], seed=wl.activation_seed(args.workload, args.m)) for _, w in weights]
     orc = OracleSample(weights, xs, args.m)
@@ -261,15 +274,51 @@ def run_w12(args):
 
     libbuild.build()
     M = args.m
-    weights = list(wl.layer_weights(args.workload))
-    if args.matrices:
-        keep = set(args.matrices.split(","))
-        weights = [(n, w) for n, w in weights if n in keep]
-    mats = [W12Weight(w) for _, w in weights]
-    xs_host = [wl.activations(M, w.shape[1], seed=wl.activation_seed(args.workload, M)) for _, w in weights]
-    xs = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs_host]
+    nshape = len(wl.LAYER_SHAPES)
+    if args.workload == "model64":
+        # 64 layers drawn and encoded on the GPU (W12Weight.from_device); one
+        # activation per shape, shared by every layer; one workspace per shape
+        # (the launches are ordered on one stream)
+        names = [f"L{layer}.{n}" for layer in range(wl.MODEL64_LAYERS) for n, _, _ in wl.LAYER_SHAPES]
+        mats = []
+        for layer in range(wl.MODEL64_LAYERS):
+            for idx in range(nshape):
+                w = wl.model64_weight_dev(layer, idx)
+                mats.append(W12Weight.from_device(w))
+                del w
+        xs_shape = [wl.model64_activation(M, i) for i in range(nshape)]
+        xs_host = [xs_shape[i % nshape] for i in range(len(mats))]
+        xs_dev = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs_shape]
+        xs = [xs_dev[i % nshape] for i in range(len(mats))]
+        ws_shape = [mats[i].workspace(M) for i in range(nshape)]
+        wss = [ws_shape[i % nshape] for i in range(len(mats))]
+
+        def dense_weights():
+            for layer in range(wl.MODEL64_LAYERS):
+                for idx in range(nshape):
+                    yield wl.model64_weight_dev(layer, idx)
+
+        def cpu_weights():
+            return [(n, wl.model64_weight_dev(0, i).view(torch.int16).cpu().numpy().view(np.uint16))
+                    for i, (n, _, _) in enumerate(wl.LAYER_SHAPES)]
+    else:
+        weights = list(wl.layer_weights(args.workload))
+        if args.matrices:
+            keep = set(args.matrices.split(","))
+            weights = [(n, w) for n, w in weights if n in keep]
+        names = [n for n, _ in weights]
+        mats = [W12Weight(w) for _, w in weights]
+        xs_host = [wl.activations(M, w.shape[1], seed=wl.activation_seed(args.workload, M)) for _, w in weights]
+        xs = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs_host]
+        wss = [m.workspace(M) for m in mats]
+
+        def dense_weights():
+            for _, w in weights:
+                yield torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16)
+
+        def cpu_weights():
+            return weights
     ys = [torch.empty((M, m.N), dtype=torch.bfloat16, device="cuda") for m in mats]
-    wss = [m.workspace(M) for m in mats]
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     calls = [(x.data_ptr(), m.blob.data_ptr(), m.info, y.data_ptr(), M, ws.data_ptr(), ws.numel(), sh)
@@ -322,7 +371,7 @@ def run_w12(args):
 
     # per-launch durations of the GEMM kernel (events around every launch)
     nl = len(calls)
-    kp = max(10, min(K, 500))
+    kp = max(10, min(K, 500 if nl <= 7 else 20))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(kp)]
     barrier()
     for k in range(kp):
@@ -352,8 +401,8 @@ def run_w12(args):
     # BF16 comparator (cuBLAS through torch.matmul), same shapes and x
     bf16 = None
     if not args.no_bf16:
-        wts = [torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16) for _, w in weights]
-        outs = [torch.empty((M, w.shape[0]), dtype=torch.bfloat16, device="cuda") for _, w in weights]
+        wts = list(dense_weights())
+        outs = [torch.empty((M, w.shape[0]), dtype=torch.bfloat16, device="cuda") for w in wts]
 
         def bstep():
             for x, wt, o in zip(xs, wts, outs):
@@ -376,10 +425,11 @@ def run_w12(args):
     e2e = None
     if not args.no_e2e:
         xh = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs_host]
+        xs_e2e = [torch.empty_like(x) for x in xs]  # one device x per launch: every step copies all of them
         yh = [torch.empty((M, m.N), dtype=torch.bfloat16).pin_memory() for m in mats]
 
         def estep():
-            for xhi, x, m, y, yhi, ws in zip(xh, xs, mats, ys, yh, wss):
+            for xhi, x, m, y, yhi, ws in zip(xh, xs_e2e, mats, ys, yh, wss):
                 x.copy_(xhi, non_blocking=True)
                 w12.w12_gemm(x, m.blob, m.info, y, M, ws, stream)
                 yhi.copy_(y, non_blocking=True)
@@ -407,7 +457,7 @@ def run_w12(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        orc = OracleSample(weights, xs_host, M)
+        orc = OracleSample(cpu_weights(), xs_host[:nshape] if args.workload == "model64" else xs_host, M)
         v, sample, _, _ = orc.run(3.0)
         cpu = {"value": round(v, 4), "unit": "GB/s", "cores": orc.cores, "kind": "oracle", "sample": sample}
 
@@ -421,13 +471,10 @@ def run_w12(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {
-            "workload": f"{args.workload}: 27B-class decoder layer (q 6144x5120, k/v 1024x5120, o 5120x6144, "
-                        f"gate/up 17408x5120, down 5120x17408; 340.8 M weights), weights N(0,0.02)"
-                        if args.workload == "layer" else
-                        f"{args.workload}: layer shapes, Student-t(3)*0.02 weights with 0.5% x100 outliers",
+            "workload": WORKLOAD_TEXT[args.workload],
             "M": M, "global_batch": M * world, "parallelism": f"replicas x{world}",
             "l2": f"inputs larger than L2: {packed / 1e6:.1f} MB of W12 streamed per step (L2 129 MB)",
-            "launch": "cuda graph" if graph is not None else "stream (7 launches per step)",
+            "launch": "cuda graph" if graph is not None else f"stream ({nl} launches per step)",
         },
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": traffic,
@@ -438,13 +485,18 @@ def run_w12(args):
         "e2e": e2e,
         "gpu_launches": K * nl,
         "detail": {
-            "us_per_layer": round(ms_step * 1e3, 2),
+            "us_per_layer": round(ms_step * 1e3 / (wl.MODEL64_LAYERS if args.workload == "model64" else 1), 2),
+            "layers_per_step": wl.MODEL64_LAYERS if args.workload == "model64" else 1,
             "packed_GBps": round(packed / (ms_step * 1e-3) / 1e9, 1),
             "packed_frac_of_hbm_peak": round(packed / (ms_step * 1e-3) / 1e9 / peak, 4),
             "bits_per_weight": round(8.0 * packed / layer_weights, 5),
             "n_escapes": int(sum(int(m.info.n_escapes) for m in mats)),
-            "per_matrix_us": {n: round(v * 1e3, 2) for (n, _), v in zip(weights, launch_ms)},
-            "bf16_cublas_us_per_layer": round(bf16 * 1e3, 2) if bf16 else None,
+            "per_matrix_us": {n: round(statistics.mean(launch_ms[i::nshape]) * 1e3, 2)
+                              for i, (n, _, _) in enumerate(wl.LAYER_SHAPES)}
+                             if args.workload == "model64" else
+                             {n: round(v * 1e3, 2) for n, v in zip(names, launch_ms)},
+            "bf16_cublas_us_per_layer": round(bf16 * 1e3 / (wl.MODEL64_LAYERS if args.workload == "model64"
+                                                            else 1), 2) if bf16 else None,
             "speedup_vs_bf16": round(bf16 / ms_step, 4) if bf16 else None,
         },
     }

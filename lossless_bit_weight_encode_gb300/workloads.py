@@ -14,10 +14,15 @@ synthetic):
             down 5120x17408; weights ~N(0, 0.02), activations ~N(0, 1)
   heavy     the layer shapes with Student-t(3) * 0.02 weights and 0.5 % of
             entries (Bernoulli) multiplied by 100 before rounding
-  model64   64 layers of the layer shapes, weights ~N(0, 0.02)
+  model64   64 layers of the layer shapes, weights ~N(0, 0.02) drawn on the
+            GPU (21.8 G weights: 43.6 GB BF16, 32.7 GB W12), one activation
+            per shape shared by all layers
 
 Seeds: weights use numpy PCG64 seeded with 100 * workload_id + matrix_index
 (q0 k1 v2 o3 gate4 up5 down6); activations use 10000 + 100 * workload_id + M.
+model64 weights use torch's CUDA generator seeded with
+50000 + 7 * layer + matrix_index, its activations PCG64 seeded with
+(10000 + 100 * 5 + M, matrix_index).
 """
 from __future__ import annotations
 
@@ -138,6 +143,24 @@ def layer_weights(workload: str = "layer"):
     gen = heavy_tail_weights if workload == "heavy" else gaussian_weights
     for idx, (name, n, k) in enumerate(LAYER_SHAPES):
         yield name, gen(n, k, weight_seed(workload, idx))
+
+
+def model64_weight_dev(layer: int, index: int) -> torch.Tensor:
+    """Weight `index` (q0 .. down6) of layer `layer` of the 64-layer stream,
+    drawn on the current CUDA device as BF16 [N, K]."""
+    _, n, k = LAYER_SHAPES[index]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(50000 + 7 * layer + index)
+    w = torch.randn((n, k), generator=g, device="cuda", dtype=torch.float32)
+    return (w * WEIGHT_STD).to(torch.bfloat16)
+
+
+def model64_activation(m: int, index: int) -> np.ndarray:
+    """The x [m, K] fed to matrix `index` of every layer of the 64-layer
+    stream (N(0, 1), PCG64 seeded with (activation_seed, index))."""
+    k = LAYER_SHAPES[index][2]
+    rng = np.random.Generator(np.random.PCG64([activation_seed("model64", m), index]))
+    return to_bf16_bits(rng.standard_normal((m, k), dtype=np.float32))
 
 
 def single_case():
