@@ -444,6 +444,66 @@ __device__ void gemm_decode(const GemmParams &p, uint8_t *smem, const Bars &b, v
 }
 
 // ------------------------------------------------------------------ epilogue
+// The last CTA of a tile sums the tile's split partials in ascending split
+// order (fixed, so results repeat run to run) and stores y.  The M x 128
+// outputs are spread over the CTA's decode threads; a thread keeps several
+// loads in flight: eight splits of one output when it has one or two outputs,
+// else one split of kBatch outputs.
+template <int kThreads, int kBatch>
+__device__ __forceinline__ void reduce_splits(const GemmParams &p, int64_t tile, int t) {
+    static_assert(kThreads % kTileRows == 0, "outputs of one thread share a row");
+    const int total = p.M * kTileRows;
+    const int64_t sstride = (int64_t)p.M * p.Npad;
+    const float *base = p.partials + tile * kTileRows;
+    if (total <= 2 * kThreads) {
+        for (int o = t; o < total; o += kThreads) {
+            const int m = o / kTileRows, rr = o % kTileRows;
+            if (tile * kTileRows + rr >= p.N) continue;
+            const float *src = base + (int64_t)m * p.Npad + rr;
+            float s = 0.0f;
+            int sp = 0;
+            for (; sp + 8 <= p.splits; sp += 8) {
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (sp + u) * sstride);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) s += v[u];
+            }
+            for (; sp < p.splits; ++sp) s += __ldcg(src + sp * sstride);
+            p.y[(int64_t)m * p.N + tile * kTileRows + rr] = bf16_bits_rn(s);
+        }
+        return;
+    }
+    for (int o0 = t; o0 < total; o0 += kBatch * kThreads) {
+        float s[kBatch];
+        uint32_t ok = 0;  // bit b: output o0 + b * kThreads exists
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int o = o0 + b * kThreads;
+            if (o < total && tile * kTileRows + o % kTileRows < p.N) ok |= 1u << b;
+            s[b] = 0.0f;
+        }
+        // outputs b and b + 1 are kThreads / 128 tokens apart, same row
+        const float *src = base + (int64_t)(o0 / kTileRows) * p.Npad + o0 % kTileRows;
+        constexpr int kTokStep = kThreads / kTileRows;
+        for (int sp = 0; sp < p.splits; ++sp) {
+            float v[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b)
+                v[b] = (ok >> b) & 1u ? __ldcg(src + sp * sstride + (int64_t)(b * kTokStep) * p.Npad) : 0.0f;
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) s[b] += v[b];
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if ((ok >> b) & 1u) {
+                const int o = o0 + b * kThreads;
+                p.y[(int64_t)(o / kTileRows) * p.N + tile * kTileRows + o % kTileRows] = bf16_bits_rn(s[b]);
+            }
+        }
+    }
+}
+
 // D (fp32, TMEM lane = weight row, column = token) -> y, or -> partials and
 // the last CTA of the tile sums the partials in split order.
 template <class C>
@@ -512,17 +572,7 @@ __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint3
     }
     if (*last_flag == 0) return;
     __threadfence();
-    if (n < p.N) {
-#pragma unroll
-        for (int m = m0; m < m0 + kHalf; ++m) {
-            if (m < p.M) {
-                float s = 0.0f;
-                for (int sp = 0; sp < p.splits; ++sp)
-                    s += __ldcg(p.partials + ((int64_t)sp * p.M + m) * p.Npad + n);
-                p.y[(int64_t)m * p.N + n] = bf16_bits_rn(s);
-            }
-        }
-    }
+    reduce_splits<C::kDecWarps * 32, 8>(p, tile, (int)threadIdx.x);
     if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next call
 }
 

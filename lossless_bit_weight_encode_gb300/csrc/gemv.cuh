@@ -295,8 +295,18 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
     if (*last_flag == 0) return;
     __threadfence();
     if (n < p.N) {
+        // ascending split order; eight loads in flight at a time
+        const float *src = p.partials + n;
         float s = 0.0f;
-        for (int sp = 0; sp < p.splits; ++sp) s += __ldcg(p.partials + (int64_t)sp * p.Npad + n);
+        int sp = 0;
+        for (; sp + 8 <= p.splits; sp += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (int64_t)(sp + u) * p.Npad);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s += v[u];
+        }
+        for (; sp < p.splits; ++sp) s += __ldcg(src + (int64_t)sp * p.Npad);
         p.y[n] = bf16_bits_rn(s);
     }
     if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next call
