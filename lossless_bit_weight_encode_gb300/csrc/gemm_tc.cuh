@@ -551,16 +551,19 @@ __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint3
 #pragma unroll
     for (int m = 0; m < kHalf; ++m)
         if (m0 + m < p.M) __stcg(part + (int64_t)(m0 + m) * p.Npad, acc[m]);
-    __threadfence();
     // the decode warps meet on mbarriers (bounded waits, no bar.sync that
-    // a warp which gave up could leave the others stuck in)
+    // a warp which gave up could leave the others stuck in); the mbarrier
+    // arrive/wait pair orders this CTA's partial stores before thread 0's
+    // fence, which publishes them all with the counter increment
     __syncwarp();
     if (lane == 0) mbar_arrive(b.epi_in);
     if (threadIdx.x == 0) {
         if (mbar_wait(b.epi_in, 0, deadline)) {
             __threadfence();
             const uint32_t old = atomicAdd(p.counters + tile, 1u);
-            *last_flag = (old == (uint32_t)(p.splits - 1)) ? 1u : 0u;
+            const bool last = old == (uint32_t)(p.splits - 1);
+            if (last) __threadfence();  // the other CTAs' partials are visible past here
+            *last_flag = last ? 1u : 0u;
             mbar_arrive(b.epi_out);
         } else {
             raise_timeout(p.status, abort_flag);
@@ -571,7 +574,6 @@ __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint3
         return;
     }
     if (*last_flag == 0) return;
-    __threadfence();
     reduce_splits<C::kDecWarps * 32, 8>(p, tile, (int)threadIdx.x);
     if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next call
 }

@@ -275,14 +275,17 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
         return;
     }
     __stcg(p.partials + (int64_t)split * p.Npad + n, total);
-    __threadfence();
+    // the mbarrier arrive/wait pair orders these stores before thread 0's
+    // fence, which publishes them all with the counter increment
     __syncwarp();
     if (lane == 0) mbar_arrive(b.epi_in);
     if (threadIdx.x == 0) {
         if (mbar_wait(b.epi_in, 0, deadline)) {
             __threadfence();
             const uint32_t old = atomicAdd(p.counters + tile, 1u);
-            *last_flag = (old == (uint32_t)(p.splits - 1)) ? 1u : 0u;
+            const bool last = old == (uint32_t)(p.splits - 1);
+            if (last) __threadfence();  // the other CTAs' partials are visible past here
+            *last_flag = last ? 1u : 0u;
             mbar_arrive(b.epi_out);
         } else {
             raise_timeout(p.status, abort_flag);
@@ -293,7 +296,6 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
         return;
     }
     if (*last_flag == 0) return;
-    __threadfence();
     if (n < p.N) {
         // ascending split order; eight loads in flight at a time
         const float *src = p.partials + n;
