@@ -448,8 +448,8 @@ __device__ void gemm_decode(const GemmParams &p, uint8_t *smem, const Bars &b, v
 // order (fixed, so results repeat run to run) and stores y.  The M x 128
 // outputs are spread over the CTA's decode threads; a thread keeps several
 // loads in flight: eight splits of one output when it has one or two outputs,
-// else one split of kBatch outputs.
-template <int kThreads, int kBatch>
+// else kUnroll splits of kBatch outputs.
+template <int kThreads, int kBatch, int kUnroll>
 __device__ __forceinline__ void reduce_splits(const GemmParams &p, int64_t tile, int t) {
     static_assert(kThreads % kTileRows == 0, "outputs of one thread share a row");
     const int total = p.M * kTileRows;
@@ -486,13 +486,25 @@ __device__ __forceinline__ void reduce_splits(const GemmParams &p, int64_t tile,
         // outputs b and b + 1 are kThreads / 128 tokens apart, same row
         const float *src = base + (int64_t)(o0 / kTileRows) * p.Npad + o0 % kTileRows;
         constexpr int kTokStep = kThreads / kTileRows;
-        for (int sp = 0; sp < p.splits; ++sp) {
-            float v[kBatch];
+        int sp = 0;
+        for (; sp + kUnroll <= p.splits; sp += kUnroll) {
+            float v[kUnroll][kBatch];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b)
+                    v[u][b] = (ok >> b) & 1u
+                                  ? __ldcg(src + (sp + u) * sstride + (int64_t)(b * kTokStep) * p.Npad)
+                                  : 0.0f;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) s[b] += v[u][b];
+        }
+        for (; sp < p.splits; ++sp) {
 #pragma unroll
             for (int b = 0; b < kBatch; ++b)
-                v[b] = (ok >> b) & 1u ? __ldcg(src + sp * sstride + (int64_t)(b * kTokStep) * p.Npad) : 0.0f;
-#pragma unroll
-            for (int b = 0; b < kBatch; ++b) s[b] += v[b];
+                s[b] += (ok >> b) & 1u ? __ldcg(src + sp * sstride + (int64_t)(b * kTokStep) * p.Npad) : 0.0f;
         }
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
@@ -574,7 +586,7 @@ __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint3
         return;
     }
     if (*last_flag == 0) return;
-    reduce_splits<C::kDecWarps * 32, 8>(p, tile, (int)threadIdx.x);
+    reduce_splits<C::kDecWarps * 32, 8, C::kNtok == 16 ? 3 : 4>(p, tile, (int)threadIdx.x);
     if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next call
 }
 
