@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
     ap.add_argument("--m", type=int, default=1, help="tokens per GEMM (1..32)")
-    ap.add_argument("--workload", default="layer", choices=["layer", "heavy", "model64"])
+    ap.add_argument("--workload", default="layer", choices=["layer", "heavy", "model64", "lmhead"])
     ap.add_argument("--graph", action="store_true", help="replay the step as a CUDA graph")
     ap.add_argument("--no-bf16", action="store_true", help="skip the cuBLAS BF16 comparator")
     ap.add_argument("--no-e2e", action="store_true")
@@ -161,6 +161,8 @@ WORKLOAD_TEXT = {
     "layer": "layer: 27B-class decoder layer (q 6144x5120, k/v 1024x5120, o 5120x6144, gate/up 17408x5120, "
              "down 5120x17408; 340.8 M weights), weights N(0,0.02)",
     "heavy": "heavy: layer shapes, Student-t(3)*0.02 weights with 0.5% x100 outliers",
+    "lmhead": "lmhead: LM head 151936x5120 (vocabulary x hidden), weights N(0,0.02), GEMM with the fused "
+              "exact-argmax epilogue (per-token index and fp32 logit; logits not stored)",
     "model64": "model64: 64 layers of the 27B-class shapes chained in layer order (448 GEMMs, 21.8 G weights, "
                "32.7 GB of W12 resident), weights N(0,0.02) drawn and encoded on the GPU",
 }
@@ -215,7 +217,11 @@ def run_reference(args):
         # its weights come from the GPU's generator; the host-only arm times
         # the oracle on the layer workload's matrices of the same shapes
         args.workload = "layer"
-    weights = list(wl.layer_weights(args.workload))
+    if args.workload == "lmhead":
+        name, n, k = wl.LMHEAD_SHAPE
+        weights = [(name, wl.gaussian_weights(n, k, seed=wl.weight_seed("lmhead", 0)))]
+    else:
+        weights = list(wl.layer_weights(args.workload))
     xs = [wl.activations(args.m, w.shape[1], seed=wl.activation_seed(args.workload, args.m)) for _, w in weights]
     orc = OracleSample(weights, xs, args.m)
     # one step = one layer matrix (cycling q, k, v, o, gate, up, down): a
@@ -302,7 +308,11 @@ def run_w12(args):
             return [(n, wl.model64_weight_dev(0, i).view(torch.int16).cpu().numpy().view(np.uint16))
                     for i, (n, _, _) in enumerate(wl.LAYER_SHAPES)]
     else:
-        weights = list(wl.layer_weights(args.workload))
+        if args.workload == "lmhead":
+            name, n, k = wl.LMHEAD_SHAPE
+            weights = [(name, wl.gaussian_weights(n, k, seed=wl.weight_seed("lmhead", 0)))]
+        else:
+            weights = list(wl.layer_weights(args.workload))
         if args.matrices:
             keep = set(args.matrices.split(","))
             weights = [(n, w) for n, w in weights if n in keep]
@@ -321,12 +331,23 @@ def run_w12(args):
     ys = [torch.empty((M, m.N), dtype=torch.bfloat16, device="cuda") for m in mats]
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
-    calls = [(x.data_ptr(), m.blob.data_ptr(), m.info, y.data_ptr(), M, ws.data_ptr(), ws.numel(), sh)
-             for x, m, y, ws in zip(xs, mats, ys, wss)]
+    argmax = args.workload == "lmhead"
+    if argmax:
+        # the LM head: GEMM with the fused argmax epilogue (no logits stored)
+        idx = torch.empty(M, dtype=torch.int32, device="cuda")
+        val = torch.empty(M, dtype=torch.float32, device="cuda")
+        aws = [m.argmax_workspace(M) for m in mats]
+        calls = [(x.data_ptr(), m.blob.data_ptr(), m.info, M, None, idx.data_ptr(), val.data_ptr(), ws.data_ptr(),
+                  ws.numel(), sh) for x, m, ws in zip(xs, mats, aws)]
+        launch = w12.w12_gemm_argmax_ptr
+    else:
+        calls = [(x.data_ptr(), m.blob.data_ptr(), m.info, y.data_ptr(), M, ws.data_ptr(), ws.numel(), sh)
+                 for x, m, y, ws in zip(xs, mats, ys, wss)]
+        launch = w12.w12_gemm_ptr
 
     def step():
         for c in calls:
-            rc = w12.w12_gemm_ptr(*c)
+            rc = launch(*c)
             if rc != 0:
                 raise w12.W12Error(rc, w12.w12_last_error())
 
@@ -377,7 +398,7 @@ def run_w12(args):
     for k in range(kp):
         for i, c in enumerate(calls):
             evs[k][i].record()
-            rc = w12.w12_gemm_ptr(*c)
+            rc = launch(*c)
             if rc != 0:
                 raise w12.W12Error(rc, w12.w12_last_error())
         evs[k][nl].record()
@@ -407,6 +428,8 @@ def run_w12(args):
         def bstep():
             for x, wt, o in zip(xs, wts, outs):
                 torch.matmul(x, wt.t(), out=o)
+                if argmax:
+                    torch.argmax(o, dim=1)
 
         for _ in range(args.warmup):
             bstep()
@@ -427,12 +450,18 @@ def run_w12(args):
         xh = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs_host]
         xs_e2e = [torch.empty_like(x) for x in xs]  # one device x per launch: every step copies all of them
         yh = [torch.empty((M, m.N), dtype=torch.bfloat16).pin_memory() for m in mats]
+        if argmax:
+            idx_h = torch.empty(M, dtype=torch.int32).pin_memory()
 
         def estep():
             for xhi, x, m, y, yhi, ws in zip(xh, xs_e2e, mats, ys, yh, wss):
                 x.copy_(xhi, non_blocking=True)
-                w12.w12_gemm(x, m.blob, m.info, y, M, ws, stream)
-                yhi.copy_(y, non_blocking=True)
+                if argmax:
+                    w12.w12_gemm_argmax(x, m.blob, m.info, M, None, idx, val, m.argmax_workspace(M), stream)
+                    idx_h.copy_(idx, non_blocking=True)
+                else:
+                    w12.w12_gemm(x, m.blob, m.info, y, M, ws, stream)
+                    yhi.copy_(y, non_blocking=True)
 
         for _ in range(args.warmup):
             estep()
@@ -452,7 +481,7 @@ def run_w12(args):
             e_ms = float(t.item())
         e2e = {"value": round(world * 2.0 * layer_weights / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(sum(2 * M * m.K for m in mats)),
-               "d2h_bytes_per_step": int(sum(2 * M * m.N for m in mats)),
+               "d2h_bytes_per_step": int(4 * M) if argmax else int(sum(2 * M * m.N for m in mats)),
                "ms_per_step": round(e_ms, 5)}
 
     cpu = None
@@ -483,7 +512,7 @@ def run_w12(args):
         "cpu_baseline": cpu,
         "clocks": csum,
         "e2e": e2e,
-        "gpu_launches": K * nl,
+        "gpu_launches": K * nl * (2 if argmax else 1),
         "detail": {
             "us_per_layer": round(ms_step * 1e3 / (wl.MODEL64_LAYERS if args.workload == "model64" else 1), 2),
             "layers_per_step": wl.MODEL64_LAYERS if args.workload == "model64" else 1,

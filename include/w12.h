@@ -159,6 +159,30 @@ int w12_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info *info,
              uint16_t *y_dev, int M, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * LM-head product with a fused exact argmax ("SpecPilot: an agent doubled
+ * speculative decoding speed, and the 10.87x needs context" (ai.jakubjirak.com),
+ * §The mechanisms it found, lists a certified exact-argmax LM head; the page
+ * does not say how it is certified).  Reading taken: for each token m,
+ * idx_dev[m] = the row n that maximizes logit[m][n] = sum_k x[m][k] * W[n][k]
+ * as w12_gemm accumulates it (fp32, the same order), compared in fp32 before
+ * any rounding to BF16, ties to the smallest n; val_dev[m] = that fp32 logit.
+ * -0 compares equal to +0 and a NaN logit ranks as -infinity (val is then
+ * -inf).  y_dev may be NULL; otherwise it receives the BF16 logits exactly as
+ * w12_gemm would.  x_dev, blob_dev, info and M as w12_gemm; idx_dev int32[M],
+ * val_dev float[M], 4-byte aligned; N must fit in int32 (SHAPE).  workspace:
+ * w12_gemm_argmax_workspace_size bytes, 256-byte aligned, zero-filled before
+ * its first use (the call clears its own argmax keys).  Asynchronous on
+ * stream: a memset, the GEMM kernel with the argmax epilogue (each CTA folds
+ * its rows' best candidate into one 64-bit key per token with an atomic max)
+ * and a one-warp finalize kernel.
+ */
+int w12_gemm_argmax_workspace_size(const w12_info *info, int M, size_t *bytes);
+
+int w12_gemm_argmax(const uint16_t *x_dev, const void *blob_dev, const w12_info *info, int M,
+                    uint16_t *y_dev, int32_t *idx_dev, float *val_dev, void *workspace,
+                    size_t ws_bytes, void *stream);
+
+/*
  * Size of the fixed scratch array behind w12_gemm_noalloc (16 MiB).
  */
 #define W12_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)

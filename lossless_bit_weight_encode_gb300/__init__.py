@@ -78,6 +78,32 @@ class W12Weight:
         w12.w12_gemm(x, self.blob, self.info, out, M, self.workspace(M), stream)
         return out
 
+    def argmax_workspace(self, M: int):
+        import torch
+
+        size = w12.w12_gemm_argmax_workspace_size(self.info, M)
+        key = ("argmax", M)
+        ws = self._ws.get(key)
+        if ws is None or ws.numel() < size:
+            ws = torch.zeros(max(size, 256), dtype=torch.uint8, device=self.blob.device)
+            self._ws[key] = ws
+        return ws
+
+    def gemm_argmax(self, x, logits: bool = False, stream=None):
+        """Per token: (row index int32 [M], fp32 logit [M]) of the largest
+        entry of x . W^T (ties to the lowest row), plus the BF16 logits
+        [M, N] when `logits` is set (else None)."""
+        import torch
+
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != self.K or not x.is_contiguous():
+            raise ValueError("x must be a contiguous BF16 tensor of shape [M, K]")
+        M = int(x.shape[0])
+        idx = torch.empty(M, dtype=torch.int32, device=x.device)
+        val = torch.empty(M, dtype=torch.float32, device=x.device)
+        y = torch.empty((M, self.N), dtype=torch.bfloat16, device=x.device) if logits else None
+        w12.w12_gemm_argmax(x, self.blob, self.info, M, y, idx, val, self.argmax_workspace(M), stream)
+        return idx, val, y
+
     def decode(self, out=None, stream=None):
         import torch
 

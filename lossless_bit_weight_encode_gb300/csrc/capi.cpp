@@ -169,6 +169,45 @@ int w12_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info *info, 
     });
 }
 
+int w12_gemm_argmax_workspace_size(const w12_info *info, int M, size_t *bytes) {
+    return guarded([&](std::string &err) {
+        int rc = check_info(info, err);
+        if (rc != W12_OK) return rc;
+        if (!bytes || M < 1 || M > 32) {
+            err = "null pointer or M outside 1..32";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        return w12::launch::argmax_workspace_size(*info, M, bytes, &err);
+    });
+}
+
+int w12_gemm_argmax(const uint16_t *x_dev, const void *blob_dev, const w12_info *info, int M, uint16_t *y_dev,
+                    int32_t *idx_dev, float *val_dev, void *workspace, size_t ws_bytes, void *stream) {
+    return guarded([&](std::string &err) {
+        int rc = check_info(info, err);
+        if (rc != W12_OK) return rc;
+        if (!x_dev || !blob_dev || !idx_dev || !val_dev || !workspace) {
+            err = "null device pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (M < 1 || M > 32) {
+            err = "M must be in 1..32";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (info->N > 0x7FFFFFFF) {
+            err = "N must fit in int32 for the argmax index";
+            return (int)W12_ERR_SHAPE;
+        }
+        if (!aligned(blob_dev, 256) || !aligned(workspace, 256) || !aligned(x_dev, 2) || !aligned(y_dev, 2) ||
+            !aligned(idx_dev, 4) || !aligned(val_dev, 4)) {
+            err = "blob_dev and workspace must be 256-byte aligned, x_dev and y_dev 2-byte, idx and val 4-byte";
+            return (int)W12_ERR_ALIGNMENT;
+        }
+        return w12::launch::gemm_argmax(x_dev, blob_dev, *info, M, y_dev, idx_dev, val_dev, workspace, ws_bytes,
+                                        stream, &err);
+    });
+}
+
 int w12_gemm_noalloc(const uint16_t *x_dev, const void *blob_dev, const w12_info *info, uint16_t *y_dev, int M,
                      void *stream) {
     return guarded([&](std::string &err) {

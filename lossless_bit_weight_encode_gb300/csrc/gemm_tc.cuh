@@ -57,7 +57,8 @@ struct GemmParams {
     int32_t M, splits;
     float *partials;          // [splits][M][Npad] fp32 (splits > 1)
     uint32_t *counters;       // [tiles] arrival counters (splits > 1)
-    uint16_t *y;              // [M][N] BF16
+    uint16_t *y;              // [M][N] BF16 (may be null when amax is set)
+    unsigned long long *amax; // [M] argmax keys (null: plain GEMM)
     uint32_t *status;         // device status word
     uint64_t timeout_ns;
 };
@@ -456,10 +457,11 @@ __device__ __forceinline__ void reduce_splits(const GemmParams &p, int64_t tile,
     const int64_t sstride = (int64_t)p.M * p.Npad;
     const float *base = p.partials + tile * kTileRows;
     if (total <= 2 * kThreads) {
+        // total is a multiple of 128, so a warp's lanes leave this loop together
         for (int o = t; o < total; o += kThreads) {
             const int m = o / kTileRows, rr = o % kTileRows;
-            if (tile * kTileRows + rr >= p.N) continue;
-            const float *src = base + (int64_t)m * p.Npad + rr;
+            const bool valid = tile * kTileRows + rr < p.N;
+            const float *src = base + (int64_t)m * p.Npad + (valid ? rr : 0);
             float s = 0.0f;
             int sp = 0;
             for (; sp + 8 <= p.splits; sp += 8) {
@@ -470,7 +472,9 @@ __device__ __forceinline__ void reduce_splits(const GemmParams &p, int64_t tile,
                 for (int u = 0; u < 8; ++u) s += v[u];
             }
             for (; sp < p.splits; ++sp) s += __ldcg(src + sp * sstride);
-            p.y[(int64_t)m * p.N + tile * kTileRows + rr] = bf16_bits_rn(s);
+            if (p.y != nullptr && valid) p.y[(int64_t)m * p.N + tile * kTileRows + rr] = bf16_bits_rn(s);
+            if (p.amax != nullptr)
+                argmax_warp(p.amax + m, valid ? argmax_key(s, (uint32_t)(tile * kTileRows + rr)) : 0ull);
         }
         return;
     }
@@ -508,10 +512,13 @@ __device__ __forceinline__ void reduce_splits(const GemmParams &p, int64_t tile,
         }
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
-            if ((ok >> b) & 1u) {
-                const int o = o0 + b * kThreads;
+            const int o = o0 + b * kThreads;
+            if (p.y != nullptr && ((ok >> b) & 1u))
                 p.y[(int64_t)(o / kTileRows) * p.N + tile * kTileRows + o % kTileRows] = bf16_bits_rn(s[b]);
-            }
+            // o < total is the same for the 32 lanes of a warp
+            if (p.amax != nullptr && o < total)
+                argmax_warp(p.amax + o / kTileRows,
+                            ((ok >> b) & 1u) ? argmax_key(s[b], (uint32_t)(tile * kTileRows + o % kTileRows)) : 0ull);
         }
     }
 }
@@ -552,10 +559,15 @@ __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint3
     }
     const int64_t n = tile * kTileRows + 32 * q + lane;
     if (p.splits == 1) {
-        if (n < p.N) {
+        if (p.y != nullptr && n < p.N) {
 #pragma unroll
             for (int m = 0; m < kHalf; ++m)
                 if (m0 + m < p.M) p.y[(int64_t)(m0 + m) * p.N + n] = bf16_bits_rn(acc[m]);
+        }
+        if (p.amax != nullptr) {
+#pragma unroll
+            for (int m = 0; m < kHalf; ++m)
+                if (m0 + m < p.M) argmax_warp(p.amax + m0 + m, n < p.N ? argmax_key(acc[m], (uint32_t)n) : 0ull);
         }
         return;
     }

@@ -271,7 +271,8 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
     const float total = mine + red[r];
     const int64_t n = tile * kTileRows + r;
     if (p.splits == 1) {
-        if (n < p.N) p.y[n] = bf16_bits_rn(total);
+        if (p.y != nullptr && n < p.N) p.y[n] = bf16_bits_rn(total);
+        if (p.amax != nullptr) argmax_warp(p.amax, n < p.N ? argmax_key(total, (uint32_t)n) : 0ull);
         return;
     }
     __stcg(p.partials + (int64_t)split * p.Npad + n, total);
@@ -296,9 +297,9 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
         return;
     }
     if (*last_flag == 0) return;
-    if (n < p.N) {
+    {
         // ascending split order; eight loads in flight at a time
-        const float *src = p.partials + n;
+        const float *src = p.partials + (n < p.N ? n : tile * kTileRows);
         float s = 0.0f;
         int sp = 0;
         for (; sp + 8 <= p.splits; sp += 8) {
@@ -309,7 +310,8 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
             for (int u = 0; u < 8; ++u) s += v[u];
         }
         for (; sp < p.splits; ++sp) s += __ldcg(src + (int64_t)sp * p.Npad);
-        p.y[n] = bf16_bits_rn(s);
+        if (p.y != nullptr && n < p.N) p.y[n] = bf16_bits_rn(s);
+        if (p.amax != nullptr) argmax_warp(p.amax, n < p.N ? argmax_key(s, (uint32_t)n) : 0ull);
     }
     if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next call
 }

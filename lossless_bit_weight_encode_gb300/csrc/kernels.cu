@@ -33,6 +33,17 @@ __global__ void w12_pad_x_kernel(const uint16_t *__restrict__ x, uint16_t *__res
     }
 }
 
+// Turns the argmax keys of the LM-head GEMM back into (row index, fp32 logit).
+__global__ void w12_argmax_finalize_kernel(const unsigned long long *__restrict__ keys, int M,
+                                           int32_t *__restrict__ idx, float *__restrict__ val) {
+    const int m = (int)threadIdx.x;
+    if (m >= M) return;
+    const unsigned long long k = keys[m];
+    const uint32_t ord = (uint32_t)(k >> 32);
+    idx[m] = (int32_t)(0xFFFFFFFFu - (uint32_t)k);
+    val[m] = __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+}
+
 // Waits on an mbarrier that nothing arrives on, with a short deadline, and
 // records the timeout: exercises the bounded-wait path without a fault.
 __global__ void w12_selftest_timeout_kernel(uint32_t *status, uint64_t timeout_ns) {
@@ -311,8 +322,49 @@ cudaError_t launch_gemm_kernel(const dev::GemmParams &p, const CUtensorMap &tm, 
 }
 }  // namespace
 
+namespace {
+int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev,
+              unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err);
+}  // namespace
+
 int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,
          void *workspace, size_t ws_bytes, void *stream, std::string *err) {
+    return gemm_impl(x_dev, blob_dev, info, y_dev, nullptr, M, workspace, ws_bytes, stream, err);
+}
+
+int argmax_workspace_size(const w12_info &info, int M, size_t *bytes, std::string *err) {
+    GemmPlan plan;
+    const int rc = plan_gemm(info, M, &plan, err);
+    if (rc != W12_OK) return rc;
+    *bytes = up256(plan.ws_bytes) + up256(sizeof(unsigned long long) * (size_t)M);
+    return W12_OK;
+}
+
+int gemm_argmax(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, int M, uint16_t *y_dev,
+                int32_t *idx_dev, float *val_dev, void *workspace, size_t ws_bytes, void *stream, std::string *err) {
+    GemmPlan plan;
+    int rc = plan_gemm(info, M, &plan, err);
+    if (rc != W12_OK) return rc;
+    const size_t keys_off = up256(plan.ws_bytes);
+    if (ws_bytes < keys_off + up256(sizeof(unsigned long long) * (size_t)M)) {
+        *err = "workspace smaller than w12_gemm_argmax_workspace_size";
+        return W12_ERR_BUFFER_TOO_SMALL;
+    }
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto *keys = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + keys_off);
+    cudaError_t e = cudaMemsetAsync(keys, 0, sizeof(unsigned long long) * (size_t)M, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(argmax keys)", err);
+    rc = gemm_impl(x_dev, blob_dev, info, y_dev, keys, M, workspace, keys_off, stream, err);
+    if (rc != W12_OK) return rc;
+    dev::w12_argmax_finalize_kernel<<<1, 32, 0, st>>>(keys, M, idx_dev, val_dev);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "argmax finalize launch", err);
+    return W12_OK;
+}
+
+namespace {
+int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev,
+              unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err) {
     GemmPlan plan;
     int rc = plan_gemm(info, M, &plan, err);
     if (rc != W12_OK) return rc;
@@ -371,6 +423,7 @@ int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint
     p.partials = reinterpret_cast<float *>(ws + plan.ws_partials);
     p.counters = reinterpret_cast<uint32_t *>(ws + plan.ws_counters);
     p.y = y_dev;
+    p.amax = amax;
     p.status = s->status;
     p.timeout_ns = timeout_ns();
 
@@ -389,6 +442,7 @@ int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch", err);
     return W12_OK;
 }
+}  // namespace
 
 int check_status(void *stream, std::string *err) {
     DeviceState *s = nullptr;

@@ -485,5 +485,30 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
         : "memory");
 }
 
+// ---------------------------------------------------------------- argmax
+// LM-head argmax ("certified exact-argmax LM head": "SpecPilot: an agent
+// doubled speculative decoding speed, and the 10.87x needs context", §The
+// mechanisms it found).  A candidate (fp32 logit v of row n) becomes a 64-bit
+// key whose unsigned order is: larger v first, then smaller n; the maximum
+// key over all rows is the argmax with ties to the lowest index.  -0 ranks as
+// +0 and NaN as -inf.  Key 0 is below every real candidate.
+__device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t n) {
+    uint32_t b = __float_as_uint(v);
+    if (v != v) b = 0xFF800000u;
+    if ((b << 1) == 0u) b = 0u;
+    const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - n);
+}
+
+// Whole-warp maximum of the lanes' keys, folded into *dst by one lane.
+__device__ __forceinline__ void argmax_warp(unsigned long long *dst, unsigned long long key) {
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, key, off);
+        key = o > key ? o : key;
+    }
+    if ((threadIdx.x & 31u) == 0u && key != 0ull) atomicMax(dst, key);
+}
+
 }  // namespace dev
 }  // namespace w12

@@ -25,7 +25,7 @@ STATUS_NAMES = {
 EXPORTED = (
     "w12_last_error", "w12_status_string", "w12_format_version", "w12_encoded_size_host", "w12_encode_host",
     "w12_blob_info", "w12_blob_validate", "w12_decode", "w12_gemm_workspace_size", "w12_gemm_launch_info",
-    "w12_gemm", "w12_gemm_noalloc", "w12_encode_workspace_size", "w12_encoded_size_device", "w12_encode_device",
+    "w12_gemm", "w12_gemm_argmax_workspace_size", "w12_gemm_argmax", "w12_gemm_noalloc", "w12_encode_workspace_size", "w12_encoded_size_device", "w12_encode_device",
     "w12_check_status", "w12_selftest_timeout",
 )
 
@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
     L.w12_gemm_workspace_size.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(sz)]
     L.w12_gemm_launch_info.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(ctypes.c_int32)]
     L.w12_gemm.argtypes = [vp, vp, ctypes.POINTER(w12_info), vp, i32, vp, sz, vp]
+    L.w12_gemm_argmax_workspace_size.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(sz)]
+    L.w12_gemm_argmax.argtypes = [vp, vp, ctypes.POINTER(w12_info), i32, vp, vp, vp, vp, sz, vp]
     L.w12_gemm_noalloc.argtypes = [vp, vp, ctypes.POINTER(w12_info), vp, i32, vp]
     L.w12_encode_workspace_size.argtypes = [i64, i64, ctypes.POINTER(sz)]
     L.w12_encoded_size_device.argtypes = [vp, i64, i64, vp, sz, ctypes.POINTER(sz), vp]
@@ -174,6 +176,29 @@ def w12_gemm_ptr(x_ptr: int, blob_ptr: int, info: w12_info, y_ptr: int, M: int, 
     """Raw-pointer form of w12_gemm that returns the status instead of raising
     (for timing loops that check once at the end)."""
     return lib().w12_gemm(x_ptr, blob_ptr, ctypes.byref(info), y_ptr, int(M), ws_ptr, ws_bytes, stream_handle)
+
+
+def w12_gemm_argmax_ptr(x_ptr: int, blob_ptr: int, info: w12_info, M: int, y_ptr: int | None, idx_ptr: int,
+                        val_ptr: int, ws_ptr: int, ws_bytes: int, stream_handle: int | None) -> int:
+    """Raw-pointer form of w12_gemm_argmax that returns the status."""
+    return lib().w12_gemm_argmax(x_ptr, blob_ptr, ctypes.byref(info), int(M), y_ptr, idx_ptr, val_ptr, ws_ptr,
+                                 ws_bytes, stream_handle)
+
+
+def w12_gemm_argmax_workspace_size(info: w12_info, M: int) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().w12_gemm_argmax_workspace_size(ctypes.byref(info), int(M), ctypes.byref(out)))
+    return out.value
+
+
+def w12_gemm_argmax(x_dev, blob_dev, info: w12_info, M: int, y_dev, idx_dev, val_dev, workspace,
+                    stream=None) -> None:
+    """Argmax over rows of x . W^T per token (int32 idx_dev[M], float val_dev[M]);
+    y_dev (BF16 [M, N]) may be None."""
+    _check(lib().w12_gemm_argmax(x_dev.data_ptr(), blob_dev.data_ptr(), ctypes.byref(info), int(M),
+                                 None if y_dev is None else y_dev.data_ptr(), idx_dev.data_ptr(),
+                                 val_dev.data_ptr(), workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), _stream_handle(stream)))
 
 
 def w12_gemm_noalloc(x_dev, blob_dev, info: w12_info, y_dev, M: int, stream=None) -> None:

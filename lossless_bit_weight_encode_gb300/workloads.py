@@ -14,6 +14,7 @@ synthetic):
             down 5120x17408; weights ~N(0, 0.02), activations ~N(0, 1)
   heavy     the layer shapes with Student-t(3) * 0.02 weights and 0.5 % of
             entries (Bernoulli) multiplied by 100 before rounding
+  lmhead    the LM head, 151936 x 5120, weights ~N(0, 0.02)
   model64   64 layers of the layer shapes, weights ~N(0, 0.02) drawn on the
             GPU (21.8 G weights: 43.6 GB BF16, 32.7 GB W12), one activation
             per shape shared by all layers
@@ -42,7 +43,11 @@ LAYER_SHAPES = (
     ("down", 5120, 17408),
 )
 
-WORKLOAD_IDS = {"single": 1, "layer": 2, "layer_sweep": 3, "heavy": 4, "model64": 5}
+# LM head of the same model: hidden 5120 and a ~152K-token vocabulary (the
+# pages give no vocabulary size; this one is assumed)
+LMHEAD_SHAPE = ("lm_head", 151936, 5120)
+
+WORKLOAD_IDS = {"single": 1, "layer": 2, "layer_sweep": 3, "heavy": 4, "model64": 5, "lmhead": 6}
 SWEEP_M = (2, 4, 8, 16, 32)
 HEAVY_M = (1, 16)
 MODEL64_M = (16, 32)

@@ -138,6 +138,17 @@ def gemm_f64(x: np.ndarray, w: np.ndarray) -> np.ndarray:
     return y
 
 
+def argmax_f64(x: np.ndarray, w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """LM-head argmax ("SpecPilot: an agent doubled speculative decoding
+    speed, and the 10.87x needs context", §The mechanisms it found): per token
+    m, the row n with the largest logit sum_k x[m,k] * W[n,k] (fp64, from
+    gemm_f64), ties to the smallest n, a NaN logit ranking as -infinity.
+    Returns (indices [M], logits [M, N])."""
+    y = gemm_f64(x, w)
+    ranked = np.where(np.isnan(y), -np.inf, y)
+    return np.argmax(ranked, axis=1).astype(np.int64), y
+
+
 def w12_gemm_f64(x: np.ndarray, blob: np.ndarray, threads: int = 0) -> np.ndarray:
     """fp64 GEMM over the weights a blob holds (decode, then dot products)."""
     x = _as_u16(x)

@@ -260,3 +260,30 @@ def test_malformed_blobs_are_rejected():
     bad[0x11] ^= 1  # N grows by 256: padded geometry no longer matches
     with pytest.raises(ValueError):
         oracle.decode(bad)
+
+
+def test_argmax_f64_ties_nan_and_brute_force():
+    """The LM-head argmax restated: lowest index among equal maxima, NaN
+    logits never chosen, and agreement with an explicit scan on small cases."""
+    one = np.uint16(0x3F80)  # 1.0
+    w = np.zeros((6, 4), dtype=np.uint16)
+    w[1, 0] = w[4, 0] = np.uint16(0x4000)  # 2.0 in rows 1 and 4: a tie
+    w[2, 1] = np.uint16(0x7FC0)            # NaN
+    w[3, 1] = np.uint16(0xBF80)            # -1.0
+    x = np.zeros((2, 4), dtype=np.uint16)
+    x[0, 0] = one
+    x[1, 1] = one
+    idx, y = oracle.argmax_f64(x, w)
+    assert idx[0] == 1                      # tie between rows 1 and 4
+    assert np.isnan(y[1, 2]) and idx[1] == 0  # NaN ranks below 0.0 and -1.0 is below 0.0
+    rng = np.random.default_rng(13)
+    for trial in range(5):
+        w = wl.to_bf16_bits(rng.integers(-3, 4, (50, 30)).astype(np.float32))
+        x = wl.to_bf16_bits(rng.integers(-3, 4, (3, 30)).astype(np.float32))
+        idx, y = oracle.argmax_f64(x, w)
+        for m in range(3):
+            best, arg = -np.inf, -1
+            for n in range(50):
+                if y[m, n] > best:
+                    best, arg = y[m, n], n
+            assert idx[m] == arg
