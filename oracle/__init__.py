@@ -38,7 +38,7 @@ def build(force: bool = False) -> str:
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     subprocess.run(
         ["gcc", "-O2", "-std=c99", "-Wall", "-Wextra", "-fPIC", "-shared", "-fopenmp",
-         _SRC, "-o", tmp],
+         _SRC, "-o", tmp, "-lm"],
         check=True,
     )
     os.replace(tmp, _LIB_PATH)
@@ -54,6 +54,12 @@ def _load():
     u8p = ctypes.POINTER(ctypes.c_uint8)
     f64p = ctypes.POINTER(ctypes.c_double)
     i64 = ctypes.c_int64
+    lib.oracle_q8_size.argtypes = [i64, i64]
+    lib.oracle_q8_size.restype = i64
+    lib.oracle_q8_encode.argtypes = [u16p, i64, i64, u8p, i64]
+    lib.oracle_q8_encode.restype = i64
+    lib.oracle_q8_decode.argtypes = [u8p, i64, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int8)]
+    lib.oracle_q8_decode.restype = ctypes.c_int
     lib.oracle_w12_size.argtypes = [u16p, i64, i64]
     lib.oracle_w12_size.restype = i64
     lib.oracle_w12_encode.argtypes = [u16p, i64, i64, u8p, i64]
@@ -163,6 +169,39 @@ def w12_gemm_f64(x: np.ndarray, blob: np.ndarray, threads: int = 0) -> np.ndarra
     if rc != 0:
         raise ValueError("malformed W12 blob")
     return y
+
+
+def q8_encode(w: np.ndarray) -> np.ndarray:
+    """Q8 v1 blob (INT8 per-row copy) of the N x K BF16 bit patterns."""
+    w = _as_u16(w)
+    n, k = w.shape
+    size = int(_load().oracle_q8_size(n, k))
+    blob = np.empty(size, dtype=np.uint8)
+    if _load().oracle_q8_encode(_u16(w), n, k, _u8(blob), size) != size:
+        raise ValueError("bad arguments or a non-finite weight")
+    return blob
+
+
+def q8_decode(blob: np.ndarray, n: int, k: int) -> tuple[np.ndarray, np.ndarray]:
+    """(scales float32 [N], q int8 [N, K]) held by a Q8 blob."""
+    blob = np.ascontiguousarray(blob, dtype=np.uint8)
+    s = np.empty(n, dtype=np.float32)
+    q = np.empty((n, k), dtype=np.int8)
+    rc = _load().oracle_q8_decode(_u8(blob), blob.size, s.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                  q.ctypes.data_as(ctypes.POINTER(ctypes.c_int8)))
+    if rc != 0:
+        raise ValueError("malformed Q8 blob")
+    return s, q
+
+
+def q8_gemm_f64(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """y[m, n] = s[n] * sum_k x[m, k] * q[n, k] in float64, (s, q) the
+    oracle's own Q8 copy of w."""
+    x = _as_u16(x)
+    w = _as_u16(w)
+    s, q = q8_decode(q8_encode(w), w.shape[0], w.shape[1])
+    xf = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return (xf @ q.astype(np.float64).T) * s.astype(np.float64)[None, :]
 
 
 def max_threads(threads: int = 0) -> int:

@@ -19,6 +19,7 @@
  */
 #include "w12_oracle.h"
 
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
@@ -522,4 +523,134 @@ int oracle_w12_gemm_f64(const uint16_t *x, const uint8_t *blob, int64_t len,
     }
     free(w);
     return bad ? -1 : 0;
+}
+
+/* ======================================================================
+ * Q8: the 8-bit weight copy used by the first level of a two-level
+ * verification ("SpecPilot: an agent doubled speculative decoding speed, and
+ * the 10.87x needs context", §The mechanisms it found, names a two-level
+ * verification with an 8-bit or INT6/INT8 copy of the weights; the page gives
+ * no scheme).  Reading taken: symmetric INT8 per output row.
+ *   a[n] = max_k |W[n][k]|, s[n] = a[n] / 127 (fp32), q = rint(W / s) in fp32
+ *   (nearest, ties to even), clamped to [-127, 127]; a zero row has s = 0 and
+ *   q = 0.  A row holding Inf or NaN cannot be quantized (error).
+ *   The product it feeds: y[m][n] = s[n] * sum_k x[m][k] * q[n][k].
+ * Layout (Q8 v1): header 256 B | scales fp32[N_pad] (pad rows 0) | q plane,
+ * each part 256-byte aligned.  q plane: per 128-row tile, per 32-column
+ * chunk, two 2048-byte slabs of 128 rows x 16 bytes (columns 0-15, 16-31);
+ * padded entries are 0.  Header: 0x00 "Q8W1", 0x04 u32 1, 0x08 u32 256,
+ * 0x0C u32 0, 0x10 N, 0x18 K, 0x20 N_pad, 0x28 K_pad, 0x30 tiles, 0x38 chunks,
+ * 0x40/0x48 scales offset/size, 0x50/0x58 q offset/size, 0x60 total.
+ * ====================================================================== */
+
+typedef struct {
+    int64_t N, K, Npad, Kpad, tiles, chunks;
+    int64_t off_s, bytes_s, off_q, bytes_q, total;
+} o_q8geom;
+
+static void o_q8_geometry(int64_t N, int64_t K, o_q8geom *g)
+{
+    g->N = N;
+    g->K = K;
+    g->Npad = o_up(N, 128);
+    g->Kpad = o_up(K, 32);
+    g->tiles = g->Npad / 128;
+    g->chunks = g->Kpad / 32;
+    g->off_s = 256;
+    g->bytes_s = 4 * g->Npad;
+    g->off_q = o_up(g->off_s + g->bytes_s, 256);
+    g->bytes_q = 4096 * g->tiles * g->chunks;
+    g->total = o_up(g->off_q + g->bytes_q, 256);
+}
+
+static float o_bf16_to_float(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+int64_t oracle_q8_size(int64_t N, int64_t K)
+{
+    o_q8geom g;
+    if (N < 1 || K < 1)
+        return -1;
+    o_q8_geometry(N, K, &g);
+    return g.total;
+}
+
+int64_t oracle_q8_encode(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, int64_t cap)
+{
+    o_q8geom g;
+    int64_t n, k;
+    if (!w || !blob || N < 1 || K < 1)
+        return -1;
+    o_q8_geometry(N, K, &g);
+    if (cap < g.total)
+        return -1;
+    memset(blob, 0, (size_t)g.total);
+    for (n = 0; n < N; ++n) {
+        float a = 0.0f, s;
+        for (k = 0; k < K; ++k) {
+            float v = o_bf16_to_float(w[n * K + k]);
+            if (!(v - v == 0.0f))
+                return -1; /* Inf or NaN */
+            if (fabsf(v) > a)
+                a = fabsf(v);
+        }
+        s = a / 127.0f;
+        memcpy(blob + g.off_s + 4 * n, &s, 4);
+        for (k = 0; k < K; ++k) {
+            int64_t t = n / 128, r = n % 128, c = k / 32, col = k % 32;
+            float q = 0.0f;
+            int qi;
+            if (a > 0.0f) {
+                q = rintf(o_bf16_to_float(w[n * K + k]) / s);
+                if (q > 127.0f) q = 127.0f;
+                if (q < -127.0f) q = -127.0f;
+            }
+            qi = (int)q;
+            blob[g.off_q + 4096 * (t * g.chunks + c) + 2048 * (col / 16) + 16 * r + col % 16] = (uint8_t)(int8_t)qi;
+        }
+    }
+    o_put(blob + 0x00, 0x31573851u, 4); /* "Q8W1" */
+    o_put(blob + 0x04, 1, 4);
+    o_put(blob + 0x08, 256, 4);
+    o_put(blob + 0x10, (uint64_t)g.N, 8);
+    o_put(blob + 0x18, (uint64_t)g.K, 8);
+    o_put(blob + 0x20, (uint64_t)g.Npad, 8);
+    o_put(blob + 0x28, (uint64_t)g.Kpad, 8);
+    o_put(blob + 0x30, (uint64_t)g.tiles, 8);
+    o_put(blob + 0x38, (uint64_t)g.chunks, 8);
+    o_put(blob + 0x40, (uint64_t)g.off_s, 8);
+    o_put(blob + 0x48, (uint64_t)g.bytes_s, 8);
+    o_put(blob + 0x50, (uint64_t)g.off_q, 8);
+    o_put(blob + 0x58, (uint64_t)g.bytes_q, 8);
+    o_put(blob + 0x60, (uint64_t)g.total, 8);
+    return g.total;
+}
+
+int oracle_q8_decode(const uint8_t *blob, int64_t len, float *scales, int8_t *q)
+{
+    o_q8geom g;
+    int64_t N, K, n, k;
+    if (!blob || len < 256 || o_get(blob, 4) != 0x31573851u || o_get(blob + 4, 4) != 1)
+        return -1;
+    N = (int64_t)o_get(blob + 0x10, 8);
+    K = (int64_t)o_get(blob + 0x18, 8);
+    if (N < 1 || K < 1)
+        return -1;
+    o_q8_geometry(N, K, &g);
+    if ((int64_t)o_get(blob + 0x60, 8) != g.total || len < g.total ||
+        (int64_t)o_get(blob + 0x50, 8) != g.off_q)
+        return -1;
+    for (n = 0; n < N; ++n) {
+        memcpy(&scales[n], blob + g.off_s + 4 * n, 4);
+        for (k = 0; k < K; ++k) {
+            int64_t t = n / 128, r = n % 128, c = k / 32, col = k % 32;
+            q[n * K + k] = (int8_t)blob[g.off_q + 4096 * (t * g.chunks + c) + 2048 * (col / 16) + 16 * r + col % 16];
+        }
+    }
+    return 0;
 }

@@ -27,6 +27,8 @@
  *                   example, table-optimality and escape-mass invariants, the
  *                   size closed form, normal-CDF escape rate on Gaussian data.
  *   gemm_f64      : numpy float64 matmul, one-hot and small-integer exact cases.
+ *   q8 encode     : a hand-worked row, the scale/range invariants, the
+ *                   half-step rounding bound, ties to even.
  */
 #ifndef W12_ORACLE_H
 #define W12_ORACLE_H
@@ -67,6 +69,17 @@ int oracle_w12_gemm_f64(const uint16_t *x, const uint8_t *blob, int64_t len,
 
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int oracle_max_threads(int threads);
+
+/* Q8 weight copy (see w12_oracle.c for the scheme and layout).  Size of the
+ * Q8 v1 blob of an N x K matrix (-1 on bad arguments). */
+int64_t oracle_q8_size(int64_t N, int64_t K);
+
+/* Quantize w (N x K BF16 bit patterns) into blob; returns the size, or -1 on
+ * bad arguments, a short buffer or a non-finite weight. */
+int64_t oracle_q8_encode(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, int64_t cap);
+
+/* Read scales[N] and q[N*K] (row-major) back from a Q8 blob; 0 on success. */
+int oracle_q8_decode(const uint8_t *blob, int64_t len, float *scales, int8_t *q);
 
 #ifdef __cplusplus
 }

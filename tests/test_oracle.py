@@ -287,3 +287,42 @@ def test_argmax_f64_ties_nan_and_brute_force():
                 if y[m, n] > best:
                     best, arg = y[m, n], n
             assert idx[m] == arg
+
+
+def test_q8_hand_worked_row():
+    """Row maximum 127/64 makes the scale exactly 1/64, so q = rint(64 w) can
+    be worked by hand: 32.5 -> 32 and 33.5 -> 34 (ties to even)."""
+    vals = np.array([127 / 64, 32.5 / 64, 33.5 / 64, -32.5 / 64, 0.0, -127 / 64, 1 / 128, 3 / 128],
+                    dtype=np.float32)
+    w = wl.to_bf16_bits(vals[None, :])
+    assert np.array_equal(wl.bf16_bits_to_f32(w)[0], vals)  # all exact in BF16
+    s, q = oracle.q8_decode(oracle.q8_encode(w), 1, 8)
+    assert s[0] == np.float32(1 / 64)
+    assert q[0].tolist() == [127, 32, 34, -32, 0, -127, 0, 2]  # 0.5 -> 0 and 1.5 -> 2: ties to even
+
+
+def test_q8_invariants_and_layout():
+    rng = np.random.default_rng(14)
+    w = wl.heavy_tail_weights(300, 333, seed=15)
+    w[7] = 0  # a zero row
+    s, q = oracle.q8_decode(oracle.q8_encode(w), 300, 333)
+    wf = wl.bf16_bits_to_f32(w).astype(np.float64)
+    nz = np.abs(wf).max(axis=1) > 0
+    assert np.all(np.abs(q).max(axis=1)[nz] == 127) and s[7] == 0 and not q[7].any()
+    # each entry within half a step of its weight (plus the fp32 rounding of s)
+    err = np.abs(wf - s.astype(np.float64)[:, None] * q)
+    assert np.all(err <= 0.5 * s.astype(np.float64)[:, None] * (1 + 1e-5) + 1e-30)
+    # byte position of (n=129, k=40): tile 1, chunk 1, slab 0 (column 8), row 1
+    w2 = np.zeros((130, 64), dtype=np.uint16)
+    w2[129, 40] = np.uint16(0xBF80)  # -1.0
+    b = oracle.q8_encode(w2)
+    off_q = int(b[0x50:0x58].view(np.uint64)[0])
+    chunks = 2
+    assert b[off_q + 4096 * (1 * chunks + 1) + 16 * 1 + 8] == np.uint8(256 - 127)
+    assert int(np.count_nonzero(b[off_q:])) == 1
+    assert b[:4].tobytes() == b"Q8W1"
+    bad = w.copy()
+    bad[3, 3] = np.uint16(0x7F80)  # +Inf
+    with pytest.raises(ValueError):
+        oracle.q8_encode(bad)
+    del rng
