@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
     ap.add_argument("--m", type=int, default=1, help="tokens per GEMM (1..32)")
     ap.add_argument("--workload", default="layer", choices=["layer", "heavy", "model64", "lmhead"])
+    ap.add_argument("--weights", default="w12", choices=["w12", "q8"],
+                    help="w12: the lossless format; q8: the 8-bit verification copy of the same weights")
     ap.add_argument("--graph", action="store_true", help="replay the step as a CUDA graph")
     ap.add_argument("--no-bf16", action="store_true", help="skip the cuBLAS BF16 comparator")
     ap.add_argument("--no-e2e", action="store_true")
@@ -274,7 +276,7 @@ def run_w12(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    from lossless_bit_weight_encode_gb300 import W12Weight, w12
+    from lossless_bit_weight_encode_gb300 import Q8Weight, W12Weight, w12
     from lossless_bit_weight_encode_gb300 import build as libbuild
     from lossless_bit_weight_encode_gb300 import workloads as wl
 
@@ -317,7 +319,7 @@ def run_w12(args):
             keep = set(args.matrices.split(","))
             weights = [(n, w) for n, w in weights if n in keep]
         names = [n for n, _ in weights]
-        mats = [W12Weight(w) for _, w in weights]
+        mats = [Q8Weight(w) if args.weights == "q8" else W12Weight(w) for _, w in weights]
         xs_host = [wl.activations(M, w.shape[1], seed=wl.activation_seed(args.workload, M)) for _, w in weights]
         xs = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs_host]
         wss = [m.workspace(M) for m in mats]
@@ -343,7 +345,7 @@ def run_w12(args):
     else:
         calls = [(x.data_ptr(), m.blob.data_ptr(), m.info, y.data_ptr(), M, ws.data_ptr(), ws.numel(), sh)
                  for x, m, y, ws in zip(xs, mats, ys, wss)]
-        launch = w12.w12_gemm_ptr
+        launch = w12.w12_q8_gemm_ptr if args.weights == "q8" else w12.w12_gemm_ptr
 
     def step():
         for c in calls:
@@ -406,7 +408,8 @@ def run_w12(args):
     w12.w12_check_status()
     launch_ms = [statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(kp)) for i in range(nl)]
 
-    kernel_name = "w12_gemv_kernel" if w12.w12_gemm_launch_info(mats[0].info, M).get("ntok") and M == 1 \
+    kernel_name = "w12_gemm_tc_kernel (Q8 copy)" if args.weights == "q8" else \
+        "w12_gemv_kernel" if w12.w12_gemm_launch_info(mats[0].info, M).get("ntok") and M == 1 \
         and os.environ.get("W12_M1_PATH", "") != "tc" else "w12_gemm_tc_kernel"
     layer_weights = sum(m.N * m.K for m in mats)
     packed = sum(int(m.info.total_bytes) for m in mats)
@@ -460,7 +463,7 @@ def run_w12(args):
                     w12.w12_gemm_argmax(x, m.blob, m.info, M, None, idx, val, m.argmax_workspace(M), stream)
                     idx_h.copy_(idx, non_blocking=True)
                 else:
-                    w12.w12_gemm(x, m.blob, m.info, y, M, ws, stream)
+                    m.gemm(x, out=y, stream=stream)
                     yhi.copy_(y, non_blocking=True)
 
         for _ in range(args.warmup):
@@ -519,7 +522,8 @@ def run_w12(args):
             "packed_GBps": round(packed / (ms_step * 1e-3) / 1e9, 1),
             "packed_frac_of_hbm_peak": round(packed / (ms_step * 1e-3) / 1e9 / peak, 4),
             "bits_per_weight": round(8.0 * packed / layer_weights, 5),
-            "n_escapes": int(sum(int(m.info.n_escapes) for m in mats)),
+            "n_escapes": int(sum(int(getattr(m.info, "n_escapes", 0)) for m in mats)),
+            "weights": args.weights,
             "per_matrix_us": {n: round(statistics.mean(launch_ms[i::nshape]) * 1e3, 2)
                               for i, (n, _, _) in enumerate(wl.LAYER_SHAPES)}
                              if args.workload == "model64" else

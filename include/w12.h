@@ -249,6 +249,53 @@ int w12_encode_device(const uint16_t *w_dev, int64_t N, int64_t K, void *blob_de
                       void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * ---------------------------------------------------------------- Q8 copy
+ * An 8-bit copy of a weight matrix for the first level of a two-level
+ * verification ("SpecPilot: an agent doubled speculative decoding speed, and
+ * the 10.87x needs context" (ai.jakubjirak.com), §The mechanisms it found,
+ * names a two-level verification with an 8-bit or INT6/INT8 weight copy; it
+ * gives no scheme).  Reading taken: symmetric INT8 per output row, lossy by
+ * design (it only drafts; W12 stays the exact weights):
+ *   a[n] = max_k |W[n][k]|, s[n] = a[n] / 127 in fp32, q[n][k] = rint(W[n][k]
+ *   / s[n]) in fp32 (nearest, ties to even) clamped to [-127, 127]; a zero row
+ *   has s = 0, q = 0; a row with Inf or NaN is rejected (INVALID_ARG).
+ * Q8 v1 blob: 256-byte header | scales fp32[N_pad] (pad rows 0) | q plane,
+ * each part 256-byte aligned.  q plane: per 128-row tile, per 32-column chunk
+ * (chunks in column order), two 2048-byte slabs of 128 rows x 16 int8
+ * (columns 0-15, then 16-31); padding is 0.  Header (little-endian): 0x00
+ * "Q8W1", 0x04 u32 1, 0x08 u32 256, 0x0C u32 0, 0x10 i64 N, 0x18 K, 0x20 N_pad,
+ * 0x28 K_pad, 0x30 tiles, 0x38 chunks, 0x40/0x48 u64 scales offset/size,
+ * 0x50/0x58 q offset/size, 0x60 total; the rest 0.
+ */
+typedef struct w12_q8_info {
+    int64_t N, K, N_pad, K_pad, tiles, chunks, segs;
+    uint64_t off_scales, bytes_scales, off_q, bytes_q, total_bytes;
+} w12_q8_info;
+
+/* Blob size for an N x K matrix (SHAPE on bad sizes). */
+int w12_q8_encoded_size(int64_t N, int64_t K, size_t *bytes);
+
+/* Quantize w_host (N x K BF16 bit patterns) into blob_host (>= the size);
+ * canonical bytes; all host cores. */
+int w12_q8_encode_host(const uint16_t *w_host, int64_t N, int64_t K, void *blob_host, size_t bytes);
+
+/* Check the header of a Q8 blob (a host copy of its first 256 bytes is
+ * enough) and fill *out.  CORRUPT_BLOB / BUFFER_TOO_SMALL as w12_blob_info. */
+int w12_q8_blob_info(const void *blob_host, size_t bytes, w12_q8_info *out);
+
+/* Workspace bytes w12_q8_gemm needs (1 <= M <= 32). */
+int w12_q8_gemm_workspace_size(const w12_q8_info *info, int M, size_t *bytes);
+
+/*
+ * y_dev[m * N + n] = BF16_rne( s[n] * sum_k x_dev[m * K + k] * q[n][k] ), fp32
+ * accumulation and scale multiply, 1 <= M <= 32, on the same tcgen05 kernel as
+ * w12_gemm (the copy is converted to BF16 exactly in registers: |q| <= 127).
+ * Arguments, alignment, workspace rules and errors as w12_gemm.
+ */
+int w12_q8_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_q8_info *info,
+                uint16_t *y_dev, int M, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's status word,
  * which kernels set when a bounded wait gives up (TIMEOUT) or the device
  * encoder finds its output buffer too short (BUFFER_TOO_SMALL) or too many

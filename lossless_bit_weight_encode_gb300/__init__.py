@@ -11,7 +11,7 @@ import numpy as np
 from . import w12
 from .w12 import W12Error
 
-__all__ = ["w12", "W12Error", "W12Weight"]
+__all__ = ["w12", "W12Error", "W12Weight", "Q8Weight"]
 
 
 class W12Weight:
@@ -110,4 +110,41 @@ class W12Weight:
         if out is None:
             out = torch.empty((self.N, self.K), dtype=torch.bfloat16, device=self.blob.device)
         w12.w12_decode(self.blob, self.info, out, stream)
+        return out
+
+
+class Q8Weight:
+    """The 8-bit (symmetric INT8 per row) copy of a weight matrix on the
+    device, for the first level of a two-level verification.  Lossy by design:
+    ``gemm(x)`` returns ``x . (s * q)^T`` (BF16) for x [M, K], 1 <= M <= 32."""
+
+    def __init__(self, bits: np.ndarray, device=None):
+        import torch
+
+        self.blob_host = w12.w12_q8_encode_host(bits)
+        self.info = w12.w12_q8_blob_info(self.blob_host)
+        self.N, self.K = int(self.info.N), int(self.info.K)
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.blob = torch.from_numpy(self.blob_host).to(dev)
+        self._ws = {}
+
+    def workspace(self, M: int):
+        import torch
+
+        size = w12.w12_q8_gemm_workspace_size(self.info, M)
+        ws = self._ws.get(M)
+        if ws is None or ws.numel() < size:
+            ws = torch.zeros(max(size, 256), dtype=torch.uint8, device=self.blob.device)
+            self._ws[M] = ws
+        return ws
+
+    def gemm(self, x, out=None, stream=None):
+        import torch
+
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != self.K or not x.is_contiguous():
+            raise ValueError("x must be a contiguous BF16 tensor of shape [M, K]")
+        M = int(x.shape[0])
+        if out is None:
+            out = torch.empty((M, self.N), dtype=torch.bfloat16, device=x.device)
+        w12.w12_q8_gemm(x, self.blob, self.info, out, M, self.workspace(M), stream)
         return out

@@ -17,7 +17,7 @@ NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 CUDA_SOURCES = ["kernels.cu"]
-CXX_SOURCES = ["encoder.cpp", "capi.cpp"]
+CXX_SOURCES = ["encoder.cpp", "q8_host.cpp", "capi.cpp"]
 
 
 def _inputs():

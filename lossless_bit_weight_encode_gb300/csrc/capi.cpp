@@ -47,6 +47,21 @@ int check_info(const w12_info *info, std::string &err) {
     return W12_OK;
 }
 
+int check_q8_info(const w12_q8_info *info, std::string &err) {
+    if (!info) {
+        err = "info is null";
+        return W12_ERR_INVALID_ARG;
+    }
+    const w12::q8::Geometry g = w12::q8::Geometry::of(info->N, info->K);
+    if (info->N < 1 || info->K < 1 || info->tiles != g.tiles || info->chunks != g.chunks || info->segs != g.segs ||
+        info->N_pad != g.Npad || info->K_pad != g.Kpad || info->off_scales != g.off_s || info->off_q != g.off_q ||
+        info->total_bytes != g.total) {
+        err = "info does not describe a Q8 v1 blob (fill it with w12_q8_blob_info)";
+        return W12_ERR_INVALID_ARG;
+    }
+    return W12_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -266,6 +281,64 @@ int w12_encode_device(const uint16_t *w_dev, int64_t N, int64_t K, void *blob_de
             return (int)W12_ERR_ALIGNMENT;
         }
         return w12::launch::encode_device(w_dev, N, K, blob_dev, bytes, workspace, ws_bytes, stream, &err);
+    });
+}
+
+int w12_q8_encoded_size(int64_t N, int64_t K, size_t *bytes) {
+    return guarded([&](std::string &err) {
+        if (!bytes) {
+            err = "null pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        uint64_t b = 0;
+        const int rc = w12::host::q8_encoded_size(N, K, &b, &err);
+        if (rc == W12_OK) *bytes = (size_t)b;
+        return rc;
+    });
+}
+
+int w12_q8_encode_host(const uint16_t *w_host, int64_t N, int64_t K, void *blob_host, size_t bytes) {
+    return guarded([&](std::string &err) {
+        return w12::host::q8_encode(w_host, N, K, static_cast<uint8_t *>(blob_host), bytes, &err);
+    });
+}
+
+int w12_q8_blob_info(const void *blob_host, size_t bytes, w12_q8_info *out) {
+    return guarded([&](std::string &err) {
+        return w12::host::q8_parse_header(static_cast<const uint8_t *>(blob_host), bytes, out, &err);
+    });
+}
+
+int w12_q8_gemm_workspace_size(const w12_q8_info *info, int M, size_t *bytes) {
+    return guarded([&](std::string &err) {
+        int rc = check_q8_info(info, err);
+        if (rc != W12_OK) return rc;
+        if (!bytes) {
+            err = "null pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        return w12::launch::q8_workspace_size(*info, M, bytes, &err);
+    });
+}
+
+int w12_q8_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_q8_info *info, uint16_t *y_dev, int M,
+                void *workspace, size_t ws_bytes, void *stream) {
+    return guarded([&](std::string &err) {
+        int rc = check_q8_info(info, err);
+        if (rc != W12_OK) return rc;
+        if (!x_dev || !blob_dev || !y_dev || !workspace) {
+            err = "null device pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (M < 1 || M > 32) {
+            err = "M must be in 1..32";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (!aligned(blob_dev, 256) || !aligned(workspace, 256) || !aligned(y_dev, 2) || !aligned(x_dev, 2)) {
+            err = "blob_dev and workspace must be 256-byte aligned, x_dev and y_dev 2-byte aligned";
+            return (int)W12_ERR_ALIGNMENT;
+        }
+        return w12::launch::q8_gemm(x_dev, blob_dev, *info, y_dev, M, workspace, ws_bytes, stream, &err);
     });
 }
 

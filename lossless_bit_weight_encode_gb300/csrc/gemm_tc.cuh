@@ -59,25 +59,28 @@ struct GemmParams {
     uint32_t *counters;       // [tiles] arrival counters (splits > 1)
     uint16_t *y;              // [M][N] BF16 (may be null when amax is set)
     unsigned long long *amax; // [M] argmax keys (null: plain GEMM)
+    const float *scales;      // [Npad] per-row scales of a Q8 copy (null: W12)
     uint32_t *status;         // device status word
     uint64_t timeout_ns;
 };
 
-template <int NTOK, int STAGES, bool A_SMEM>
+template <int NTOK, int STAGES, bool A_SMEM, bool Q8 = false>
 struct GemmCfg {
+    static constexpr bool kQ8 = Q8;                             // weights: Q8 copy instead of W12
+    static constexpr int kChunkB = Q8 ? q8::kChunkBytes : kChunkBytes;
     static constexpr int kThreads = 320;
     static constexpr int kDecWarps = 8;
     static constexpr int kStages = STAGES;
     static constexpr bool kASmem = A_SMEM;
     static constexpr int kNtok = NTOK;
-    static constexpr int kWBytes = 2 * kChunkBytes;             // weight stage: 2 chunks
+    static constexpr int kWBytes = 2 * kChunkB;                 // weight stage: 2 chunks
     static constexpr int kXBoxBytes = NTOK * 128;               // one 64-column x box
     static constexpr int kXBytes = 4 * kXBoxBytes;              // x tile of one segment
     static constexpr int kSegSlots = 2;                         // x + escapes per segment
     static constexpr int kASlots = 3;                             // one weight stage (2 chunks) each
     static constexpr int kASlotBytes = 2 * kTileRows * kChunkK * 2;  // 16 KB (SMEM A variant)
     static constexpr int kAChunkBytes = kTileRows * kChunkK * 2;     // 8 KB per chunk
-    static constexpr int kEscCap = 2048;
+    static constexpr int kEscCap = Q8 ? 0 : 2048;
     static constexpr int kMaxSegs = 96;   // segments per CTA (K range <= 24576)
     static constexpr int kTmemCols = 128;
     static constexpr int kDCol = 0;
@@ -139,15 +142,18 @@ __device__ __forceinline__ bool escapes_staged(uint32_t total) {
 // issued after griddepcontrol.wait, so a blob written by that previous kernel
 // is still read correctly.
 constexpr uint32_t kPrefetchBytes = 96 * 1024;
+template <int kChunkB, bool kHeaders>
 __device__ __forceinline__ void prefetch_cta_weights(const GemmParams &p, int64_t tile, int s0, int c0, int c1) {
-    const int nsegs_cta = (c1 - c0 + kChunksPerSeg - 1) / kChunksPerSeg;
-    prefetch_l2(p.blob + p.off_seg + (uint64_t)(tile * p.segs + s0) * kSegHdrBytes,
-                (uint32_t)nsegs_cta * kSegHdrBytes);
-    const uint8_t *w = p.blob + p.off_w + (uint64_t)(tile * p.chunks + c0) * kChunkBytes;
-    uint32_t left = (uint32_t)(c1 - c0) * kChunkBytes;
+    if (kHeaders) {
+        const int nsegs_cta = (c1 - c0 + kChunksPerSeg - 1) / kChunksPerSeg;
+        prefetch_l2(p.blob + p.off_seg + (uint64_t)(tile * p.segs + s0) * kSegHdrBytes,
+                    (uint32_t)nsegs_cta * kSegHdrBytes);
+    }
+    const uint8_t *w = p.blob + p.off_w + (uint64_t)(tile * p.chunks + c0) * kChunkB;
+    uint32_t left = (uint32_t)(c1 - c0) * kChunkB;
     if (left > kPrefetchBytes) left = kPrefetchBytes;
-    for (uint32_t off = 0; off < left; off += 4 * kChunkBytes) {
-        const uint32_t n = left - off < 4u * kChunkBytes ? left - off : 4u * kChunkBytes;
+    for (uint32_t off = 0; off < left; off += 4 * kChunkB) {
+        const uint32_t n = left - off < 4u * kChunkB ? left - off : 4u * kChunkB;
         prefetch_l2(w + off, n);
     }
 }
@@ -163,9 +169,13 @@ __device__ void gemm_producer(const GemmParams &p, const CUtensorMap *tmap, uint
     uint8_t *hdr = smem + C::kOffHdr;
     prefetch_tmap(tmap);
 
-    const uint32_t hbytes = (uint32_t)nsegs_cta * kSegHdrBytes;
-    mbar_arrive_expect_tx(b.hdr, hbytes);
-    bulk_g2s(hdr, p.blob + p.off_seg + (uint64_t)(tile * p.segs + s0) * kSegHdrBytes, hbytes, b.hdr);
+    if constexpr (C::kQ8) {
+        mbar_arrive(b.hdr);  // a Q8 copy has no segment headers
+    } else {
+        const uint32_t hbytes = (uint32_t)nsegs_cta * kSegHdrBytes;
+        mbar_arrive_expect_tx(b.hdr, hbytes);
+        bulk_g2s(hdr, p.blob + p.off_seg + (uint64_t)(tile * p.segs + s0) * kSegHdrBytes, hbytes, b.hdr);
+    }
     bool hdr_ready = false;
     int issued = 0, seg_issued = 0;
     bool failed = false;
@@ -180,9 +190,9 @@ __device__ void gemm_producer(const GemmParams &p, const CUtensorMap *tmap, uint
             break;
         }
         const int nch = min(2, c1 - chunk);
-        mbar_arrive_expect_tx(b.wfull + slot, (uint32_t)(nch * kChunkBytes));
+        mbar_arrive_expect_tx(b.wfull + slot, (uint32_t)(nch * C::kChunkB));
         bulk_g2s(smem + C::kOffW + slot * C::kWBytes,
-                 p.blob + p.off_w + (uint64_t)(tile * p.chunks + chunk) * kChunkBytes, (uint32_t)(nch * kChunkBytes),
+                 p.blob + p.off_w + (uint64_t)(tile * p.chunks + chunk) * C::kChunkB, (uint32_t)(nch * C::kChunkB),
                  b.wfull + slot);
         issued = st + 1;
         if ((chunk & (kChunksPerSeg - 1)) == 0) {
@@ -200,18 +210,21 @@ __device__ void gemm_producer(const GemmParams &p, const CUtensorMap *tmap, uint
             for (int bx = 0; bx < 4; ++bx)
                 tma_load_2d(xs + bx * C::kXBoxBytes, tmap, chunk * kChunkK + bx * 64, 0, b.sfull + sslot);
             seg_issued = ls + 1;
-            if (!hdr_ready) {
-                if (!mbar_wait(b.hdr, 0, deadline)) { failed = true; break; }
-                hdr_ready = true;
-            }
-            const uint4 meta = *reinterpret_cast<const uint4 *>(hdr + ls * kSegHdrBytes + 16);
-            const uint32_t base = meta.x;
-            const uint32_t total = seg_escape_total(meta);
-            if (escapes_staged<C>(total)) {
-                const uint32_t src0 = base & ~15u;
-                const uint32_t ebytes = ((base + total + 15u) & ~15u) - src0;
-                mbar_expect_tx(b.sfull + sslot, ebytes);
-                bulk_g2s(smem + C::kOffEsc + sslot * C::kEscCap, p.blob + p.off_esc + src0, ebytes, b.sfull + sslot);
+            if constexpr (!C::kQ8) {
+                if (!hdr_ready) {
+                    if (!mbar_wait(b.hdr, 0, deadline)) { failed = true; break; }
+                    hdr_ready = true;
+                }
+                const uint4 meta = *reinterpret_cast<const uint4 *>(hdr + ls * kSegHdrBytes + 16);
+                const uint32_t base = meta.x;
+                const uint32_t total = seg_escape_total(meta);
+                if (escapes_staged<C>(total)) {
+                    const uint32_t src0 = base & ~15u;
+                    const uint32_t ebytes = ((base + total + 15u) & ~15u) - src0;
+                    mbar_expect_tx(b.sfull + sslot, ebytes);
+                    bulk_g2s(smem + C::kOffEsc + sslot * C::kEscCap, p.blob + p.off_esc + src0, ebytes,
+                             b.sfull + sslot);
+                }
             }
             mbar_arrive(b.sfull + sslot);
         }
@@ -330,7 +343,7 @@ __device__ void gemm_decode(const GemmParams &p, uint8_t *smem, const Bars &b, v
         const int jj0 = chunk0 & (kChunksPerSeg - 1);
         const int ls = st / (kChunksPerSeg / 2);
         const int nch = min(2, c1 - chunk0);
-        if (jj0 == 0) {
+        if (!C::kQ8 && jj0 == 0) {
             const uint8_t *hp = hdr + (chunk0 / kChunksPerSeg - s0) * kSegHdrBytes;
             T = make_table(*reinterpret_cast<const uint4 *>(hp));
             const uint4 meta = *reinterpret_cast<const uint4 *>(hp + 16);
@@ -353,16 +366,20 @@ __device__ void gemm_decode(const GemmParams &p, uint8_t *smem, const Bars &b, v
         }
         const uint32_t sa = s_row + (uint32_t)(slot * C::kWBytes);
         const uint4 sb0 = lds128(sa);
-        const uint4 cd0 = lds128(sa + c_off);
+        const uint4 cd0 = C::kQ8 ? make_uint4(0, 0, 0, 0) : lds128(sa + c_off);
         uint4 sb1 = make_uint4(0, 0, 0, 0), cd1 = make_uint4(0, 0, 0, 0);
         if (nch == 2) {
-            sb1 = lds128(sa + kChunkBytes);
-            cd1 = lds128(sa + kChunkBytes + c_off);
+            sb1 = lds128(sa + C::kChunkB);
+            if (!C::kQ8) cd1 = lds128(sa + C::kChunkB + c_off);
         }
         warp_arrive(b.wempty + slot);  // this warp is done with the stage's bytes
 
         uint32_t out0[8], out1[8];
-        if (nch == 2 && ((mask_q >> jj0) & 3u) == 0) {
+        if constexpr (C::kQ8) {
+            // 8-bit copy: 16 int8 per chunk half, exact in BF16
+            q8_half(sb0, out0);
+            q8_half(sb1, out1);  // a short last stage leaves these columns unread
+        } else if (nch == 2 && ((mask_q >> jj0) & 3u) == 0) {
             // common case, decided once per stage for the whole warp: two
             // chunks without escapes
             uint32_t E[4];
@@ -472,6 +489,7 @@ __device__ __forceinline__ void reduce_splits(const GemmParams &p, int64_t tile,
                 for (int u = 0; u < 8; ++u) s += v[u];
             }
             for (; sp < p.splits; ++sp) s += __ldcg(src + sp * sstride);
+            if (p.scales != nullptr) s *= p.scales[tile * kTileRows + rr];
             if (p.y != nullptr && valid) p.y[(int64_t)m * p.N + tile * kTileRows + rr] = bf16_bits_rn(s);
             if (p.amax != nullptr)
                 argmax_warp(p.amax + m, valid ? argmax_key(s, (uint32_t)(tile * kTileRows + rr)) : 0ull);
@@ -509,6 +527,11 @@ __device__ __forceinline__ void reduce_splits(const GemmParams &p, int64_t tile,
 #pragma unroll
             for (int b = 0; b < kBatch; ++b)
                 s[b] += (ok >> b) & 1u ? __ldcg(src + sp * sstride + (int64_t)(b * kTokStep) * p.Npad) : 0.0f;
+        }
+        if (p.scales != nullptr) {
+            const float sc = p.scales[tile * kTileRows + o0 % kTileRows];  // one row for all b
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) s[b] *= sc;
         }
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
@@ -559,6 +582,11 @@ __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint3
     }
     const int64_t n = tile * kTileRows + 32 * q + lane;
     if (p.splits == 1) {
+        if (p.scales != nullptr) {
+            const float sc = p.scales[n];  // rows past N have scale 0
+#pragma unroll
+            for (int m = 0; m < kHalf; ++m) acc[m] *= sc;
+        }
         if (p.y != nullptr && n < p.N) {
 #pragma unroll
             for (int m = 0; m < kHalf; ++m)
@@ -603,10 +631,10 @@ __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint3
 }
 
 // ------------------------------------------------------------------ kernel
-template <int NTOK, int STAGES, bool A_SMEM>
+template <int NTOK, int STAGES, bool A_SMEM, bool Q8 = false>
 __global__ void __launch_bounds__(320, NTOK == 16 ? 3 : 2)
     w12_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_x) {
-    using C = GemmCfg<NTOK, STAGES, A_SMEM>;
+    using C = GemmCfg<NTOK, STAGES, A_SMEM, Q8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBars);
@@ -667,7 +695,7 @@ __global__ void __launch_bounds__(320, NTOK == 16 ? 3 : 2)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (threadIdx.x == 0) pdl_launch_dependents();
-    if (warp == 8 && (threadIdx.x & 31) == 0) prefetch_cta_weights(p, tile, s0, c0, c1);
+    if (warp == 8 && (threadIdx.x & 31) == 0) prefetch_cta_weights<C::kChunkB, !Q8>(p, tile, s0, c0, c1);
     pdl_wait();
 
     if (warp == 8) {

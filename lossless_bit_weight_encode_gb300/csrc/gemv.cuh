@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(288, 2)
     }
     __syncthreads();
     if (threadIdx.x == 0) pdl_launch_dependents();
-    if (warp == 8 && (threadIdx.x & 31) == 0) prefetch_cta_weights(p, tile, s0, c0, c1);
+    if (warp == 8 && (threadIdx.x & 31) == 0) prefetch_cta_weights<kChunkBytes, true>(p, tile, s0, c0, c1);
     pdl_wait();
     if (warp == 8) {
         if ((threadIdx.x & 31) == 0) gemv_producer<C>(p, &tmap_x, smem, b, abort_flag, tile, s0, c0, c1, deadline);

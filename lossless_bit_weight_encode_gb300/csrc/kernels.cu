@@ -72,19 +72,20 @@ struct DeviceState {
     int sm_count = 0;
     uint32_t *status = nullptr;
     int occupancy[2][2] = {{0, 0}, {0, 0}};  // [ntok==32][a_smem]
+    int q8_occupancy[2] = {0, 0};            // [ntok==32], Q8 copy kernels
     int gemv_occupancy = 0;
 };
 
 DeviceState g_state[kMaxDevices];
 std::mutex g_mu;
 
-template <int NTOK, bool ASMEM>
+template <int NTOK, bool ASMEM, bool Q8 = false>
 void *gemm_kernel_ptr() {
-    return reinterpret_cast<void *>(&dev::w12_gemm_tc_kernel<NTOK, kStages, ASMEM>);
+    return reinterpret_cast<void *>(&dev::w12_gemm_tc_kernel<NTOK, kStages, ASMEM, Q8>);
 }
-template <int NTOK, bool ASMEM>
+template <int NTOK, bool ASMEM, bool Q8 = false>
 int gemm_smem_bytes() {
-    return dev::GemmCfg<NTOK, kStages, ASMEM>::kSmemBytes;
+    return dev::GemmCfg<NTOK, kStages, ASMEM, Q8>::kSmemBytes;
 }
 
 int cuda_fail(cudaError_t e, const char *what, std::string *err) {
@@ -115,21 +116,25 @@ int resident_ctas(const void *kernel, int threads, int smem_bytes, int device, s
     return W12_OK;
 }
 
-template <int NTOK, bool ASMEM>
+template <int NTOK, bool ASMEM, bool Q8 = false>
 int prepare_gemm(DeviceState &s, std::string *err) {
-    void *k = gemm_kernel_ptr<NTOK, ASMEM>();
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm_smem_bytes<NTOK, ASMEM>());
+    void *k = gemm_kernel_ptr<NTOK, ASMEM, Q8>();
+    cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, gemm_smem_bytes<NTOK, ASMEM, Q8>());
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute", err);
     // all of the unified L1/shared storage as shared memory, so that several
     // CTAs fit on an SM
     e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(carveout)", err);
     int occ = 0;
-    const int rc = resident_ctas(k, dev::GemmCfg<NTOK, kStages, ASMEM>::kThreads, gemm_smem_bytes<NTOK, ASMEM>(),
-                                 s.device, err, &occ);
+    const int rc = resident_ctas(k, dev::GemmCfg<NTOK, kStages, ASMEM, Q8>::kThreads,
+                                 gemm_smem_bytes<NTOK, ASMEM, Q8>(), s.device, err, &occ);
     if (rc != W12_OK) return rc;
     // TMEM: each CTA holds 128 of the SM's 512 columns
-    s.occupancy[NTOK == 32][ASMEM] = occ < 4 ? occ : 4;
+    if (Q8)
+        s.q8_occupancy[NTOK == 32] = occ < 4 ? occ : 4;
+    else
+        s.occupancy[NTOK == 32][ASMEM] = occ < 4 ? occ : 4;
     return W12_OK;
 }
 
@@ -180,6 +185,8 @@ int device_state(DeviceState **out, std::string *err) {
         if (rc == W12_OK) rc = prepare_gemm<32, false>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<16, true>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<32, true>(s, err);
+        if (rc == W12_OK) rc = prepare_gemm<16, false, true>(s, err);
+        if (rc == W12_OK) rc = prepare_gemm<32, false, true>(s, err);
         if (rc != W12_OK) return rc;
         s.ready = true;
     }
@@ -225,7 +232,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder(std::string *err) {
 
 }  // namespace
 
-int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err) {
+int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, bool q8) {
     if (M < 1 || M > 32) {
         *err = "M must be in 1..32";
         return W12_ERR_INVALID_ARG;
@@ -233,9 +240,11 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err) {
     DeviceState *s = nullptr;
     int rc = device_state(&s, err);
     if (rc != W12_OK) return rc;
-    plan->gemv = use_gemv(M);
+    plan->gemv = !q8 && use_gemv(M);
     plan->ntok = M <= 16 ? 16 : 32;
-    const int occ = plan->gemv ? s->gemv_occupancy : s->occupancy[plan->ntok == 32][use_smem_a_operand()];
+    const int occ = plan->gemv ? s->gemv_occupancy
+                    : q8       ? s->q8_occupancy[plan->ntok == 32]
+                               : s->occupancy[plan->ntok == 32][use_smem_a_operand()];
     if (occ < 1) {
         *err = "GEMM kernel cannot be resident on this device";
         return W12_ERR_CUDA;
@@ -312,20 +321,48 @@ cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-template <int NTOK, bool ASMEM>
+template <int NTOK, bool ASMEM, bool Q8 = false>
 cudaError_t launch_gemm_kernel(const dev::GemmParams &p, const CUtensorMap &tm, int splits, int64_t tiles,
                                cudaStream_t st) {
     dim3 grid((unsigned)splits, (unsigned)tiles);
-    return launch_overlapped(dev::w12_gemm_tc_kernel<NTOK, kStages, ASMEM>, grid,
-                             dim3(dev::GemmCfg<NTOK, kStages, ASMEM>::kThreads),
-                             (size_t)gemm_smem_bytes<NTOK, ASMEM>(), st, p, tm);
+    return launch_overlapped(dev::w12_gemm_tc_kernel<NTOK, kStages, ASMEM, Q8>, grid,
+                             dim3(dev::GemmCfg<NTOK, kStages, ASMEM, Q8>::kThreads),
+                             (size_t)gemm_smem_bytes<NTOK, ASMEM, Q8>(), st, p, tm);
 }
 }  // namespace
 
 namespace {
 int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev,
-              unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err);
+              unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err,
+              const w12_q8_info *q8 = nullptr);
+
+// The planner and launcher work on a w12_info; a Q8 copy has the same grid.
+w12_info q8_as_info(const w12_q8_info &q) {
+    w12_info i{};
+    i.N = q.N;
+    i.K = q.K;
+    i.N_pad = q.N_pad;
+    i.K_pad = q.K_pad;
+    i.tiles = q.tiles;
+    i.chunks = q.chunks;
+    i.segs = q.segs;
+    i.off_weights = q.off_q;
+    i.total_bytes = q.total_bytes;
+    return i;
+}
 }  // namespace
+
+int q8_workspace_size(const w12_q8_info &info, int M, size_t *bytes, std::string *err) {
+    GemmPlan plan;
+    const int rc = plan_gemm(q8_as_info(info), M, &plan, err, true);
+    if (rc == W12_OK) *bytes = plan.ws_bytes;
+    return rc;
+}
+
+int q8_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_q8_info &info, uint16_t *y_dev, int M,
+            void *workspace, size_t ws_bytes, void *stream, std::string *err) {
+    return gemm_impl(x_dev, blob_dev, q8_as_info(info), y_dev, nullptr, M, workspace, ws_bytes, stream, err, &info);
+}
 
 int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,
          void *workspace, size_t ws_bytes, void *stream, std::string *err) {
@@ -364,9 +401,10 @@ int gemm_argmax(const uint16_t *x_dev, const void *blob_dev, const w12_info &inf
 
 namespace {
 int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev,
-              unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err) {
+              unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err,
+              const w12_q8_info *q8) {
     GemmPlan plan;
-    int rc = plan_gemm(info, M, &plan, err);
+    int rc = plan_gemm(info, M, &plan, err, q8 != nullptr);
     if (rc != W12_OK) return rc;
     if (ws_bytes < plan.ws_bytes) {
         *err = "workspace smaller than w12_gemm_workspace_size";
@@ -424,6 +462,7 @@ int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info,
     p.counters = reinterpret_cast<uint32_t *>(ws + plan.ws_counters);
     p.y = y_dev;
     p.amax = amax;
+    p.scales = q8 ? reinterpret_cast<const float *>(p.blob + q8->off_scales) : nullptr;
     p.status = s->status;
     p.timeout_ns = timeout_ns();
 
@@ -433,6 +472,9 @@ int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info,
         dim3 grid((unsigned)plan.splits, (unsigned)info.tiles);
         e = launch_overlapped(dev::w12_gemv_kernel<kGemvStages, kGemvChunks>, grid, dim3(GemvC::kThreads),
                               (size_t)GemvC::kSmemBytes, st, p, tm);
+    } else if (q8) {
+        e = plan.ntok == 16 ? launch_gemm_kernel<16, false, true>(p, tm, plan.splits, info.tiles, st)
+                            : launch_gemm_kernel<32, false, true>(p, tm, plan.splits, info.tiles, st);
     } else if (plan.ntok == 16)
         e = asmem ? launch_gemm_kernel<16, true>(p, tm, plan.splits, info.tiles, st)
                   : launch_gemm_kernel<16, false>(p, tm, plan.splits, info.tiles, st);

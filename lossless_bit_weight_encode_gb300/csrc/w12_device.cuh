@@ -485,6 +485,26 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
         : "memory");
 }
 
+// ---------------------------------------------------------------- Q8 copy
+// 16 int8 weights (two's complement; one chunk half of a row) to 8 BF16 pairs,
+// lower column in the low half, exactly: byte b ^ 0x80 = b + 128 goes into
+// the low mantissa bits of 2^23 (0x4B000000), and subtracting 2^23 + 128 in
+// fp32 leaves b; |b| <= 128 keeps the value exact in BF16, so its top 16 bits
+// are the BF16 pattern.
+__device__ __forceinline__ void q8_half(const uint4 &v, uint32_t (&out)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t u = w[j] ^ 0x80808080u;
+        const float f0 = __uint_as_float(prmt(u, 0x4B000000u, 0x7440u)) - 8388736.0f;
+        const float f1 = __uint_as_float(prmt(u, 0x4B000000u, 0x7441u)) - 8388736.0f;
+        const float f2 = __uint_as_float(prmt(u, 0x4B000000u, 0x7442u)) - 8388736.0f;
+        const float f3 = __uint_as_float(prmt(u, 0x4B000000u, 0x7443u)) - 8388736.0f;
+        out[2 * j] = prmt(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
+        out[2 * j + 1] = prmt(__float_as_uint(f2), __float_as_uint(f3), 0x7632u);
+    }
+}
+
 // ---------------------------------------------------------------- argmax
 // LM-head argmax ("certified exact-argmax LM head": "SpecPilot: an agent
 // doubled speculative decoding speed, and the 10.87x needs context", §The

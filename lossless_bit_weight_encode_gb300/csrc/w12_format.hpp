@@ -79,4 +79,40 @@ struct Geometry {
     }
 };
 
+// Q8 v1: the 8-bit weight copy (symmetric INT8 per row, fp32 scale per row;
+// format in include/w12.h).  Same tile/chunk/segment grid as W12; a chunk is
+// two slabs of 128 rows x 16 int8 (columns 0-15, 16-31).
+namespace q8 {
+constexpr int kChunkBytes = 2 * kSlabBytes;      // 4096
+constexpr uint32_t kMagic = 0x31573851u;         // "Q8W1" little-endian
+constexpr uint32_t kVersion = 1;
+namespace hdr {
+constexpr int kMagicOff = 0x00, kVersionOff = 0x04, kHeaderBytesOff = 0x08, kFlagsOff = 0x0C;
+constexpr int kN = 0x10, kK = 0x18, kNpad = 0x20, kKpad = 0x28, kTiles = 0x30, kChunks = 0x38;
+constexpr int kOffS = 0x40, kBytesS = 0x48, kOffQ = 0x50, kBytesQ = 0x58, kTotal = 0x60;
+}  // namespace hdr
+
+struct Geometry {
+    int64_t N = 0, K = 0, Npad = 0, Kpad = 0, tiles = 0, chunks = 0, segs = 0;
+    uint64_t off_s = 0, bytes_s = 0, off_q = 0, bytes_q = 0, total = 0;
+
+    static inline Geometry of(int64_t n, int64_t k) {
+        Geometry g;
+        g.N = n;
+        g.K = k;
+        g.Npad = (int64_t)w12::Geometry::round_up((uint64_t)n, kTileRows);
+        g.Kpad = (int64_t)w12::Geometry::round_up((uint64_t)k, kChunkK);
+        g.tiles = g.Npad / kTileRows;
+        g.chunks = g.Kpad / kChunkK;
+        g.segs = (g.chunks + kChunksPerSeg - 1) / kChunksPerSeg;
+        g.off_s = kHeaderBytes;
+        g.bytes_s = 4ull * (uint64_t)g.Npad;
+        g.off_q = w12::Geometry::round_up(g.off_s + g.bytes_s, kPlaneAlign);
+        g.bytes_q = (uint64_t)kChunkBytes * (uint64_t)(g.tiles * g.chunks);
+        g.total = w12::Geometry::round_up(g.off_q + g.bytes_q, kPlaneAlign);
+        return g;
+    }
+};
+}  // namespace q8
+
 }  // namespace w12

@@ -17,5 +17,9 @@ int encode(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, uint64_t cap,
 int parse_header(const uint8_t *blob, uint64_t bytes, w12_info *out, std::string *err);
 int validate(const uint8_t *blob, uint64_t bytes, std::string *err);
 
+int q8_encoded_size(int64_t N, int64_t K, uint64_t *bytes, std::string *err);
+int q8_encode(const uint16_t *w, int64_t N, int64_t K, uint8_t *blob, uint64_t cap, std::string *err);
+int q8_parse_header(const uint8_t *blob, uint64_t bytes, w12_q8_info *out, std::string *err);
+
 }  // namespace host
 }  // namespace w12

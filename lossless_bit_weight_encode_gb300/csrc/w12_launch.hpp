@@ -21,7 +21,12 @@ struct GemmPlan {
     size_t ws_bytes = 0;
 };
 
-int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err);
+int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, bool q8 = false);
+
+int q8_workspace_size(const w12_q8_info &info, int M, size_t *bytes, std::string *err);
+
+int q8_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_q8_info &info, uint16_t *y_dev, int M,
+            void *workspace, size_t ws_bytes, void *stream, std::string *err);
 
 int decode(const void *blob_dev, const w12_info &info, uint16_t *out_dev, void *stream, std::string *err);
 

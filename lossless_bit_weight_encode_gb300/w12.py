@@ -26,6 +26,7 @@ EXPORTED = (
     "w12_last_error", "w12_status_string", "w12_format_version", "w12_encoded_size_host", "w12_encode_host",
     "w12_blob_info", "w12_blob_validate", "w12_decode", "w12_gemm_workspace_size", "w12_gemm_launch_info",
     "w12_gemm", "w12_gemm_argmax_workspace_size", "w12_gemm_argmax", "w12_gemm_noalloc", "w12_encode_workspace_size", "w12_encoded_size_device", "w12_encode_device",
+    "w12_q8_encoded_size", "w12_q8_encode_host", "w12_q8_blob_info", "w12_q8_gemm_workspace_size", "w12_q8_gemm",
     "w12_check_status", "w12_selftest_timeout",
 )
 
@@ -45,6 +46,18 @@ class w12_info(ctypes.Structure):
         ("off_escapes", ctypes.c_uint64), ("bytes_escapes", ctypes.c_uint64),
         ("n_escapes", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64),
         ("bits_per_weight", ctypes.c_double),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class w12_q8_info(ctypes.Structure):
+    _fields_ = [
+        ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("N_pad", ctypes.c_int64), ("K_pad", ctypes.c_int64),
+        ("tiles", ctypes.c_int64), ("chunks", ctypes.c_int64), ("segs", ctypes.c_int64),
+        ("off_scales", ctypes.c_uint64), ("bytes_scales", ctypes.c_uint64),
+        ("off_q", ctypes.c_uint64), ("bytes_q", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64),
     ]
 
     def as_dict(self) -> dict:
@@ -83,6 +96,11 @@ def lib() -> ctypes.CDLL:
     L.w12_encode_workspace_size.argtypes = [i64, i64, ctypes.POINTER(sz)]
     L.w12_encoded_size_device.argtypes = [vp, i64, i64, vp, sz, ctypes.POINTER(sz), vp]
     L.w12_encode_device.argtypes = [vp, i64, i64, vp, sz, vp, sz, vp]
+    L.w12_q8_encoded_size.argtypes = [i64, i64, ctypes.POINTER(sz)]
+    L.w12_q8_encode_host.argtypes = [vp, i64, i64, vp, sz]
+    L.w12_q8_blob_info.argtypes = [vp, sz, ctypes.POINTER(w12_q8_info)]
+    L.w12_q8_gemm_workspace_size.argtypes = [ctypes.POINTER(w12_q8_info), i32, ctypes.POINTER(sz)]
+    L.w12_q8_gemm.argtypes = [vp, vp, ctypes.POINTER(w12_q8_info), vp, i32, vp, sz, vp]
     L.w12_check_status.argtypes = [vp]
     L.w12_selftest_timeout.argtypes = [ctypes.c_uint32, vp]
     for name in EXPORTED[3:]:
@@ -238,6 +256,43 @@ def w12_encode_device(w_dev, blob_dev, workspace, stream=None, nbytes: int | Non
     cap = blob_dev.numel() if nbytes is None else int(nbytes)
     _check(lib().w12_encode_device(w_dev.data_ptr(), N, K, blob_dev.data_ptr(), cap, workspace.data_ptr(),
                                    workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+
+
+# ---------------------------------------------------------------- Q8 copy
+def w12_q8_encode_host(w: np.ndarray) -> np.ndarray:
+    """Q8 v1 blob (symmetric INT8 per row) of the N x K BF16 bit patterns."""
+    w = _host_u16(w)
+    size = ctypes.c_size_t()
+    _check(lib().w12_q8_encoded_size(w.shape[0], w.shape[1], ctypes.byref(size)))
+    blob = np.empty(size.value, dtype=np.uint8)
+    _check(lib().w12_q8_encode_host(w.ctypes.data, w.shape[0], w.shape[1], blob.ctypes.data, size.value))
+    return blob
+
+
+def w12_q8_blob_info(blob: np.ndarray, blob_bytes: int | None = None) -> w12_q8_info:
+    blob = np.ascontiguousarray(blob, dtype=np.uint8)
+    info = w12_q8_info()
+    _check(lib().w12_q8_blob_info(blob.ctypes.data, blob.size if blob_bytes is None else int(blob_bytes),
+                                  ctypes.byref(info)))
+    return info
+
+
+def w12_q8_gemm_workspace_size(info: w12_q8_info, M: int) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().w12_q8_gemm_workspace_size(ctypes.byref(info), int(M), ctypes.byref(out)))
+    return out.value
+
+
+def w12_q8_gemm(x_dev, blob_dev, info: w12_q8_info, y_dev, M: int, workspace, stream=None) -> None:
+    _check(lib().w12_q8_gemm(x_dev.data_ptr(), blob_dev.data_ptr(), ctypes.byref(info), y_dev.data_ptr(), int(M),
+                             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                             _stream_handle(stream)))
+
+
+def w12_q8_gemm_ptr(x_ptr: int, blob_ptr: int, info: w12_q8_info, y_ptr: int, M: int, ws_ptr: int, ws_bytes: int,
+                    stream_handle: int | None) -> int:
+    """Raw-pointer form of w12_q8_gemm that returns the status."""
+    return lib().w12_q8_gemm(x_ptr, blob_ptr, ctypes.byref(info), y_ptr, int(M), ws_ptr, ws_bytes, stream_handle)
 
 
 def w12_check_status(stream=None) -> None:

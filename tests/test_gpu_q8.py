@@ -1,0 +1,75 @@
+"""Q8 copy GEMM (w12_q8_gemm) on the tensor-core kernel against the oracle's
+fp64 product over its own Q8 copy (same quantizer, same fp32 decisions):
+tolerance on every output, bit-exact where the arithmetic is exact (one-hot
+x), and full layer shapes on sampled rows."""
+import numpy as np
+import pytest
+
+import oracle
+from lossless_bit_weight_encode_gb300 import Q8Weight, w12
+from lossless_bit_weight_encode_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from gpu_util import ensure_built
+    ensure_built()
+
+
+def _gemm(mat, x_bits):
+    import torch
+    from gpu_util import dev_to_bits, to_dev_bf16
+    y = mat.gemm(to_dev_bf16(x_bits))
+    w12.w12_check_status()
+    torch.cuda.synchronize()
+    return dev_to_bits(y)
+
+
+def test_q8_single_output_within_one_ulp():
+    """A 1 x 1 product has one output: the relative Frobenius bound (written
+    for many outputs) does not apply, the BF16 rounding does: at most one unit
+    in the last place from the fp64 value."""
+    for seed in range(20):
+        w = wl.heavy_tail_weights(1, 1 + seed, seed=80 + seed)
+        x = wl.activations(1, 1 + seed, seed=90 + seed)
+        y = wl.bf16_bits_to_f32(_gemm(Q8Weight(w), x))[0, 0]
+        ref = oracle.q8_gemm_f64(x, w)[0, 0]
+        ulp = 2.0 ** (np.floor(np.log2(abs(ref))) - 7) if ref != 0 else 0.0
+        assert abs(float(y) - ref) <= ulp, (seed, float(y), ref)
+
+
+@pytest.mark.parametrize("shape", [(129, 33), (384, 2048), (300, 1001), (130, 7000)])
+@pytest.mark.parametrize("M", [1, 2, 5, 16, 17, 32])
+def test_q8_gemm_matches_oracle(shape, M):
+    from gpu_util import check_tolerance
+    n, k = shape
+    w = wl.heavy_tail_weights(n, k, seed=70 + n + k)
+    x = wl.activations(M, k, seed=71 + M)
+    check_tolerance(_gemm(Q8Weight(w), x), oracle.q8_gemm_f64(x, w), f"q8 {shape} M={M}")
+
+
+def test_q8_one_hot_is_exact():
+    """x = e_k: the sum is q[n][k] exactly; y = BF16(fp32(s[n] * q[n][k]))."""
+    w = wl.gaussian_weights(256, 512, seed=72)
+    s, q = oracle.q8_decode(oracle.q8_encode(w), 256, 512)
+    mat = Q8Weight(w)
+    for kk in (0, 200, 511):
+        x = np.zeros((3, 512), dtype=np.uint16)
+        x[:, kk] = 0x3F80
+        y = _gemm(mat, x)
+        ref = wl.to_bf16_bits((s * q[:, kk].astype(np.float32)).astype(np.float32))
+        assert np.array_equal(y[0], ref) and np.array_equal(y[2], ref), f"column {kk}"
+
+
+def test_q8_layer_shapes_sampled_rows():
+    from gpu_util import check_tolerance
+    rng = np.random.default_rng(73)
+    for name, w in wl.layer_weights("layer"):
+        mat = Q8Weight(w)
+        rows = np.sort(rng.choice(w.shape[0], size=256, replace=False))
+        for M in (1, 16, 32):
+            x = wl.activations(M, w.shape[1], seed=wl.activation_seed("layer", M))
+            ref = oracle.q8_gemm_f64(x, np.ascontiguousarray(w[rows]))
+            check_tolerance(_gemm(mat, x)[:, rows], ref, f"q8 {name} M={M}")

@@ -124,3 +124,41 @@ def test_host_argument_errors():
     buf = np.empty(size, dtype=np.uint8)
     assert lib.w12_encode_host(w.ctypes.data, 4, 4, buf.ctypes.data, size - 1) == 3
     assert lib.w12_encode_host(w.ctypes.data, 4, 4, buf.ctypes.data, size) == 0
+
+
+Q8_CASES = {
+    "gauss": lambda: wl.gaussian_weights(300, 1000, seed=20),
+    "heavy": lambda: wl.heavy_tail_weights(129, 4099, seed=21),
+    "tiny": lambda: wl.gaussian_weights(1, 1, seed=22),
+    "zero_rows": lambda: np.where(np.arange(200)[:, None] % 3 == 0, np.uint16(0),
+                                  wl.gaussian_weights(200, 70, seed=23)).astype(np.uint16),
+    "ties": lambda: wl.to_bf16_bits(np.tile(np.array([127, 32.5, 33.5, -0.5, 1.5], np.float32) / 64, (3, 7))),
+}
+
+
+@pytest.mark.parametrize("case", sorted(Q8_CASES))
+def test_q8_encoder_is_byte_equal_to_oracle(case):
+    w = Q8_CASES[case]()
+    ref = oracle.q8_encode(w)
+    blob = w12.w12_q8_encode_host(w)
+    assert np.array_equal(blob, ref), f"first difference at byte {int(np.argmax(blob != ref))}"
+    info = w12.w12_q8_blob_info(blob)
+    assert (info.N, info.K, info.total_bytes) == (w.shape[0], w.shape[1], ref.size)
+    assert w12.w12_q8_blob_info(blob[:256], blob.size).as_dict() == info.as_dict()
+
+
+def test_q8_rejects_bad_input():
+    w = wl.gaussian_weights(10, 10, seed=24)
+    w[4, 4] = np.uint16(0x7FC0)  # NaN
+    with pytest.raises(w12.W12Error) as ei:
+        w12.w12_q8_encode_host(w)
+    assert ei.value.status == 1
+    blob = w12.w12_q8_encode_host(wl.gaussian_weights(10, 10, seed=25))
+    bad = blob.copy()
+    bad[0x11] ^= 1  # N grows by 256: the padded geometry no longer matches
+    with pytest.raises(w12.W12Error) as ei:
+        w12.w12_q8_blob_info(bad)
+    assert ei.value.status == 5
+    with pytest.raises(w12.W12Error) as ei:
+        w12.w12_q8_blob_info(oracle.encode(wl.gaussian_weights(10, 10, seed=26)))  # a W12 blob
+    assert ei.value.status == 5
