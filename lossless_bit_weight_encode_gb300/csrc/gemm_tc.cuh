@@ -611,10 +611,8 @@ __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint3
     if (lane == 0) mbar_arrive(b.epi_in);
     if (threadIdx.x == 0) {
         if (mbar_wait(b.epi_in, 0, deadline)) {
-            __threadfence();
-            const uint32_t old = atomicAdd(p.counters + tile, 1u);
+            const uint32_t old = arrive_acq_rel(p.counters + tile);
             const bool last = old == (uint32_t)(p.splits - 1);
-            if (last) __threadfence();  // the other CTAs' partials are visible past here
             *last_flag = last ? 1u : 0u;
             mbar_arrive(b.epi_out);
         } else {

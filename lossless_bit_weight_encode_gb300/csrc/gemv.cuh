@@ -277,15 +277,13 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
     }
     __stcg(p.partials + (int64_t)split * p.Npad + n, total);
     // the mbarrier arrive/wait pair orders these stores before thread 0's
-    // fence, which publishes them all with the counter increment
+    // release increment of the tile counter, which publishes them all
     __syncwarp();
     if (lane == 0) mbar_arrive(b.epi_in);
     if (threadIdx.x == 0) {
         if (mbar_wait(b.epi_in, 0, deadline)) {
-            __threadfence();
-            const uint32_t old = atomicAdd(p.counters + tile, 1u);
+            const uint32_t old = arrive_acq_rel(p.counters + tile);
             const bool last = old == (uint32_t)(p.splits - 1);
-            if (last) __threadfence();  // the other CTAs' partials are visible past here
             *last_flag = last ? 1u : 0u;
             mbar_arrive(b.epi_out);
         } else {

@@ -485,6 +485,18 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
         : "memory");
 }
 
+// Split-K arrival: add 1 to a tile's counter at GPU scope with acquire-release
+// semantics and return the old value.  The release half publishes this
+// thread's earlier stores and, cumulatively, those it has synchronised with
+// (the CTA's partials, ordered before it by an mbarrier or __syncwarp); the
+// acquire half lets the last arrival read every other CTA's partials.  One
+// ordered atomic instead of a full fence on each side.
+__device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t *counter) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+    return old;
+}
+
 // ---------------------------------------------------------------- Q8 copy
 // 16 int8 weights (two's complement; one chunk half of a row) to 8 BF16 pairs,
 // lower column in the low half, exactly: byte b ^ 0x80 = b + 128 goes into
