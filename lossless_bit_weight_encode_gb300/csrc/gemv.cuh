@@ -6,18 +6,19 @@
 //
 // With one token the product is 2 flops per weight, far below what needs the
 // tensor cores; what bounds this path is streaming the packed bytes and the
-// integer decode.  So the decoded BF16 pairs go straight into fp32 fused
-// multiply-adds (fma.rn.f32x2: two weights per instruction) with no TMEM
-// store and no handshake with an MMA warp.
+// integer decode.  So the decoded BF16 weights go straight into mixed
+// precision fused multiply-adds (fma.rn.f32.bf16: BF16 weight times BF16 x
+// into an fp32 sum, one per weight, on the FMA pipe) with no widening of
+// either operand, no TMEM store and no handshake with an MMA warp.
 //
 // Warp roles (288 threads):
 //   warps 0-7  decode: warp w handles rows 32q..32q+31 (q = w mod 4) and
 //              columns 16h..16h+15 of every chunk (h = w / 4); per weight
-//              stage (2 chunks) a thread reads its row's S bytes and codes from
-//              SMEM, decodes 2 x 16 weights, patches escapes and accumulates
-//              them against x (fp32 in SMEM, converted once per segment);
+//              stage (4 chunks) a thread reads its row's S bytes and codes from
+//              SMEM, decodes 4 x 16 weights, patches escapes and accumulates
+//              them against x (BF16 in SMEM, as the tensor TMA wrote it);
 //   warp 8     producer: cp.async.bulk for the segment headers and every
-//              weight stage (12 KB); per segment cp.async.bulk.tensor for the
+//              weight stage (24 KB); per segment cp.async.bulk.tensor for the
 //              256 x values and cp.async.bulk for the escape bytes.
 // The two column halves of a row are added in fixed order at the end, then
 // the split-K partials as in the tensor-core kernel.  Every wait is bounded.
@@ -37,19 +38,17 @@ struct GemvCfg {
     static constexpr int kStagesPerSeg = kChunksPerSeg / SCHUNKS;
     static constexpr int kWBytes = SCHUNKS * kChunkBytes;
     static constexpr int kXbBytes = kSegK * 2;        // one segment of x, BF16 (TMA destination)
-    static constexpr int kXfBytes = kSegK * 4;        // the same as fp32
     static constexpr int kSegSlots = 2;
     static constexpr int kEscCap = 2048;
     static constexpr int kMaxSegs = 96;
     static constexpr int kOffW = 0;
     static constexpr int kOffXb = kOffW + STAGES * kWBytes;  // 128-byte aligned
-    static constexpr int kOffXf = kOffXb + kSegSlots * kXbBytes;
-    static constexpr int kOffEsc = kOffXf + kSegSlots * kXfBytes;
+    static constexpr int kOffEsc = kOffXb + kSegSlots * kXbBytes;
     static constexpr int kOffHdr = kOffEsc + kSegSlots * kEscCap;
     static constexpr int kOffRed = kOffHdr + kMaxSegs * kSegHdrBytes;  // 128 fp32
     static constexpr int kOffBars = kOffRed + kTileRows * 4;
-    // wfull[S], wempty[S], sfull[2], sempty[2], xconv[2], hdr, red, epi_in, epi_out
-    static constexpr int kNumBars = 2 * STAGES + 3 * kSegSlots + 4;
+    // wfull[S], wempty[S], sfull[2], sempty[2], hdr, red, epi_in, epi_out
+    static constexpr int kNumBars = 2 * STAGES + 2 * kSegSlots + 4;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 64 + 128;  // + slack to align the base to 128
     static_assert(kOffXb % 128 == 0, "TMA destination alignment");
@@ -57,37 +56,32 @@ struct GemvCfg {
 };
 
 struct GemvBars {
-    uint64_t *wfull, *wempty, *sfull, *sempty, *xconv, *hdr, *red, *epi_in, *epi_out;
+    uint64_t *wfull, *wempty, *sfull, *sempty, *hdr, *red, *epi_in, *epi_out;
 };
 
-// two fp32 values as one 64-bit operand of the packed instructions
-__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
-    uint64_t v;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(lo), "r"(hi));
-    return v;
-}
-
-__device__ __forceinline__ void fma2(uint64_t &acc, uint64_t a, uint64_t b) {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
-}
-
-// acc += w . x over 16 columns: w as 8 BF16 pairs (even column low), x as
-// 16 fp32 at shared address xs.  Exact widening: BF16 -> fp32 is a shift.
-__device__ __forceinline__ void dot16(const uint32_t (&w)[8], uint32_t xs, uint64_t &acc0, uint64_t &acc1) {
+// acc[j] += w * x over 16 columns with x as BF16 (16 values at shared
+// address xs), one fma.rn.f32.bf16 per weight: the product of two BF16 values
+// is exact in fp32, so this is the same single rounding as fma.rn.f32 on the
+// widened operands.  acc[j] collects the columns congruent to j mod 4.
+__device__ __forceinline__ void dot16_bf(const uint32_t (&w)[8], uint32_t xs, float (&acc)[4]) {
+    const uint4 x0 = lds128(xs), x1 = lds128(xs + 16u);
+    const uint32_t X[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-        const uint4 xv = lds128(xs + 16u * (uint32_t)g);
-        const uint32_t w0 = w[2 * g], w1 = w[2 * g + 1];
-        fma2(acc0, pack2(w0 << 16, w0 & 0xFFFF0000u), pack2(xv.x, xv.y));
-        fma2(acc1, pack2(w1 << 16, w1 & 0xFFFF0000u), pack2(xv.z, xv.w));
+        asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+            "mov.b32 {wl, wh}, %4;\n\t"
+            "mov.b32 {xl, xh}, %5;\n\t"
+            "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+            "fma.rn.f32.bf16 %1, wh, xh, %1;\n\t"
+            "mov.b32 {wl, wh}, %6;\n\t"
+            "mov.b32 {xl, xh}, %7;\n\t"
+            "fma.rn.f32.bf16 %2, wl, xl, %2;\n\t"
+            "fma.rn.f32.bf16 %3, wh, xh, %3;\n\t}"
+            : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
+            : "r"(w[2 * g]), "r"(X[2 * g]), "r"(w[2 * g + 1]), "r"(X[2 * g + 1]));
     }
 }
 
-__device__ __forceinline__ float unpack_sum(uint64_t a, uint64_t b) {
-    const float a0 = __uint_as_float((uint32_t)a), a1 = __uint_as_float((uint32_t)(a >> 32));
-    const float b0 = __uint_as_float((uint32_t)b), b1 = __uint_as_float((uint32_t)(b >> 32));
-    return (a0 + a1) + (b0 + b1);
-}
 
 // ------------------------------------------------------------------ producer
 template <class C>
@@ -172,15 +166,14 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
     const int h = warp >> 2;      // columns 16h..16h+15 of each chunk
     const int lane = threadIdx.x & 31;
     const int r = 32 * q + lane;  // row in the tile
-    const int t = threadIdx.x;    // 0..255: the x element this thread widens per segment
     const int nchunks = c1 - c0;
     const int nstages = (nchunks + C::kStageChunks - 1) / C::kStageChunks;
     const uint8_t *hdr = smem + C::kOffHdr;
     const uint32_t s_row = smem_u32(smem + C::kOffW) + (uint32_t)(h * kSlabBytes + 16 * r);
     const uint32_t c_off = (uint32_t)((2 - h) * kSlabBytes);
-    const uint32_t xf0 = smem_u32(smem + C::kOffXf) + (uint32_t)(16 * h) * 4u;
+    const uint32_t xb0 = smem_u32(smem + C::kOffXb) + (uint32_t)(16 * h) * 2u;
 
-    uint64_t acc0 = 0, acc1 = 0;  // two fp32 pairs each, +0.0
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     bool ok = warp_wait(b.hdr, 0, deadline);
     Table T{};
     uint32_t mask_q = 0, xseg = 0;
@@ -203,13 +196,7 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
                 run = smem + C::kOffEsc + sslot * C::kEscCap + (meta.x & 15u) + qoff;
             else
                 run = p.blob + p.off_esc + meta.x + qoff;
-            // widen this segment's 256 x values to fp32, one per thread
-            const uint16_t xb = reinterpret_cast<const uint16_t *>(smem + C::kOffXb + sslot * C::kXbBytes)[t];
-            reinterpret_cast<float *>(smem + C::kOffXf + sslot * C::kXfBytes)[t] = __uint_as_float((uint32_t)xb << 16);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b.xconv + sslot);
-            if (!(ok = warp_wait(b.xconv + sslot, (uint32_t)(ls >> 1) & 1u, deadline))) break;
-            xseg = xf0 + (uint32_t)(sslot * C::kXfBytes);
+            xseg = xb0 + (uint32_t)(sslot * C::kXbBytes);
         }
         const int slot = st % C::kStages;
         if (!(ok = warp_wait(b.wfull + slot, (uint32_t)(st / C::kStages) & 1u, deadline))) break;
@@ -234,7 +221,7 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
                 uint32_t E[4], out[8];
                 decode_exponents_half(T, h ? cd[e].z : cd[e].x, h ? cd[e].w : cd[e].y, E);
                 assemble_half(sb[e], E, out);
-                dot16(out, xseg + (uint32_t)((jj0 + e) * kChunkK * 4), acc0, acc1);
+                dot16_bf(out, xseg + (uint32_t)((jj0 + e) * kChunkK * 2), acc);
             }
         } else {
 #pragma unroll
@@ -242,7 +229,7 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
                 if (e < nch) {
                     uint32_t out[8];
                     decode_half_chunk(T, sb[e], cd[e], h, (stage_esc >> e) & 1u, run, out);
-                    dot16(out, xseg + (uint32_t)((jj0 + e) * kChunkK * 4), acc0, acc1);
+                    dot16_bf(out, xseg + (uint32_t)((jj0 + e) * kChunkK * 2), acc);
                 }
             }
         }
@@ -256,7 +243,7 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
     }
 
     // ---- epilogue: add the two column halves of each row in fixed order
-    const float mine = unpack_sum(acc0, acc1);
+    const float mine = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     float *red = reinterpret_cast<float *>(smem + C::kOffRed);
     if (h == 1) {
         red[r] = mine;
@@ -327,8 +314,7 @@ __global__ void __launch_bounds__(288, 2)
     b.wempty = b.wfull + STAGES;
     b.sfull = b.wempty + STAGES;
     b.sempty = b.sfull + C::kSegSlots;
-    b.xconv = b.sempty + C::kSegSlots;
-    b.hdr = b.xconv + C::kSegSlots;
+    b.hdr = b.sempty + C::kSegSlots;
     b.red = b.hdr + 1;
     b.epi_in = b.red + 1;
     b.epi_out = b.epi_in + 1;
@@ -353,7 +339,6 @@ __global__ void __launch_bounds__(288, 2)
         for (int i = 0; i < C::kSegSlots; ++i) {
             mbar_init(b.sfull + i, 1);
             mbar_init(b.sempty + i, C::kDecWarps);
-            mbar_init(b.xconv + i, C::kDecWarps);
         }
         mbar_init(b.hdr, 1);
         mbar_init(b.red, 4);
