@@ -409,8 +409,7 @@ def run_w12(args):
     launch_ms = [statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(kp)) for i in range(nl)]
 
     kernel_name = "w12_gemm_tc_kernel (Q8 copy)" if args.weights == "q8" else \
-        "w12_gemv_kernel" if w12.w12_gemm_launch_info(mats[0].info, M).get("ntok") and M == 1 \
-        and os.environ.get("W12_M1_PATH", "") != "tc" else "w12_gemm_tc_kernel"
+        "w12_gemv_kernel" if w12.w12_gemm_launch_info(mats[0].info, M).get("ntok") <= 4 else "w12_gemm_tc_kernel"
     layer_weights = sum(m.N * m.K for m in mats)
     packed = sum(int(m.info.total_bytes) for m in mats)
     alg = [int(m.info.total_bytes) + 2 * M * m.K + 2 * M * m.N for m in mats]

@@ -1,12 +1,12 @@
-// W12 GEMV on CUDA cores (one token, M = 1): y = x . W^T with W streamed from
+// W12 GEMV on CUDA cores (one or two tokens, M <= MT): y = x . W^T with W streamed from
 // HBM in W12 form and decoded in registers ("decoded inside the GEMM
 // registers", "SpecPilot: an agent doubled speculative decoding speed, and
 // the 10.87x needs context", §The mechanisms it found; bit-exact weights,
 // "StargazerX0/SpecPilot", §What it is).
 //
-// With one token the product is 2 flops per weight, far below what needs the
-// tensor cores; what bounds this path is streaming the packed bytes and the
-// integer decode.  So the decoded BF16 weights go straight into mixed
+// With one or two tokens the product is 2 or 4 flops per weight, far below
+// what needs the tensor cores; what bounds this path is streaming the packed
+// bytes and the integer decode.  So the decoded BF16 weights go straight into mixed
 // precision fused multiply-adds (fma.rn.f32.bf16: BF16 weight times BF16 x
 // into an fp32 sum, one per weight, on the FMA pipe) with no widening of
 // either operand, no TMEM store and no handshake with an MMA warp.
@@ -29,15 +29,16 @@
 namespace w12 {
 namespace dev {
 
-template <int STAGES, int SCHUNKS>
+template <int STAGES, int SCHUNKS, int MT>
 struct GemvCfg {
+    static constexpr int kMT = MT;                              // token rows of x (1 or 2)
     static constexpr int kThreads = 288;
     static constexpr int kDecWarps = 8;
     static constexpr int kStages = STAGES;
     static constexpr int kStageChunks = SCHUNKS;                // chunks per weight stage
     static constexpr int kStagesPerSeg = kChunksPerSeg / SCHUNKS;
     static constexpr int kWBytes = SCHUNKS * kChunkBytes;
-    static constexpr int kXbBytes = kSegK * 2;        // one segment of x, BF16 (TMA destination)
+    static constexpr int kXbBytes = MT * kSegK * 2;   // one segment of x, [MT][256] BF16 (TMA destination)
     static constexpr int kSegSlots = 2;
     static constexpr int kEscCap = 2048;
     static constexpr int kMaxSegs = 96;
@@ -45,8 +46,8 @@ struct GemvCfg {
     static constexpr int kOffXb = kOffW + STAGES * kWBytes;  // 128-byte aligned
     static constexpr int kOffEsc = kOffXb + kSegSlots * kXbBytes;
     static constexpr int kOffHdr = kOffEsc + kSegSlots * kEscCap;
-    static constexpr int kOffRed = kOffHdr + kMaxSegs * kSegHdrBytes;  // 128 fp32
-    static constexpr int kOffBars = kOffRed + kTileRows * 4;
+    static constexpr int kOffRed = kOffHdr + kMaxSegs * kSegHdrBytes;  // [MT][128] fp32
+    static constexpr int kOffBars = kOffRed + MT * kTileRows * 4;
     // wfull[S], wempty[S], sfull[2], sempty[2], hdr, red, epi_in, epi_out
     static constexpr int kNumBars = 2 * STAGES + 2 * kSegSlots + 4;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
@@ -59,26 +60,31 @@ struct GemvBars {
     uint64_t *wfull, *wempty, *sfull, *sempty, *hdr, *red, *epi_in, *epi_out;
 };
 
-// acc[j] += w * x over 16 columns with x as BF16 (16 values at shared
-// address xs), one fma.rn.f32.bf16 per weight: the product of two BF16 values
-// is exact in fp32, so this is the same single rounding as fma.rn.f32 on the
-// widened operands.  acc[j] collects the columns congruent to j mod 4.
-__device__ __forceinline__ void dot16_bf(const uint32_t (&w)[8], uint32_t xs, float (&acc)[4]) {
-    const uint4 x0 = lds128(xs), x1 = lds128(xs + 16u);
-    const uint32_t X[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+// acc[t][j] += w * x[t] over 16 columns for each token t, with x as BF16 (16
+// values per token at shared address xs + t * 512), one fma.rn.f32.bf16 per
+// weight and token: the product of two BF16 values is exact in fp32, so this
+// is the same single rounding as fma.rn.f32 on the widened operands.
+// acc[t][j] collects the columns congruent to j mod 4.
+template <int MT>
+__device__ __forceinline__ void dot16_bf(const uint32_t (&w)[8], uint32_t xs, float (&acc)[MT][4]) {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-        asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
-            "mov.b32 {wl, wh}, %4;\n\t"
-            "mov.b32 {xl, xh}, %5;\n\t"
-            "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
-            "fma.rn.f32.bf16 %1, wh, xh, %1;\n\t"
-            "mov.b32 {wl, wh}, %6;\n\t"
-            "mov.b32 {xl, xh}, %7;\n\t"
-            "fma.rn.f32.bf16 %2, wl, xl, %2;\n\t"
-            "fma.rn.f32.bf16 %3, wh, xh, %3;\n\t}"
-            : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
-            : "r"(w[2 * g]), "r"(X[2 * g]), "r"(w[2 * g + 1]), "r"(X[2 * g + 1]));
+    for (int t = 0; t < MT; ++t) {
+        const uint4 x0 = lds128(xs + (uint32_t)(t * kSegK * 2)), x1 = lds128(xs + (uint32_t)(t * kSegK * 2) + 16u);
+        const uint32_t X[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+                "mov.b32 {wl, wh}, %4;\n\t"
+                "mov.b32 {xl, xh}, %5;\n\t"
+                "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+                "fma.rn.f32.bf16 %1, wh, xh, %1;\n\t"
+                "mov.b32 {wl, wh}, %6;\n\t"
+                "mov.b32 {xl, xh}, %7;\n\t"
+                "fma.rn.f32.bf16 %2, wl, xl, %2;\n\t"
+                "fma.rn.f32.bf16 %3, wh, xh, %3;\n\t}"
+                : "+f"(acc[t][0]), "+f"(acc[t][1]), "+f"(acc[t][2]), "+f"(acc[t][3])
+                : "r"(w[2 * g]), "r"(X[2 * g]), "r"(w[2 * g + 1]), "r"(X[2 * g + 1]));
+        }
     }
 }
 
@@ -173,7 +179,9 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
     const uint32_t c_off = (uint32_t)((2 - h) * kSlabBytes);
     const uint32_t xb0 = smem_u32(smem + C::kOffXb) + (uint32_t)(16 * h) * 2u;
 
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float acc[C::kMT][4];
+#pragma unroll
+    for (int t = 0; t < C::kMT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
     bool ok = warp_wait(b.hdr, 0, deadline);
     Table T{};
     uint32_t mask_q = 0, xseg = 0;
@@ -221,7 +229,7 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
                 uint32_t E[4], out[8];
                 decode_exponents_half(T, h ? cd[e].z : cd[e].x, h ? cd[e].w : cd[e].y, E);
                 assemble_half(sb[e], E, out);
-                dot16_bf(out, xseg + (uint32_t)((jj0 + e) * kChunkK * 2), acc);
+                dot16_bf<C::kMT>(out, xseg + (uint32_t)((jj0 + e) * kChunkK * 2), acc);
             }
         } else {
 #pragma unroll
@@ -229,7 +237,7 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
                 if (e < nch) {
                     uint32_t out[8];
                     decode_half_chunk(T, sb[e], cd[e], h, (stage_esc >> e) & 1u, run, out);
-                    dot16_bf(out, xseg + (uint32_t)((jj0 + e) * kChunkK * 2), acc);
+                    dot16_bf<C::kMT>(out, xseg + (uint32_t)((jj0 + e) * kChunkK * 2), acc);
                 }
             }
         }
@@ -243,10 +251,14 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
     }
 
     // ---- epilogue: add the two column halves of each row in fixed order
-    const float mine = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    constexpr int MT = C::kMT;
+    float mine[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) mine[t] = (acc[t][0] + acc[t][1]) + (acc[t][2] + acc[t][3]);
     float *red = reinterpret_cast<float *>(smem + C::kOffRed);
     if (h == 1) {
-        red[r] = mine;
+#pragma unroll
+        for (int t = 0; t < MT; ++t) red[t * kTileRows + r] = mine[t];
         __syncwarp();
         if (lane == 0) mbar_arrive(b.red);
         return;
@@ -255,14 +267,23 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
         if (lane == 0) raise_timeout(p.status, abort_flag);
         return;
     }
-    const float total = mine + red[r];
+    float total[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) total[t] = mine[t] + red[t * kTileRows + r];
     const int64_t n = tile * kTileRows + r;
     if (p.splits == 1) {
-        if (p.y != nullptr && n < p.N) p.y[n] = bf16_bits_rn(total);
-        if (p.amax != nullptr) argmax_warp(p.amax, n < p.N ? argmax_key(total, (uint32_t)n) : 0ull);
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            if (t < p.M) {
+                if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(total[t]);
+                if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(total[t], (uint32_t)n) : 0ull);
+            }
+        }
         return;
     }
-    __stcg(p.partials + (int64_t)split * p.Npad + n, total);
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+        if (t < p.M) __stcg(p.partials + ((int64_t)split * p.M + t) * p.Npad + n, total[t]);
     // the mbarrier arrive/wait pair orders these stores before thread 0's
     // release increment of the tile counter, which publishes them all
     __syncwarp();
@@ -282,30 +303,33 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
         return;
     }
     if (*last_flag == 0) return;
-    {
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        if (t >= p.M) continue;
         // ascending split order; eight loads in flight at a time
-        const float *src = p.partials + (n < p.N ? n : tile * kTileRows);
+        const float *src = p.partials + (int64_t)t * p.Npad + (n < p.N ? n : tile * kTileRows);
+        const int64_t stride = (int64_t)p.M * p.Npad;
         float s = 0.0f;
         int sp = 0;
         for (; sp + 8 <= p.splits; sp += 8) {
             float v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (int64_t)(sp + u) * p.Npad);
+            for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (int64_t)(sp + u) * stride);
 #pragma unroll
             for (int u = 0; u < 8; ++u) s += v[u];
         }
-        for (; sp < p.splits; ++sp) s += __ldcg(src + (int64_t)sp * p.Npad);
-        if (p.y != nullptr && n < p.N) p.y[n] = bf16_bits_rn(s);
-        if (p.amax != nullptr) argmax_warp(p.amax, n < p.N ? argmax_key(s, (uint32_t)n) : 0ull);
+        for (; sp < p.splits; ++sp) s += __ldcg(src + (int64_t)sp * stride);
+        if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(s);
+        if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(s, (uint32_t)n) : 0ull);
     }
     if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next call
 }
 
 // ------------------------------------------------------------------ kernel
-template <int STAGES, int SCHUNKS>
+template <int STAGES, int SCHUNKS, int MT>
 __global__ void __launch_bounds__(288, 2)
     w12_gemv_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_x) {
-    using C = GemvCfg<STAGES, SCHUNKS>;
+    using C = GemvCfg<STAGES, SCHUNKS, MT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBars);

@@ -73,7 +73,7 @@ struct DeviceState {
     uint32_t *status = nullptr;
     int occupancy[2][2] = {{0, 0}, {0, 0}};  // [ntok==32][a_smem]
     int q8_occupancy[2] = {0, 0};            // [ntok==32], Q8 copy kernels
-    int gemv_occupancy = 0;
+    int gemv_occupancy[2] = {0, 0};          // GEMV with 1, 2 token rows
 };
 
 DeviceState g_state[kMaxDevices];
@@ -140,18 +140,20 @@ int prepare_gemm(DeviceState &s, std::string *err) {
 
 constexpr int kGemvStages = 4;
 constexpr int kGemvChunks = 4;  // chunks per weight stage
-using GemvC = dev::GemvCfg<kGemvStages, kGemvChunks>;
+template <int MT>
+using GemvC = dev::GemvCfg<kGemvStages, kGemvChunks, MT>;
 
+template <int MT>
 int prepare_gemv(DeviceState &s, std::string *err) {
-    void *k = reinterpret_cast<void *>(&dev::w12_gemv_kernel<kGemvStages, kGemvChunks>);
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GemvC::kSmemBytes);
+    void *k = reinterpret_cast<void *>(&dev::w12_gemv_kernel<kGemvStages, kGemvChunks, MT>);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GemvC<MT>::kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemv)", err);
     e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemv carveout)", err);
     int occ = 0;
-    const int rc = resident_ctas(k, GemvC::kThreads, GemvC::kSmemBytes, s.device, err, &occ);
+    const int rc = resident_ctas(k, GemvC<MT>::kThreads, GemvC<MT>::kSmemBytes, s.device, err, &occ);
     if (rc != W12_OK) return rc;
-    s.gemv_occupancy = occ < 8 ? occ : 8;
+    s.gemv_occupancy[MT - 1] = occ < 8 ? occ : 8;
     return W12_OK;
 }
 
@@ -180,7 +182,8 @@ int device_state(DeviceState **out, std::string *err) {
         }
         e = cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), dev::g_w12_status);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)", err);
-        int rc = prepare_gemv(s, err);
+        int rc = prepare_gemv<1>(s, err);
+        if (rc == W12_OK) rc = prepare_gemv<2>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<16, false>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<32, false>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<16, true>(s, err);
@@ -194,10 +197,15 @@ int device_state(DeviceState **out, std::string *err) {
     return W12_OK;
 }
 
-// One token runs on CUDA cores unless W12_M1_PATH=tc asks for the tensor-core
-// kernel (kept selectable so both stay tested).
+// One and two tokens run on CUDA cores (W12_GEMV_MAX_M=1 sends two tokens to
+// the tensor cores; four token rows on CUDA cores measured 35 % slower than
+// tcgen05); one token goes to the tensor-core kernel instead when
+// W12_M1_PATH=tc (kept selectable so both stay tested).
 bool use_gemv(int M) {
-    if (M != 1) return false;
+    const char *mx = std::getenv("W12_GEMV_MAX_M");  // 1 sends two tokens to the tensor cores
+    const long max_m = mx ? std::strtol(mx, nullptr, 10) : 2;
+    if (M > max_m || M > 2) return false;
+    if (M > 1) return true;
     const char *v = std::getenv("W12_M1_PATH");
     return !(v != nullptr && std::strcmp(v, "tc") == 0);
 }
@@ -241,8 +249,8 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     int rc = device_state(&s, err);
     if (rc != W12_OK) return rc;
     plan->gemv = !q8 && use_gemv(M);
-    plan->ntok = M <= 16 ? 16 : 32;
-    const int occ = plan->gemv ? s->gemv_occupancy
+    plan->ntok = plan->gemv ? M : M <= 16 ? 16 : 32;
+    const int occ = plan->gemv ? s->gemv_occupancy[M - 1]
                     : q8       ? s->q8_occupancy[plan->ntok == 32]
                                : s->occupancy[plan->ntok == 32][use_smem_a_operand()];
     if (occ < 1) {
@@ -436,7 +444,7 @@ int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info,
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
     // tensor cores: 64-column boxes of NTOK token rows, 128-byte swizzle;
     // GEMV: one 256-column box of the single row, no swizzle
-    const cuuint32_t box[2] = {plan.gemv ? (cuuint32_t)kSegK : 64u, plan.gemv ? 1u : (cuuint32_t)plan.ntok};
+    const cuuint32_t box[2] = {plan.gemv ? (cuuint32_t)kSegK : 64u, (cuuint32_t)plan.ntok};
     const cuuint32_t estr[2] = {1u, 1u};
     CUresult cr = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(xsrc), dims, strides, box,
                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -470,8 +478,12 @@ int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info,
     const bool asmem = use_smem_a_operand();
     if (plan.gemv) {
         dim3 grid((unsigned)plan.splits, (unsigned)info.tiles);
-        e = launch_overlapped(dev::w12_gemv_kernel<kGemvStages, kGemvChunks>, grid, dim3(GemvC::kThreads),
-                              (size_t)GemvC::kSmemBytes, st, p, tm);
+        if (plan.ntok == 1)
+            e = launch_overlapped(dev::w12_gemv_kernel<kGemvStages, kGemvChunks, 1>, grid, dim3(GemvC<1>::kThreads),
+                                  (size_t)GemvC<1>::kSmemBytes, st, p, tm);
+        else
+            e = launch_overlapped(dev::w12_gemv_kernel<kGemvStages, kGemvChunks, 2>, grid, dim3(GemvC<2>::kThreads),
+                                  (size_t)GemvC<2>::kSmemBytes, st, p, tm);
     } else if (q8) {
         e = plan.ntok == 16 ? launch_gemm_kernel<16, false, true>(p, tm, plan.splits, info.tiles, st)
                             : launch_gemm_kernel<32, false, true>(p, tm, plan.splits, info.tiles, st);

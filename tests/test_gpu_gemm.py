@@ -194,7 +194,7 @@ def test_one_token_paths(case, m1_path):
         w = np.where((e > 140) | (e == 255), (w & 0x807F) | np.uint16(130 << 7), w).astype(np.uint16)
     x = wl.activations(1, w.shape[1], seed=35)
     mat = W12Weight(w)
-    assert w12.w12_gemm_launch_info(mat.info, 1)["ntok"] in (16, 32)
+    assert w12.w12_gemm_launch_info(mat.info, 1)["ntok"] == (1 if m1_path == "gemv" else 16)
     check_tolerance(_gemm(mat, x), oracle.gemm_f64(x, w), f"{case} {m1_path}")
 
 
@@ -206,3 +206,33 @@ def test_one_token_one_hot_exact(m1_path):
         x[0, k] = 0x3F80
         y = bits_to_f64(_gemm(W12Weight(w), x))
         assert np.array_equal(y[0], bits_to_f64(w[:, k])), f"{m1_path} column {k}"
+
+
+@pytest.fixture(params=["2", "1"])
+def gemv_max_m(request, monkeypatch):
+    monkeypatch.setenv("W12_GEMV_MAX_M", request.param)
+    return int(request.param)
+
+
+@pytest.mark.parametrize("M", [2, 3])
+@pytest.mark.parametrize("case", ["gauss", "ragged", "forced10", "heavy_long"])
+def test_two_token_paths(case, M, gemv_max_m):
+    """Two tokens run on CUDA cores by default and on tensor cores when the
+    CUDA-core limit is 1; three always on tensor cores; every path must meet
+    the tolerance."""
+    from gpu_util import check_tolerance
+    if case == "gauss":
+        w = wl.gaussian_weights(512, 5120, seed=41)
+    elif case == "ragged":
+        w = wl.heavy_tail_weights(301, 1001, seed=42)
+    elif case == "heavy_long":
+        w = wl.heavy_tail_weights(256, 17408, seed=43)
+    else:
+        w = wl.forced_escape_weights(256, 4096, 0.10, seed=44)
+        e = (w >> 7) & 0xFF
+        w = np.where((e > 140) | (e == 255), (w & 0x807F) | np.uint16(130 << 7), w).astype(np.uint16)
+    x = wl.activations(M, w.shape[1], seed=45 + M)
+    mat = W12Weight(w)
+    ntok = w12.w12_gemm_launch_info(mat.info, M)["ntok"]
+    assert ntok == (2 if M <= gemv_max_m else 16)
+    check_tolerance(_gemm(mat, x), oracle.gemm_f64(x, w), f"{case} M={M} ntok={ntok}")
