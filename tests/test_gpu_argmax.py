@@ -54,7 +54,7 @@ def _check(idx, val, x, w):
             assert i == r, f"token {m}: clear winner {r} missed (got {i})"
 
 
-@pytest.mark.parametrize("M", [1, 3, 16, 32])
+@pytest.mark.parametrize("M", [1, 2, 3, 16, 32])
 def test_argmax_matches_oracle(M, m1_path):
     if M > 1 and m1_path == "tc":
         pytest.skip("the M = 1 path switch only matters at one token")
@@ -76,7 +76,7 @@ def test_logits_are_the_plain_gemm():
         assert np.array_equal(dev_to_bits(y), ref), f"M={M}"
 
 
-@pytest.mark.parametrize("M", [1, 4, 17])
+@pytest.mark.parametrize("M", [1, 2, 4, 17])
 def test_ties_go_to_the_lowest_row(M, m1_path):
     """Identical rows give identical fp32 sums; the lowest of them must win,
     also across tiles and with a NaN row present."""

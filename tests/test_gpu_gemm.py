@@ -45,7 +45,7 @@ def test_small_gemm_all_m(M, a_operand):
 
 
 @pytest.mark.parametrize("shape", [(1, 1), (1, 32), (129, 33), (300, 1000), (300, 1001), (130, 7000)])
-@pytest.mark.parametrize("M", [1, 5, 32])
+@pytest.mark.parametrize("M", [1, 2, 5, 32])
 def test_ragged_gemm(shape, M):
     from gpu_util import check_tolerance
     n, k = shape
@@ -55,7 +55,7 @@ def test_ragged_gemm(shape, M):
 
 
 @pytest.mark.parametrize("frac", [0.02, 0.10, 1.0])
-@pytest.mark.parametrize("M", [1, 16])
+@pytest.mark.parametrize("M", [1, 2, 16])
 def test_forced_escape_gemm(frac, M, a_operand):
     from gpu_util import check_tolerance
     w = wl.forced_escape_weights(256, 4096, frac, seed=int(frac * 1000) + M)

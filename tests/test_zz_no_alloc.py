@@ -29,7 +29,8 @@ def _noalloc_raw(x, mat, y, M):
                                 torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("n,k,M", [(384, 2048, 1), (1000, 5120, 7), (6144, 5120, 16), (1024, 17408, 32)])
+@pytest.mark.parametrize("n,k,M", [(384, 2048, 1), (640, 3000, 2), (1000, 5120, 7), (6144, 5120, 16),
+                                   (1024, 17408, 32)])
 def test_noalloc_matches_workspace_gemm_twice(n, k, M):
     import torch
     from gpu_util import bits_to_f64, check_tolerance, dev_to_bits, to_dev_bf16
