@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--workload", default="layer", choices=["layer", "heavy", "model64", "lmhead"])
     ap.add_argument("--weights", default="w12", choices=["w12", "q8"],
                     help="w12: the lossless format; q8: the 8-bit verification copy of the same weights")
+    ap.add_argument("--no-group", action="store_true",
+                    help="one launch per matrix instead of q/k/v and gate/up as grouped launches")
     ap.add_argument("--graph", action="store_true", help="replay the step as a CUDA graph")
     ap.add_argument("--no-bf16", action="store_true", help="skip the cuBLAS BF16 comparator")
     ap.add_argument("--no-e2e", action="store_true")
@@ -276,7 +278,7 @@ def run_w12(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    from lossless_bit_weight_encode_gb300 import Q8Weight, W12Weight, w12
+    from lossless_bit_weight_encode_gb300 import Q8Weight, W12Group, W12Weight, w12
     from lossless_bit_weight_encode_gb300 import build as libbuild
     from lossless_bit_weight_encode_gb300 import workloads as wl
 
@@ -342,14 +344,36 @@ def run_w12(args):
         calls = [(x.data_ptr(), m.blob.data_ptr(), m.info, M, None, idx.data_ptr(), val.data_ptr(), ws.data_ptr(),
                   ws.numel(), sh) for x, m, ws in zip(xs, mats, aws)]
         launch = w12.w12_gemm_argmax_ptr
+        groups = [[i] for i in range(len(mats))]
     else:
-        calls = [(x.data_ptr(), m.blob.data_ptr(), m.info, y.data_ptr(), M, ws.data_ptr(), ws.numel(), sh)
-                 for x, m, y, ws in zip(xs, mats, ys, wss)]
-        launch = w12.w12_q8_gemm_ptr if args.weights == "q8" else w12.w12_gemm_ptr
+        # q, k, v multiply the same x, and so do gate and up: one launch each
+        layer_names = [n for n, _, _ in wl.LAYER_SHAPES]
+        grouped = (not args.no_group and args.weights == "w12" and args.workload in ("layer", "heavy")
+                   and names == layer_names)
+        groups = [[0, 1, 2], [3], [4, 5], [6]] if grouped else [[i] for i in range(len(mats))]
+        calls = []
+        group_ws = []  # keeps the group workspaces alive for the raw pointers below
+        for g in groups:
+            if len(g) == 1:
+                i = g[0]
+                calls.append((w12.w12_q8_gemm_ptr if args.weights == "q8" else w12.w12_gemm_ptr,
+                              (xs[i].data_ptr(), mats[i].blob.data_ptr(), mats[i].info, ys[i].data_ptr(), M,
+                               wss[i].data_ptr(), wss[i].numel(), sh)))
+            else:
+                grp = W12Group([mats[i] for i in g])
+                gws = grp.workspace(M)
+                group_ws.append((grp, gws))
+                calls.append((w12.w12_gemm_group_ptr,
+                              (xs[g[0]].data_ptr(), [mats[i].blob.data_ptr() for i in g], grp.infos,
+                               [ys[i].data_ptr() for i in g], M, gws.data_ptr(), gws.numel(), sh)))
+    if argmax:
+        calls = [(launch, c) for c in calls]
+        groups = [[i] for i in range(len(mats))]
+    names_launch = ["+".join(names[i] for i in g) for g in groups]
 
     def step():
-        for c in calls:
-            rc = launch(*c)
+        for fn, c in calls:
+            rc = fn(*c)
             if rc != 0:
                 raise w12.W12Error(rc, w12.w12_last_error())
 
@@ -398,9 +422,9 @@ def run_w12(args):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(kp)]
     barrier()
     for k in range(kp):
-        for i, c in enumerate(calls):
+        for i, (fn, c) in enumerate(calls):
             evs[k][i].record()
-            rc = launch(*c)
+            rc = fn(*c)
             if rc != 0:
                 raise w12.W12Error(rc, w12.w12_last_error())
         evs[k][nl].record()
@@ -412,7 +436,8 @@ def run_w12(args):
         "w12_gemv_kernel" if w12.w12_gemm_launch_info(mats[0].info, M).get("ntok") <= 4 else "w12_gemm_tc_kernel"
     layer_weights = sum(m.N * m.K for m in mats)
     packed = sum(int(m.info.total_bytes) for m in mats)
-    alg = [int(m.info.total_bytes) + 2 * M * m.K + 2 * M * m.N for m in mats]
+    alg = [sum(int(mats[i].info.total_bytes) + 2 * M * mats[i].N for i in g) + 2 * M * mats[g[0]].K
+           for g in groups]  # per launch: its blobs, one x, its outputs
     value = world * 2.0 * layer_weights / (ms_step * 1e-3) / 1e9
     peak, peak_kind = hbm_peak_gbs()
     achieved = sum(alg) / (sum(launch_ms) * 1e-3) / 1e9
@@ -424,11 +449,15 @@ def run_w12(args):
     # BF16 comparator (cuBLAS through torch.matmul), same shapes and x
     bf16 = None
     if not args.no_bf16:
-        wts = list(dense_weights())
+        dense = list(dense_weights())
+        # the same grouping for cuBLAS: one matmul over the concatenated weights
+        wts = [torch.cat([dense[i] for i in g], dim=0) if len(g) > 1 else dense[g[0]] for g in groups]
+        del dense
+        xb = [xs[g[0]] for g in groups]
         outs = [torch.empty((M, w.shape[0]), dtype=torch.bfloat16, device="cuda") for w in wts]
 
         def bstep():
-            for x, wt, o in zip(xs, wts, outs):
+            for x, wt, o in zip(xb, wts, outs):
                 torch.matmul(x, wt.t(), out=o)
                 if argmax:
                     torch.argmax(o, dim=1)
@@ -450,20 +479,22 @@ def run_w12(args):
     e2e = None
     if not args.no_e2e:
         xh = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs_host]
-        xs_e2e = [torch.empty_like(x) for x in xs]  # one device x per launch: every step copies all of them
         yh = [torch.empty((M, m.N), dtype=torch.bfloat16).pin_memory() for m in mats]
         if argmax:
             idx_h = torch.empty(M, dtype=torch.int32).pin_memory()
 
         def estep():
-            for xhi, x, m, y, yhi, ws in zip(xh, xs_e2e, mats, ys, yh, wss):
-                x.copy_(xhi, non_blocking=True)
+            # x comes in once per launch (the members of a group share it)
+            for (fn, c), g in zip(calls, groups):
+                xs[g[0]].copy_(xh[g[0]], non_blocking=True)
+                rc = fn(*c)
+                if rc != 0:
+                    raise w12.W12Error(rc, w12.w12_last_error())
                 if argmax:
-                    w12.w12_gemm_argmax(x, m.blob, m.info, M, None, idx, val, m.argmax_workspace(M), stream)
                     idx_h.copy_(idx, non_blocking=True)
                 else:
-                    m.gemm(x, out=y, stream=stream)
-                    yhi.copy_(y, non_blocking=True)
+                    for i in g:
+                        yh[i].copy_(ys[i], non_blocking=True)
 
         for _ in range(args.warmup):
             estep()
@@ -482,7 +513,7 @@ def run_w12(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e_ms = float(t.item())
         e2e = {"value": round(world * 2.0 * layer_weights / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": int(sum(2 * M * m.K for m in mats)),
+               "h2d_bytes_per_step": int(sum(2 * M * mats[g[0]].K for g in groups)),
                "d2h_bytes_per_step": int(4 * M) if argmax else int(sum(2 * M * m.N for m in mats)),
                "ms_per_step": round(e_ms, 5)}
 
@@ -505,7 +536,8 @@ def run_w12(args):
             "workload": WORKLOAD_TEXT[args.workload],
             "M": M, "global_batch": M * world, "parallelism": f"replicas x{world}",
             "l2": f"inputs larger than L2: {packed / 1e6:.1f} MB of W12 streamed per step (L2 129 MB)",
-            "launch": "cuda graph" if graph is not None else f"stream ({nl} launches per step)",
+            "launch": ("cuda graph" if graph is not None else "stream") + f" ({nl} launches per step: "
+                      + ", ".join(names_launch[:7]) + ("..." if nl > 7 else "") + ")",
         },
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": traffic,
@@ -526,7 +558,7 @@ def run_w12(args):
             "per_matrix_us": {n: round(statistics.mean(launch_ms[i::nshape]) * 1e3, 2)
                               for i, (n, _, _) in enumerate(wl.LAYER_SHAPES)}
                              if args.workload == "model64" else
-                             {n: round(v * 1e3, 2) for n, v in zip(names, launch_ms)},
+                             {n: round(v * 1e3, 2) for n, v in zip(names_launch, launch_ms)},
             "bf16_cublas_us_per_layer": round(bf16 * 1e3 / (wl.MODEL64_LAYERS if args.workload == "model64"
                                                             else 1), 2) if bf16 else None,
             "speedup_vs_bf16": round(bf16 / ms_step, 4) if bf16 else None,

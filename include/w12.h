@@ -159,6 +159,24 @@ int w12_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info *info,
              uint16_t *y_dev, int M, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Grouped product: y_devs[i] = x_dev . W_i^T for up to W12_MAX_GROUP matrices
+ * that share x (and so K) — the q/k/v projections of a decoder layer, or its
+ * gate/up projections — in one launch, planned as one matrix of all their
+ * 128-row tiles (no passage of the pages has a counterpart; it removes the
+ * per-launch fixed cost that dominates small matrices such as k and v).  Each
+ * output is exactly what w12_gemm would return for that matrix with the same
+ * split count.  blobs_dev[i] 256-byte aligned, y_devs[i] M x N_i BF16;
+ * infos[i] from w12_blob_info; all K equal (SHAPE otherwise).  Workspace:
+ * w12_gemm_group_workspace_size bytes, same rules as w12_gemm.
+ */
+#define W12_MAX_GROUP 4
+
+int w12_gemm_group_workspace_size(int count, const w12_info *infos, int M, size_t *bytes);
+
+int w12_gemm_group(const uint16_t *x_dev, int count, const void *const *blobs_dev, const w12_info *infos,
+                   uint16_t *const *y_devs, int M, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * LM-head product with a fused exact argmax ("SpecPilot: an agent doubled
  * speculative decoding speed, and the 10.87x needs context" (ai.jakubjirak.com),
  * §The mechanisms it found, lists a certified exact-argmax LM head; the page

@@ -11,7 +11,7 @@ import numpy as np
 from . import w12
 from .w12 import W12Error
 
-__all__ = ["w12", "W12Error", "W12Weight", "Q8Weight"]
+__all__ = ["w12", "W12Error", "W12Weight", "W12Group", "Q8Weight"]
 
 
 class W12Weight:
@@ -111,6 +111,40 @@ class W12Weight:
             out = torch.empty((self.N, self.K), dtype=torch.bfloat16, device=self.blob.device)
         w12.w12_decode(self.blob, self.info, out, stream)
         return out
+
+
+class W12Group:
+    """Matrices that multiply the same x (q/k/v, or gate/up), run as one
+    launch: ``gemm(x)`` returns one BF16 output per matrix."""
+
+    def __init__(self, mats):
+        if not 1 <= len(mats) <= w12.MAX_GROUP or len({m.K for m in mats}) != 1:
+            raise ValueError(f"1..{w12.MAX_GROUP} matrices with the same K")
+        self.mats = list(mats)
+        self.K = mats[0].K
+        self.infos = [m.info for m in mats]
+        self._ws = {}
+
+    def workspace(self, M: int):
+        import torch
+
+        size = w12.w12_gemm_group_workspace_size(self.infos, M)
+        ws = self._ws.get(M)
+        if ws is None or ws.numel() < size:
+            ws = torch.zeros(max(size, 256), dtype=torch.uint8, device=self.mats[0].blob.device)
+            self._ws[M] = ws
+        return ws
+
+    def gemm(self, x, outs=None, stream=None):
+        import torch
+
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != self.K or not x.is_contiguous():
+            raise ValueError("x must be a contiguous BF16 tensor of shape [M, K]")
+        M = int(x.shape[0])
+        if outs is None:
+            outs = [torch.empty((M, m.N), dtype=torch.bfloat16, device=x.device) for m in self.mats]
+        w12.w12_gemm_group(x, [m.blob for m in self.mats], self.infos, outs, M, self.workspace(M), stream)
+        return outs
 
 
 class Q8Weight:

@@ -64,6 +64,26 @@ struct GemmParams {
     uint64_t timeout_ns;
 };
 
+// Up to kMaxGroup matrices that share x (and so K) in one launch: grid row y
+// belongs to matrix i when tile0[i] <= y < tile0[i + 1]; each matrix keeps its
+// own blob, output, partials and counters, and all use the same split count.
+constexpr int kMaxGroup = 4;
+struct GemmGroup {
+    GemmParams m[kMaxGroup];
+    int64_t tile0[kMaxGroup + 1];
+    int32_t n;
+};
+
+// The matrix of this CTA's grid row and the row's tile within it.
+__device__ __forceinline__ int group_member(const GemmGroup &g, int64_t *tile) {
+    int i = 0;
+#pragma unroll
+    for (int j = 1; j < kMaxGroup; ++j)
+        if (j < g.n && (int64_t)blockIdx.y >= g.tile0[j]) i = j;
+    *tile = (int64_t)blockIdx.y - g.tile0[i];
+    return i;
+}
+
 template <int NTOK, int STAGES, bool A_SMEM, bool Q8 = false>
 struct GemmCfg {
     static constexpr bool kQ8 = Q8;                             // weights: Q8 copy instead of W12
@@ -631,7 +651,7 @@ __device__ void gemm_epilogue(const GemmParams &p, const Bars &b, volatile uint3
 // ------------------------------------------------------------------ kernel
 template <int NTOK, int STAGES, bool A_SMEM, bool Q8 = false>
 __global__ void __launch_bounds__(320, NTOK == 16 ? 3 : 2)
-    w12_gemm_tc_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_x) {
+    w12_gemm_tc_kernel(const __grid_constant__ GemmGroup grp, const __grid_constant__ CUtensorMap tmap_x) {
     using C = GemmCfg<NTOK, STAGES, A_SMEM, Q8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -655,7 +675,8 @@ __global__ void __launch_bounds__(320, NTOK == 16 ? 3 : 2)
 
     const int warp = threadIdx.x >> 5;
     const int split = blockIdx.x;
-    const int64_t tile = blockIdx.y;
+    int64_t tile;
+    const GemmParams &p = grp.m[group_member(grp, &tile)];
     const int s0 = (int)((int64_t)split * p.segs / p.splits);
     const int s1 = (int)((int64_t)(split + 1) * p.segs / p.splits);
     const int c0 = s0 * kChunksPerSeg;

@@ -328,7 +328,7 @@ __device__ void gemv_decode(const GemmParams &p, uint8_t *smem, const GemvBars &
 // ------------------------------------------------------------------ kernel
 template <int STAGES, int SCHUNKS, int MT>
 __global__ void __launch_bounds__(288, 2)
-    w12_gemv_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_x) {
+    w12_gemv_kernel(const __grid_constant__ GemmGroup grp, const __grid_constant__ CUtensorMap tmap_x) {
     using C = GemvCfg<STAGES, SCHUNKS, MT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
@@ -348,7 +348,8 @@ __global__ void __launch_bounds__(288, 2)
 
     const int warp = threadIdx.x >> 5;
     const int split = blockIdx.x;
-    const int64_t tile = blockIdx.y;
+    int64_t tile;
+    const GemmParams &p = grp.m[group_member(grp, &tile)];
     const int s0 = (int)((int64_t)split * p.segs / p.splits);
     const int s1 = (int)((int64_t)(split + 1) * p.segs / p.splits);
     const int c0 = s0 * kChunksPerSeg;

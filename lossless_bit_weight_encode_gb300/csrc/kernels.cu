@@ -330,7 +330,7 @@ cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 template <int NTOK, bool ASMEM, bool Q8 = false>
-cudaError_t launch_gemm_kernel(const dev::GemmParams &p, const CUtensorMap &tm, int splits, int64_t tiles,
+cudaError_t launch_gemm_kernel(const dev::GemmGroup &p, const CUtensorMap &tm, int splits, int64_t tiles,
                                cudaStream_t st) {
     dim3 grid((unsigned)splits, (unsigned)tiles);
     return launch_overlapped(dev::w12_gemm_tc_kernel<NTOK, kStages, ASMEM, Q8>, grid,
@@ -340,9 +340,27 @@ cudaError_t launch_gemm_kernel(const dev::GemmParams &p, const CUtensorMap &tm, 
 }  // namespace
 
 namespace {
+int gemm_impl(const uint16_t *x_dev, int count, const void *const *blobs, const w12_info *infos,
+              uint16_t *const *ys, unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream,
+              std::string *err, const w12_q8_info *q8 = nullptr);
 int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev,
               unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err,
-              const w12_q8_info *q8 = nullptr);
+              const w12_q8_info *q8 = nullptr) {
+    uint16_t *ys[1] = {y_dev};
+    return gemm_impl(x_dev, 1, &blob_dev, &info, ys, amax, M, workspace, ws_bytes, stream, err, q8);
+}
+
+// The matrices of a group share x, so K; they are planned as one matrix of all
+// their tiles (one split count) and each gets its own share of the workspace.
+w12_info group_info(int count, const w12_info *infos) {
+    w12_info g = infos[0];
+    for (int i = 1; i < count; ++i) {
+        g.tiles += infos[i].tiles;
+        g.N_pad += infos[i].N_pad;
+        g.N += infos[i].N;
+    }
+    return g;
+}
 
 // The planner and launcher work on a w12_info; a Q8 copy has the same grid.
 w12_info q8_as_info(const w12_q8_info &q) {
@@ -377,6 +395,18 @@ int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint
     return gemm_impl(x_dev, blob_dev, info, y_dev, nullptr, M, workspace, ws_bytes, stream, err);
 }
 
+int group_workspace_size(int count, const w12_info *infos, int M, size_t *bytes, std::string *err) {
+    GemmPlan plan;
+    const int rc = plan_gemm(group_info(count, infos), M, &plan, err);
+    if (rc == W12_OK) *bytes = plan.ws_bytes;
+    return rc;
+}
+
+int gemm_group(const uint16_t *x_dev, int count, const void *const *blobs, const w12_info *infos,
+               uint16_t *const *ys, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err) {
+    return gemm_impl(x_dev, count, blobs, infos, ys, nullptr, M, workspace, ws_bytes, stream, err);
+}
+
 int argmax_workspace_size(const w12_info &info, int M, size_t *bytes, std::string *err) {
     GemmPlan plan;
     const int rc = plan_gemm(info, M, &plan, err);
@@ -408,9 +438,10 @@ int gemm_argmax(const uint16_t *x_dev, const void *blob_dev, const w12_info &inf
 }
 
 namespace {
-int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev,
-              unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err,
-              const w12_q8_info *q8) {
+int gemm_impl(const uint16_t *x_dev, int count, const void *const *blobs, const w12_info *infos,
+              uint16_t *const *ys, unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream,
+              std::string *err, const w12_q8_info *q8) {
+    const w12_info info = group_info(count, infos);
     GemmPlan plan;
     int rc = plan_gemm(info, M, &plan, err, q8 != nullptr);
     if (rc != W12_OK) return rc;
@@ -455,24 +486,34 @@ int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info,
         return W12_ERR_CUDA;
     }
 
-    dev::GemmParams p;
-    p.blob = static_cast<const uint8_t *>(blob_dev);
-    p.off_seg = info.off_seghdr;
-    p.off_w = info.off_weights;
-    p.off_esc = info.off_escapes;
-    p.N = info.N;
-    p.Npad = info.N_pad;
-    p.chunks = (int32_t)info.chunks;
-    p.segs = (int32_t)info.segs;
-    p.M = M;
-    p.splits = plan.splits;
-    p.partials = reinterpret_cast<float *>(ws + plan.ws_partials);
-    p.counters = reinterpret_cast<uint32_t *>(ws + plan.ws_counters);
-    p.y = y_dev;
-    p.amax = amax;
-    p.scales = q8 ? reinterpret_cast<const float *>(p.blob + q8->off_scales) : nullptr;
-    p.status = s->status;
-    p.timeout_ns = timeout_ns();
+    dev::GemmGroup p{};
+    p.n = count;
+    int64_t tile0 = 0, npad0 = 0;
+    for (int i = 0; i < count; ++i) {
+        const w12_info &mi = infos[i];
+        dev::GemmParams &q = p.m[i];
+        q.blob = static_cast<const uint8_t *>(blobs[i]);
+        q.off_seg = mi.off_seghdr;
+        q.off_w = mi.off_weights;
+        q.off_esc = mi.off_escapes;
+        q.N = mi.N;
+        q.Npad = mi.N_pad;
+        q.chunks = (int32_t)mi.chunks;
+        q.segs = (int32_t)mi.segs;
+        q.M = M;
+        q.splits = plan.splits;
+        q.partials = reinterpret_cast<float *>(ws + plan.ws_partials) + (size_t)plan.splits * (size_t)M * (size_t)npad0;
+        q.counters = reinterpret_cast<uint32_t *>(ws + plan.ws_counters) + tile0;
+        q.y = ys[i];
+        q.amax = amax;
+        q.scales = q8 ? reinterpret_cast<const float *>(q.blob + q8->off_scales) : nullptr;
+        q.status = s->status;
+        q.timeout_ns = timeout_ns();
+        p.tile0[i] = tile0;
+        tile0 += mi.tiles;
+        npad0 += mi.N_pad;
+    }
+    for (int i = count; i <= dev::kMaxGroup; ++i) p.tile0[i] = tile0;
 
     cudaError_t e;
     const bool asmem = use_smem_a_operand();

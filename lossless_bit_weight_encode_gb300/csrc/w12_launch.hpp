@@ -33,6 +33,11 @@ int decode(const void *blob_dev, const w12_info &info, uint16_t *out_dev, void *
 int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,
          void *workspace, size_t ws_bytes, void *stream, std::string *err);
 
+int group_workspace_size(int count, const w12_info *infos, int M, size_t *bytes, std::string *err);
+
+int gemm_group(const uint16_t *x_dev, int count, const void *const *blobs, const w12_info *infos,
+               uint16_t *const *ys, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err);
+
 int argmax_workspace_size(const w12_info &info, int M, size_t *bytes, std::string *err);
 
 int gemm_argmax(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, int M, uint16_t *y_dev,

@@ -25,7 +25,7 @@ STATUS_NAMES = {
 EXPORTED = (
     "w12_last_error", "w12_status_string", "w12_format_version", "w12_encoded_size_host", "w12_encode_host",
     "w12_blob_info", "w12_blob_validate", "w12_decode", "w12_gemm_workspace_size", "w12_gemm_launch_info",
-    "w12_gemm", "w12_gemm_argmax_workspace_size", "w12_gemm_argmax", "w12_gemm_noalloc", "w12_encode_workspace_size", "w12_encoded_size_device", "w12_encode_device",
+    "w12_gemm", "w12_gemm_group_workspace_size", "w12_gemm_group", "w12_gemm_argmax_workspace_size", "w12_gemm_argmax", "w12_gemm_noalloc", "w12_encode_workspace_size", "w12_encoded_size_device", "w12_encode_device",
     "w12_q8_encoded_size", "w12_q8_encode_host", "w12_q8_blob_info", "w12_q8_gemm_workspace_size", "w12_q8_gemm",
     "w12_check_status", "w12_selftest_timeout",
 )
@@ -90,6 +90,9 @@ def lib() -> ctypes.CDLL:
     L.w12_gemm_workspace_size.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(sz)]
     L.w12_gemm_launch_info.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(ctypes.c_int32)]
     L.w12_gemm.argtypes = [vp, vp, ctypes.POINTER(w12_info), vp, i32, vp, sz, vp]
+    L.w12_gemm_group_workspace_size.argtypes = [i32, ctypes.POINTER(w12_info), i32, ctypes.POINTER(sz)]
+    L.w12_gemm_group.argtypes = [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(w12_info), ctypes.POINTER(vp), i32, vp,
+                                 sz, vp]
     L.w12_gemm_argmax_workspace_size.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(sz)]
     L.w12_gemm_argmax.argtypes = [vp, vp, ctypes.POINTER(w12_info), i32, vp, vp, vp, vp, sz, vp]
     L.w12_gemm_noalloc.argtypes = [vp, vp, ctypes.POINTER(w12_info), vp, i32, vp]
@@ -194,6 +197,34 @@ def w12_gemm_ptr(x_ptr: int, blob_ptr: int, info: w12_info, y_ptr: int, M: int, 
     """Raw-pointer form of w12_gemm that returns the status instead of raising
     (for timing loops that check once at the end)."""
     return lib().w12_gemm(x_ptr, blob_ptr, ctypes.byref(info), y_ptr, int(M), ws_ptr, ws_bytes, stream_handle)
+
+
+MAX_GROUP = 4  # W12_MAX_GROUP in include/w12.h
+
+
+def _infos(infos) -> ctypes.Array:
+    return (w12_info * len(infos))(*infos)
+
+
+def w12_gemm_group_workspace_size(infos, M: int) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().w12_gemm_group_workspace_size(len(infos), _infos(infos), int(M), ctypes.byref(out)))
+    return out.value
+
+
+def w12_gemm_group_ptr(x_ptr: int, blob_ptrs, infos, y_ptrs, M: int, ws_ptr: int, ws_bytes: int,
+                       stream_handle: int | None) -> int:
+    """Raw-pointer form of w12_gemm_group that returns the status."""
+    n = len(infos)
+    return lib().w12_gemm_group(x_ptr, n, (ctypes.c_void_p * n)(*blob_ptrs), _infos(infos),
+                                (ctypes.c_void_p * n)(*y_ptrs), int(M), ws_ptr, ws_bytes, stream_handle)
+
+
+def w12_gemm_group(x_dev, blobs_dev, infos, ys_dev, M: int, workspace, stream=None) -> None:
+    """ys_dev[i] = x_dev . W_i^T for matrices sharing K, in one launch."""
+    _check(w12_gemm_group_ptr(x_dev.data_ptr(), [b.data_ptr() for b in blobs_dev], infos,
+                              [y.data_ptr() for y in ys_dev], M, workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _stream_handle(stream)))
 
 
 def w12_gemm_argmax_ptr(x_ptr: int, blob_ptr: int, info: w12_info, M: int, y_ptr: int | None, idx_ptr: int,
