@@ -210,6 +210,20 @@ bool use_gemv(int M) {
     return !(v != nullptr && std::strcmp(v, "tc") == 0);
 }
 
+// Token tile of the tensor-core kernel.  32 unless the matrix has enough
+// 128-row tiles for several waves (a 152K-row LM head): two CTAs per SM with
+// the 32-token tile measured 160 us per grouped layer step at M = 4..16
+// against 190 us for three CTAs per SM with the 16-token tile, while the LM
+// head took 268 us with the 16-token tile against 303 us.  W12_NTOK=16 or 32
+// forces one (kept tested).
+int tc_token_tile(int M, int64_t tiles, int sm_count) {
+    const char *v = std::getenv("W12_NTOK");
+    if (v != nullptr && std::strcmp(v, "32") == 0) return 32;
+    if (M > 16) return 32;
+    if (v != nullptr && std::strcmp(v, "16") == 0) return 16;
+    return tiles >= 3 * (int64_t)sm_count ? 16 : 32;
+}
+
 bool use_smem_a_operand() {
     const char *v = std::getenv("W12_A_OPERAND");
     return v != nullptr && std::strcmp(v, "smem") == 0;
@@ -249,7 +263,7 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     int rc = device_state(&s, err);
     if (rc != W12_OK) return rc;
     plan->gemv = !q8 && use_gemv(M);
-    plan->ntok = plan->gemv ? M : M <= 16 ? 16 : 32;
+    plan->ntok = plan->gemv ? M : tc_token_tile(M, info.tiles, s->sm_count);
     const int occ = plan->gemv ? s->gemv_occupancy[M - 1]
                     : q8       ? s->q8_occupancy[plan->ntok == 32]
                                : s->occupancy[plan->ntok == 32][use_smem_a_operand()];

@@ -12,6 +12,7 @@ from lossless_bit_weight_encode_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 A_OPERANDS = ["tmem", "smem"]
+TOKEN_TILES = ["32", "16"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -20,9 +21,11 @@ def built():
     ensure_built()
 
 
-@pytest.fixture(params=A_OPERANDS)
+@pytest.fixture(params=[(a, t) for a in A_OPERANDS for t in TOKEN_TILES], ids=lambda v: f"{v[0]}-ntok{v[1]}")
 def a_operand(request, monkeypatch):
-    monkeypatch.setenv("W12_A_OPERAND", request.param)
+    """Every tensor-core variant: A in TMEM or SMEM, 32- or 16-token tile."""
+    monkeypatch.setenv("W12_A_OPERAND", request.param[0])
+    monkeypatch.setenv("W12_NTOK", request.param[1])
     return request.param
 
 
@@ -194,7 +197,7 @@ def test_one_token_paths(case, m1_path):
         w = np.where((e > 140) | (e == 255), (w & 0x807F) | np.uint16(130 << 7), w).astype(np.uint16)
     x = wl.activations(1, w.shape[1], seed=35)
     mat = W12Weight(w)
-    assert w12.w12_gemm_launch_info(mat.info, 1)["ntok"] == (1 if m1_path == "gemv" else 16)
+    assert w12.w12_gemm_launch_info(mat.info, 1)["ntok"] == (1 if m1_path == "gemv" else 32)
     check_tolerance(_gemm(mat, x), oracle.gemm_f64(x, w), f"{case} {m1_path}")
 
 
@@ -234,5 +237,5 @@ def test_two_token_paths(case, M, gemv_max_m):
     x = wl.activations(M, w.shape[1], seed=45 + M)
     mat = W12Weight(w)
     ntok = w12.w12_gemm_launch_info(mat.info, M)["ntok"]
-    assert ntok == (2 if M <= gemv_max_m else 16)
+    assert ntok == (2 if M <= gemv_max_m else 32)
     check_tolerance(_gemm(mat, x), oracle.gemm_f64(x, w), f"{case} M={M} ntok={ntok}")
