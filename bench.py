@@ -348,9 +348,15 @@ def run_w12(args):
     else:
         # q, k, v multiply the same x, and so do gate and up: one launch each
         layer_names = [n for n, _, _ in wl.LAYER_SHAPES]
-        grouped = (not args.no_group and args.weights == "w12" and args.workload in ("layer", "heavy")
-                   and names == layer_names)
-        groups = [[0, 1, 2], [3], [4, 5], [6]] if grouped else [[i] for i in range(len(mats))]
+        layers = len(mats) // len(layer_names)
+        if args.workload == "model64":
+            whole_layers = True
+        else:
+            whole_layers = args.workload in ("layer", "heavy") and names == layer_names
+        grouped = not args.no_group and args.weights == "w12" and whole_layers
+        per_layer = [[0, 1, 2], [3], [4, 5], [6]]
+        groups = ([[7 * l + i for i in g] for l in range(layers) for g in per_layer] if grouped
+                  else [[i] for i in range(len(mats))])
         calls = []
         group_ws = []  # keeps the group workspaces alive for the raw pointers below
         for g in groups:

@@ -23,7 +23,7 @@ Seeds: weights use numpy PCG64 seeded with 100 * workload_id + matrix_index
 (q0 k1 v2 o3 gate4 up5 down6); activations use 10000 + 100 * workload_id + M.
 model64 weights use torch's CUDA generator seeded with
 50000 + 7 * layer + matrix_index, its activations PCG64 seeded with
-(10000 + 100 * 5 + M, matrix_index).
+(10000 + 100 * 5 + M, K): one x per K, shared by the matrices of that K.
 """
 from __future__ import annotations
 
@@ -162,9 +162,11 @@ def model64_weight_dev(layer: int, index: int) -> torch.Tensor:
 
 def model64_activation(m: int, index: int) -> np.ndarray:
     """The x [m, K] fed to matrix `index` of every layer of the 64-layer
-    stream (N(0, 1), PCG64 seeded with (activation_seed, index))."""
+    stream: one activation per K (N(0, 1), PCG64 seeded with
+    (activation_seed, K)), so q, k, v, gate and up (K = 5120) share it as in a
+    decoder layer, and o and down get their own."""
     k = LAYER_SHAPES[index][2]
-    rng = np.random.Generator(np.random.PCG64([activation_seed("model64", m), index]))
+    rng = np.random.Generator(np.random.PCG64([activation_seed("model64", m), k]))
     return to_bf16_bits(rng.standard_normal((m, k), dtype=np.float32))
 
 
