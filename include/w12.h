@@ -137,17 +137,21 @@ int w12_gemm_workspace_size(const w12_info *info, int M, size_t *bytes);
 
 /*
  * The launch plan w12_gemm uses for this blob and M on the current device:
- * out[0] token tile of the MMA (16 or 32), out[1] CTAs per 128-row tile along
- * K (split-K), out[2] total CTAs, out[3] resident CTAs per SM assumed.
+ * out[0] token rows per CTA (1 or 2 on the CUDA-core path, 16 or 32 on the
+ * tensor-core path), out[1] CTAs per 128-row tile along K (split-K), out[2]
+ * total CTAs, out[3] resident CTAs per SM assumed.
  */
 int w12_gemm_launch_info(const w12_info *info, int M, int32_t out[4]);
 
 /*
  * y_dev[m * N + n] = BF16_rne( sum_k x_dev[m * K + k] * W[n][k] ), fp32
  * accumulation, for 1 <= M <= 32, with W held by blob_dev.  The weights are
- * streamed from HBM in packed form and decoded in registers; tensor cores
- * (tcgen05, weights as the 128-row A operand, tokens as N = 16 or 32) do the
- * products.  x_dev: M x K row-major BF16; y_dev: M x N row-major BF16, 2-byte
+ * streamed from HBM in packed form and decoded in registers.  One or two
+ * tokens: CUDA cores multiply them (fma.rn.f32.bf16, one per weight and
+ * token); three or more: tensor cores (tcgen05, weights as the 128-row A
+ * operand, tokens as N = 16 or 32).  The sums are reproducible run to run
+ * (fixed split-K order); w12_gemm_launch_info reports the plan.
+ * x_dev: M x K row-major BF16; y_dev: M x N row-major BF16, 2-byte
  * aligned.  blob_dev must be 256-byte aligned.  workspace: at least
  * w12_gemm_workspace_size bytes, 256-byte aligned, ZERO-FILLED BEFORE ITS
  * FIRST USE; every successful call leaves the counters zero again (after a
