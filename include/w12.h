@@ -138,8 +138,10 @@ int w12_gemm_workspace_size(const w12_info *info, int M, size_t *bytes);
 /*
  * The launch plan w12_gemm uses for this blob and M on the current device:
  * out[0] token rows per CTA (1 or 2 on the CUDA-core path, 16 or 32 on the
- * tensor-core path), out[1] CTAs per 128-row tile along K (split-K), out[2]
- * total CTAs, out[3] resident CTAs per SM assumed.
+ * tensor-core path), out[1] CTAs per 128-row tile along K (split-K; when the
+ * CUDA-core path shares one wave of CTAs out as equal contiguous ranges of
+ * the tiles' 256-column segments, the most CTAs that can share a tile),
+ * out[2] total CTAs, out[3] resident CTAs per SM assumed.
  */
 int w12_gemm_launch_info(const w12_info *info, int M, int32_t out[4]);
 
@@ -168,8 +170,8 @@ int w12_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info *info,
  * gate/up projections — in one launch, planned as one matrix of all their
  * 128-row tiles (no passage of the pages has a counterpart; it removes the
  * per-launch fixed cost that dominates small matrices such as k and v).  Each
- * output is exactly what w12_gemm would return for that matrix with the same
- * split count.  blobs_dev[i] 256-byte aligned, y_devs[i] M x N_i BF16;
+ * output meets the same bound as w12_gemm's and is bit-identical to it when
+ * both split K the same way (fixed split-K with the same split count).  blobs_dev[i] 256-byte aligned, y_devs[i] M x N_i BF16;
  * infos[i] from w12_blob_info; all K equal (SHAPE otherwise).  Workspace:
  * w12_gemm_group_workspace_size bytes, same rules as w12_gemm.
  */

@@ -64,24 +64,94 @@ struct GemmParams {
     uint64_t timeout_ns;
 };
 
-// Up to kMaxGroup matrices that share x (and so K) in one launch: grid row y
-// belongs to matrix i when tile0[i] <= y < tile0[i + 1]; each matrix keeps its
-// own blob, output, partials and counters, and all use the same split count.
+// Up to kMaxGroup matrices that share x (and so K) in one launch: group tile
+// y (all members' tiles in order) belongs to matrix i when tile0[i] <= y <
+// tile0[i + 1]; each matrix keeps its own blob, output, partials and counters.
+//
+// Two ways to share the work among CTAs.  Fixed split-K (units == 0): grid
+// (splits, tiles); CTA (x, y) takes segments [x segs / splits, (x + 1) segs /
+// splits) of group tile y.  Stream-K (units > 0): the group's tiles, each cut
+// into its segs segments, form one sequence of units = tiles x segs; CTA c of
+// the 1-D grid of ctas takes units [c units / ctas, (c + 1) units / ctas), a
+// range that may end one tile and start the next, so that a single wave of
+// CTAs gets equal work however the tile count divides the SM count.  The
+// planner keeps units x ctas below 2^31, so this arithmetic is 32-bit.
 constexpr int kMaxGroup = 4;
 struct GemmGroup {
     GemmParams m[kMaxGroup];
     int64_t tile0[kMaxGroup + 1];
+    int32_t units;  // stream-K units (0: fixed split-K)
+    int32_t ctas;   // stream-K grid size
     int32_t n;
 };
 
-// The matrix of this CTA's grid row and the row's tile within it.
-__device__ __forceinline__ int group_member(const GemmGroup &g, int64_t *tile) {
+// Every member reports to the same device status word.
+__device__ __forceinline__ uint32_t *group_status(const GemmGroup &g) { return g.m[0].status; }
+
+// The member holding group tile gt and the tile's index within it.
+__device__ __forceinline__ int member_of(const GemmGroup &g, int64_t gt, int64_t *tile) {
     int i = 0;
 #pragma unroll
     for (int j = 1; j < kMaxGroup; ++j)
-        if (j < g.n && (int64_t)blockIdx.y >= g.tile0[j]) i = j;
-    *tile = (int64_t)blockIdx.y - g.tile0[i];
+        if (j < g.n && gt >= g.tile0[j]) i = j;
+    *tile = gt - g.tile0[i];
     return i;
+}
+
+// The matrix of this CTA's grid row and the row's tile within it (fixed split-K).
+__device__ __forceinline__ int group_member(const GemmGroup &g, int64_t *tile) {
+    return member_of(g, (int64_t)blockIdx.y, tile);
+}
+
+// One CTA's share of one tile: segments [s0, s1), partial-sum slot idx of the
+// tile's count shares (count == 1: the CTA owns the whole tile).
+struct Piece {
+    int member;
+    int64_t tile;  // within the member
+    int s0, s1;
+    int idx, count;
+};
+
+// The units of this CTA still to hand out as pieces.
+struct CtaWork {
+    uint32_t u, u1;
+};
+
+__device__ __forceinline__ CtaWork cta_work(const GemmGroup &g) {
+    if (g.units == 0) return CtaWork{0u, 1u};
+    const uint32_t c = blockIdx.x, units = (uint32_t)g.units, ctas = (uint32_t)g.ctas;
+    return CtaWork{c * units / ctas, (c + 1u) * units / ctas};
+}
+
+// The stream-K CTA whose range holds unit u: the largest c with
+// floor(c units / ctas) <= u.
+__device__ __forceinline__ uint32_t unit_owner(const GemmGroup &g, uint32_t u) {
+    return ((u + 1u) * (uint32_t)g.ctas - 1u) / (uint32_t)g.units;
+}
+
+// The next piece of this CTA's work, in order; false when none is left.
+__device__ __forceinline__ bool next_piece(const GemmGroup &g, CtaWork &w, Piece &pc) {
+    if (w.u >= w.u1) return false;
+    if (g.units == 0) {
+        pc.member = group_member(g, &pc.tile);
+        const GemmParams &p = g.m[pc.member];
+        pc.idx = (int)blockIdx.x;
+        pc.count = p.splits;
+        pc.s0 = (int)((int64_t)pc.idx * p.segs / p.splits);
+        pc.s1 = (int)((int64_t)(pc.idx + 1) * p.segs / p.splits);
+        w.u = w.u1;
+        return true;
+    }
+    const uint32_t segs = (uint32_t)g.m[0].segs;
+    const uint32_t gt = w.u / segs, first_unit = gt * segs;
+    pc.s0 = (int)(w.u - first_unit);
+    pc.s1 = (int)min(segs, w.u1 - first_unit);
+    const uint32_t first = unit_owner(g, first_unit);
+    pc.idx = (int)(blockIdx.x - first);
+    pc.count = (int)(unit_owner(g, first_unit + segs - 1u) - first + 1u);
+    pc.member = member_of(g, (int64_t)gt, &pc.tile);
+    w.u = first_unit + (uint32_t)pc.s1;
+    return true;
 }
 
 template <int NTOK, int STAGES, bool A_SMEM, bool Q8 = false>
@@ -163,7 +233,8 @@ __device__ __forceinline__ bool escapes_staged(uint32_t total) {
 // is still read correctly.
 constexpr uint32_t kPrefetchBytes = 96 * 1024;
 template <int kChunkB, bool kHeaders>
-__device__ __forceinline__ void prefetch_cta_weights(const GemmParams &p, int64_t tile, int s0, int c0, int c1) {
+__device__ __forceinline__ void prefetch_cta_weights(const GemmParams &p, int64_t tile, int s0, int c0, int c1,
+                                                     uint32_t &budget) {
     if (kHeaders) {
         const int nsegs_cta = (c1 - c0 + kChunksPerSeg - 1) / kChunksPerSeg;
         prefetch_l2(p.blob + p.off_seg + (uint64_t)(tile * p.segs + s0) * kSegHdrBytes,
@@ -171,10 +242,23 @@ __device__ __forceinline__ void prefetch_cta_weights(const GemmParams &p, int64_
     }
     const uint8_t *w = p.blob + p.off_w + (uint64_t)(tile * p.chunks + c0) * kChunkB;
     uint32_t left = (uint32_t)(c1 - c0) * kChunkB;
-    if (left > kPrefetchBytes) left = kPrefetchBytes;
+    if (left > budget) left = budget;
+    budget -= left;
     for (uint32_t off = 0; off < left; off += 4 * kChunkB) {
         const uint32_t n = left - off < 4u * kChunkB ? left - off : 4u * kChunkB;
         prefetch_l2(w + off, n);
+    }
+}
+
+// The same for each of a CTA's pieces in order until kPrefetchBytes are asked for.
+template <int kChunkB, bool kHeaders>
+__device__ __forceinline__ void prefetch_pieces(const GemmGroup &g, const Piece *pieces, int npieces) {
+    uint32_t budget = kPrefetchBytes;
+    for (int k = 0; k < npieces && budget > 0; ++k) {
+        const Piece &pc = pieces[k];
+        const GemmParams &p = g.m[pc.member];
+        prefetch_cta_weights<kChunkB, kHeaders>(p, pc.tile, pc.s0, pc.s0 * kChunksPerSeg,
+                                                min(pc.s1 * kChunksPerSeg, p.chunks), budget);
     }
 }
 
@@ -714,7 +798,10 @@ __global__ void __launch_bounds__(320, NTOK == 16 ? 3 : 2)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (threadIdx.x == 0) pdl_launch_dependents();
-    if (warp == 8 && (threadIdx.x & 31) == 0) prefetch_cta_weights<C::kChunkB, !Q8>(p, tile, s0, c0, c1);
+    if (warp == 8 && (threadIdx.x & 31) == 0) {
+        uint32_t budget = kPrefetchBytes;
+        prefetch_cta_weights<C::kChunkB, !Q8>(p, tile, s0, c0, c1, budget);
+    }
     pdl_wait();
 
     if (warp == 8) {

@@ -229,6 +229,13 @@ bool use_smem_a_operand() {
     return v != nullptr && std::strcmp(v, "smem") == 0;
 }
 
+// The GEMV shares a single wave's work as stream-K unit ranges unless
+// W12_STREAMK=0 (then fixed split-K as for the tensor-core kernel).
+bool use_stream_k() {
+    const char *v = std::getenv("W12_STREAMK");
+    return !(v != nullptr && std::strcmp(v, "0") == 0);
+}
+
 uint64_t timeout_ns() {
     const char *v = std::getenv("W12_TIMEOUT_MS");
     const long ms = v ? std::strtol(v, nullptr, 10) : 0;
@@ -274,18 +281,37 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     constexpr int64_t kMaxSegs = dev::GemmCfg<16, kStages, false>::kMaxSegs;
     const int64_t capacity = (int64_t)s->sm_count * occ;
     const int64_t tiles = info.tiles, segs = info.segs;
-    int64_t splits = capacity / tiles;
-    if (splits < 1) splits = 1;
-    if (splits > segs) splits = segs;
-    int64_t per = (segs + splits - 1) / splits;          // segments of the longest CTA
-    if (per > kMaxSegs) per = kMaxSegs;
-    splits = (segs + per - 1) / per;                      // fewest splits with that length
-    if (const char *v = std::getenv("W12_SPLITS")) {      // tuning override
-        const long f = std::strtol(v, nullptr, 10);
-        if (f >= 1 && f <= segs && (segs + f - 1) / f <= kMaxSegs) splits = f;
+    const char *forced = std::getenv("W12_SPLITS");  // tuning override: fixed split-K
+    plan->units = 0;
+    // one wave of equal contiguous unit ranges (stream-K): no SM idles
+    // because the tile count does not divide the resident CTA count
+    const int64_t units = tiles * segs;
+    int64_t sk_ctas = capacity < units ? capacity : units;
+    if ((units + sk_ctas - 1) / sk_ctas > kMaxSegs) sk_ctas = (units + kMaxSegs - 1) / kMaxSegs;
+    // (the device computes unit x ctas products in 32 bits)
+    if (plan->gemv && forced == nullptr && tiles < capacity && units * sk_ctas < (int64_t(1) << 31) &&
+        use_stream_k()) {
+        const int64_t shortest = units / sk_ctas;  // units of the shortest range
+        plan->units = units;
+        // most ranges one tile can meet: the one holding its first unit plus
+        // at most 1 + (segs - 2) / shortest range starts inside it
+        plan->splits = (int)(segs == 1 ? 1 : 2 + (segs - 2) / shortest);
+        plan->ctas = (int)sk_ctas;
+    } else {
+        int64_t splits = capacity / tiles;
+        if (splits < 1) splits = 1;
+        if (splits > segs) splits = segs;
+        int64_t per = (segs + splits - 1) / splits;          // segments of the longest CTA
+        if (per > kMaxSegs) per = kMaxSegs;
+        splits = (segs + per - 1) / per;                      // fewest splits with that length
+        if (forced != nullptr) {
+            const long f = std::strtol(forced, nullptr, 10);
+            if (f >= 1 && f <= segs && (segs + f - 1) / f <= kMaxSegs) splits = f;
+        }
+        plan->splits = (int)splits;
+        plan->ctas = (int)(tiles * splits);
     }
-    plan->splits = (int)splits;
-    plan->ctas = (int)(tiles * splits);
+    const int64_t splits = plan->splits;
     plan->ctas_per_sm = occ;
     const int64_t k8 = (info.K + 7) / 8 * 8;
     plan->ws_counters = 0;
@@ -502,6 +528,8 @@ int gemm_impl(const uint16_t *x_dev, int count, const void *const *blobs, const 
 
     dev::GemmGroup p{};
     p.n = count;
+    p.units = (int32_t)plan.units;
+    p.ctas = plan.ctas;
     int64_t tile0 = 0, npad0 = 0;
     for (int i = 0; i < count; ++i) {
         const w12_info &mi = infos[i];
@@ -532,7 +560,7 @@ int gemm_impl(const uint16_t *x_dev, int count, const void *const *blobs, const 
     cudaError_t e;
     const bool asmem = use_smem_a_operand();
     if (plan.gemv) {
-        dim3 grid((unsigned)plan.splits, (unsigned)info.tiles);
+        const dim3 grid = plan.units > 0 ? dim3((unsigned)plan.ctas, 1u) : dim3((unsigned)plan.splits, (unsigned)info.tiles);
         if (plan.ntok == 1)
             e = launch_overlapped(dev::w12_gemv_kernel<kGemvStages, kGemvChunks, 1>, grid, dim3(GemvC<1>::kThreads),
                                   (size_t)GemvC<1>::kSmemBytes, st, p, tm);

@@ -497,6 +497,16 @@ __device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t *counter) {
     return old;
 }
 
+// The same split into its parts, for a thread that arrives on several
+// counters: one release fence, relaxed increments that are all in flight at
+// once, and (when one of them was the last arrival) one acquire fence.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ uint32_t arrive_relaxed(uint32_t *counter) {
+    uint32_t old;
+    asm volatile("atom.add.relaxed.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+    return old;
+}
+
 // ---------------------------------------------------------------- Q8 copy
 // 16 int8 weights (two's complement; one chunk half of a row) to 8 BF16 pairs,
 // lower column in the low half, exactly: byte b ^ 0x80 = b + 128 goes into

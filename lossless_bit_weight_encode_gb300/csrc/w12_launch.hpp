@@ -14,8 +14,9 @@ namespace launch {
 struct GemmPlan {
     bool gemv = false;      // one token on CUDA cores instead of tensor cores
     int ntok = 16;          // MMA token width (16 or 32)
-    int splits = 1;         // CTAs per tile along K
+    int splits = 1;         // CTAs per tile along K (stream-K: the most CTAs sharing a tile)
     int ctas = 0;           // grid size
+    int64_t units = 0;      // stream-K: tiles x segments shared by the ctas (0: fixed split-K)
     int ctas_per_sm = 0;    // resident CTAs per SM the plan assumed
     size_t ws_counters = 0, ws_partials = 0, ws_x = 0;  // workspace offsets
     size_t ws_bytes = 0;

@@ -1,0 +1,87 @@
+"""Stream-K work sharing of the CUDA-core GEMV (one or two tokens): when a
+single wave of CTAs holds more CTAs than there are 128-row tiles, the tiles x
+segments units are cut into equal contiguous ranges, so a CTA may finish one
+tile and start the next (of the same matrix or, in a group, of the next
+member).  Every output meets the tolerance against the fp64 oracle, with and
+without stream-K; the plan uses one full wave; results are reproducible and
+the split-K counters are left at zero."""
+import numpy as np
+import pytest
+
+import oracle
+from lossless_bit_weight_encode_gb300 import W12Group, W12Weight, w12
+from lossless_bit_weight_encode_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from gpu_util import ensure_built
+    ensure_built()
+
+
+def _capacity(M):
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # two GEMV CTAs are resident per SM (288 threads, ~107 KB shared memory)
+    return 2 * sms
+
+
+@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("shape", [(12763, 5020), (5000, 17408), (1000, 3000)])
+def test_stream_k_matches_oracle(M, shape, monkeypatch):
+    import torch
+    from gpu_util import check_tolerance, dev_to_bits, to_dev_bf16
+    n, k = shape
+    w = wl.heavy_tail_weights(n, k, seed=300 + n % 97)
+    x = wl.activations(M, k, seed=301 + M)
+    ref = oracle.gemm_f64(x, w)
+    mat = W12Weight(w)
+    for mode in ("1", "0"):
+        monkeypatch.setenv("W12_STREAMK", mode)
+        plan = w12.w12_gemm_launch_info(mat.info, M)
+        tiles, segs = int(mat.info.tiles), int(mat.info.segs)
+        if mode == "1":
+            assert plan["ctas"] == min(_capacity(M), tiles * segs), plan
+        else:
+            assert plan["ctas"] == tiles * plan["splits"], plan
+        y = dev_to_bits(mat.gemm(to_dev_bf16(x)))
+        w12.w12_check_status()
+        torch.cuda.synchronize()
+        check_tolerance(y, ref, f"{shape} M={M} W12_STREAMK={mode}")
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_stream_k_crosses_group_members(M):
+    """q/k/v-like group whose ranges end inside one member and start in the next."""
+    import torch
+    from gpu_util import check_tolerance, dev_to_bits, to_dev_bf16
+    k = 5120
+    shapes = [(2560, k), (520, k), (384, k)]
+    ws = [wl.heavy_tail_weights(n, kk, seed=310 + i) for i, (n, kk) in enumerate(shapes)]
+    mats = [W12Weight(w) for w in ws]
+    units = sum(int(m.info.tiles) for m in mats) * int(mats[0].info.segs)
+    assert units > _capacity(M)  # more than one unit per CTA, so ranges cross tiles
+    x = wl.activations(M, k, seed=315 + M)
+    ys = W12Group(mats).gemm(to_dev_bf16(x))
+    w12.w12_check_status()
+    torch.cuda.synchronize()
+    for i, (w, y) in enumerate(zip(ws, ys)):
+        check_tolerance(dev_to_bits(y), oracle.gemm_f64(x, w), f"member {i} M={M}")
+
+
+def test_stream_k_reproducible_and_counters_reset():
+    import torch
+    from gpu_util import dev_to_bits, to_dev_bf16
+    w = wl.gaussian_weights(9000, 5120, seed=320)
+    x = to_dev_bf16(wl.activations(1, 5120, seed=321))
+    mat = W12Weight(w)
+    y1 = dev_to_bits(mat.gemm(x))
+    ws = mat.workspace(1)
+    w12.w12_check_status()
+    tiles = int(mat.info.tiles)
+    assert int(ws[: tiles * 4].view(torch.int32).abs().sum().item()) == 0, "split-K counters not reset"
+    for _ in range(3):
+        assert np.array_equal(dev_to_bits(mat.gemm(x)), y1)
+    w12.w12_check_status()
