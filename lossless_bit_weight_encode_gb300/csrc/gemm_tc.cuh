@@ -146,9 +146,14 @@ __device__ __forceinline__ bool next_piece(const GemmGroup &g, CtaWork &w, Piece
     const uint32_t gt = w.u / segs, first_unit = gt * segs;
     pc.s0 = (int)(w.u - first_unit);
     pc.s1 = (int)min(segs, w.u1 - first_unit);
-    const uint32_t first = unit_owner(g, first_unit);
-    pc.idx = (int)(blockIdx.x - first);
-    pc.count = (int)(unit_owner(g, first_unit + segs - 1u) - first + 1u);
+    if (pc.s0 == 0 && first_unit + segs <= w.u1) {
+        pc.idx = 0;  // the whole tile lies in this range
+        pc.count = 1;
+    } else {
+        const uint32_t first = unit_owner(g, first_unit);
+        pc.idx = (int)(blockIdx.x - first);
+        pc.count = (int)(unit_owner(g, first_unit + segs - 1u) - first + 1u);
+    }
     pc.member = member_of(g, (int64_t)gt, &pc.tile);
     w.u = first_unit + (uint32_t)pc.s1;
     return true;

@@ -149,6 +149,7 @@ __device__ void gemv_producer(const GemmGroup &g, const Piece *pieces, int npiec
                 ++gls;
                 if (!hdr_ready) {
                     if (!mbar_wait(b.hdr, 0, deadline)) {
+                        mbar_arrive(b.sfull + sslot);  // lets the phase end once x has landed
                         failed = stop = true;
                         break;
                     }

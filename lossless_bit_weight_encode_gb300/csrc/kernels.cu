@@ -14,6 +14,7 @@
 #include "encode_gpu.cuh"
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
+#include "gemv_sm.cuh"
 #include "w12_host.hpp"
 #include "w12_launch.hpp"
 
@@ -74,6 +75,7 @@ struct DeviceState {
     int occupancy[2][2] = {{0, 0}, {0, 0}};  // [ntok==32][a_smem]
     int q8_occupancy[2] = {0, 0};            // [ntok==32], Q8 copy kernels
     int gemv_occupancy[2] = {0, 0};          // GEMV with 1, 2 token rows
+    int gemv_sm_occupancy[2] = {0, 0};       // one-CTA-per-SM GEMV with 1, 2 token rows
 };
 
 DeviceState g_state[kMaxDevices];
@@ -157,6 +159,21 @@ int prepare_gemv(DeviceState &s, std::string *err) {
     return W12_OK;
 }
 
+template <int MT>
+int prepare_gemv_sm(DeviceState &s, std::string *err) {
+    using C = dev::GemvSmCfg<MT>;
+    void *k = reinterpret_cast<void *>(&dev::w12_gemv_sm_kernel<MT>);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemv_sm)", err);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemv_sm carveout)", err);
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, C::kThreads, (size_t)C::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(gemv_sm)", err);
+    s.gemv_sm_occupancy[MT - 1] = occ;
+    return W12_OK;
+}
+
 // Per-device set-up on first use (with that device current).
 int device_state(DeviceState **out, std::string *err) {
     int dev = 0;
@@ -184,6 +201,8 @@ int device_state(DeviceState **out, std::string *err) {
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)", err);
         int rc = prepare_gemv<1>(s, err);
         if (rc == W12_OK) rc = prepare_gemv<2>(s, err);
+        if (rc == W12_OK) rc = prepare_gemv_sm<1>(s, err);
+        if (rc == W12_OK) rc = prepare_gemv_sm<2>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<16, false>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<32, false>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<16, true>(s, err);
@@ -229,6 +248,24 @@ bool use_smem_a_operand() {
     return v != nullptr && std::strcmp(v, "smem") == 0;
 }
 
+// Which CUDA-core kernel: one CTA per SM with sixteen decode warps (gemv_sm.cuh)
+// or two with eight each (gemv.cuh).  The first keeps every warp of an SM busy
+// to the end of a single wave; it pays for finding where its chunks' escapes
+// start, and its long stream-K ranges cost more than the second's extra waves
+// once the tiles fill two CTAs per SM.  Measured (layer step, M = 1 / 2):
+// 114.6 / 129.3 us against 117.3 / 136.0; heavy-tail weights (0.4 % escapes)
+// 194 against 174 us; the LM head 212 against 207 us.  So: one CTA per SM
+// when the tiles are fewer than two per SM and escapes are rare enough that
+// at most ~20 % of quarter-chunks (32 x 32 weights) hold one.  W12_GEMV_SM=0 or
+// 1 forces a kernel.
+bool use_gemv_sm(const w12_info &info, int sm_count) {
+    const char *v = std::getenv("W12_GEMV_SM");
+    if (v != nullptr && std::strcmp(v, "0") == 0) return false;
+    if (v != nullptr && std::strcmp(v, "1") == 0) return true;
+    const double density = (double)info.n_escapes / ((double)info.N * (double)info.K);
+    return info.tiles < 2 * (int64_t)sm_count && density <= 2e-4;
+}
+
 // The GEMV shares a single wave's work as stream-K unit ranges unless
 // W12_STREAMK=0 (then fixed split-K as for the tensor-core kernel).
 bool use_stream_k() {
@@ -270,15 +307,17 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     int rc = device_state(&s, err);
     if (rc != W12_OK) return rc;
     plan->gemv = !q8 && use_gemv(M);
+    plan->gemv_sm = plan->gemv && use_gemv_sm(info, s->sm_count);
     plan->ntok = plan->gemv ? M : tc_token_tile(M, info.tiles, s->sm_count);
-    const int occ = plan->gemv ? s->gemv_occupancy[M - 1]
-                    : q8       ? s->q8_occupancy[plan->ntok == 32]
-                               : s->occupancy[plan->ntok == 32][use_smem_a_operand()];
+    const int occ = plan->gemv_sm ? s->gemv_sm_occupancy[M - 1]
+                    : plan->gemv  ? s->gemv_occupancy[M - 1]
+                    : q8          ? s->q8_occupancy[plan->ntok == 32]
+                                  : s->occupancy[plan->ntok == 32][use_smem_a_operand()];
     if (occ < 1) {
         *err = "GEMM kernel cannot be resident on this device";
         return W12_ERR_CUDA;
     }
-    constexpr int64_t kMaxSegs = dev::GemmCfg<16, kStages, false>::kMaxSegs;
+    const int64_t kMaxSegs = plan->gemv_sm ? dev::GemvSmCfg<1>::kMaxSegs : dev::GemmCfg<16, kStages, false>::kMaxSegs;
     const int64_t capacity = (int64_t)s->sm_count * occ;
     const int64_t tiles = info.tiles, segs = info.segs;
     const char *forced = std::getenv("W12_SPLITS");  // tuning override: fixed split-K
@@ -287,10 +326,15 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     // because the tile count does not divide the resident CTA count
     const int64_t units = tiles * segs;
     int64_t sk_ctas = capacity < units ? capacity : units;
-    if ((units + sk_ctas - 1) / sk_ctas > kMaxSegs) sk_ctas = (units + kMaxSegs - 1) / kMaxSegs;
+    // the range of a CTA: at most kMaxSegs segment headers and, for the
+    // one-CTA-per-SM kernel, at most kMaxPieces tiles; for the two-CTA kernel
+    // at most two tiles (a single wave of more CTAs than tiles)
+    const int64_t max_range = plan->gemv_sm ? std::min<int64_t>(kMaxSegs, (dev::GemvSmCfg<1>::kMaxPieces - 1) * segs + 1)
+                                            : kMaxSegs;
+    if ((units + sk_ctas - 1) / sk_ctas > max_range) sk_ctas = (units + max_range - 1) / max_range;
+    const bool sk_shape = plan->gemv_sm || tiles < capacity;
     // (the device computes unit x ctas products in 32 bits)
-    if (plan->gemv && forced == nullptr && tiles < capacity && units * sk_ctas < (int64_t(1) << 31) &&
-        use_stream_k()) {
+    if (plan->gemv && forced == nullptr && sk_shape && units * sk_ctas < (int64_t(1) << 31) && use_stream_k()) {
         const int64_t shortest = units / sk_ctas;  // units of the shortest range
         plan->units = units;
         // most ranges one tile can meet: the one holding its first unit plus
@@ -398,6 +442,7 @@ w12_info group_info(int count, const w12_info *infos) {
         g.tiles += infos[i].tiles;
         g.N_pad += infos[i].N_pad;
         g.N += infos[i].N;
+        g.n_escapes += infos[i].n_escapes;
     }
     return g;
 }
@@ -561,7 +606,13 @@ int gemm_impl(const uint16_t *x_dev, int count, const void *const *blobs, const 
     const bool asmem = use_smem_a_operand();
     if (plan.gemv) {
         const dim3 grid = plan.units > 0 ? dim3((unsigned)plan.ctas, 1u) : dim3((unsigned)plan.splits, (unsigned)info.tiles);
-        if (plan.ntok == 1)
+        if (plan.gemv_sm && plan.ntok == 1)
+            e = launch_overlapped(dev::w12_gemv_sm_kernel<1>, grid, dim3(dev::GemvSmCfg<1>::kThreads),
+                                  (size_t)dev::GemvSmCfg<1>::kSmemBytes, st, p, tm);
+        else if (plan.gemv_sm)
+            e = launch_overlapped(dev::w12_gemv_sm_kernel<2>, grid, dim3(dev::GemvSmCfg<2>::kThreads),
+                                  (size_t)dev::GemvSmCfg<2>::kSmemBytes, st, p, tm);
+        else if (plan.ntok == 1)
             e = launch_overlapped(dev::w12_gemv_kernel<kGemvStages, kGemvChunks, 1>, grid, dim3(GemvC<1>::kThreads),
                                   (size_t)GemvC<1>::kSmemBytes, st, p, tm);
         else

@@ -431,36 +431,25 @@ __device__ __forceinline__ void patch_half(uint32_t f0, uint32_t f1, const uint8
     }
 }
 
-// Escape step for half h of a quarter-chunk, before the exponent lookup.  The
-// escape run orders a row's 32 columns together, so the lane prefix is taken
-// over whole-row counts and the second half starts after the row's first-half
-// escapes.  Common case: no lane holds more than one escape in its 16 columns.
-// Then a lane with one escape puts that exponent into slot 15 of its own copy
-// of the table, and the ordinary lookup decodes it.  Slot 15 is looked up as
-// sign(slot 7) ^ slot 15, and slot 7 as slot 7 ^ sign(slot 15), so this holds
-// when the escaped exponent has the same top bit as T[7], or when the lane has
-// no code 7 to get wrong.  Otherwise the exponents are patched after the
-// lookup.  Returns the warp's escape count
-// over the whole chunk (to advance the run).
-__device__ __forceinline__ uint32_t decode_exponents_half_esc(const Table &T, const uint4 &codes, int h,
-                                                             const uint8_t *run, uint32_t (&E)[4]) {
-    const uint32_t f[4] = {escape_flags(codes.x), escape_flags(codes.y), escape_flags(codes.z),
-                           escape_flags(codes.w)};
-    const uint32_t c0 = __popc(f[0]) + __popc(f[1]);
-    const uint32_t cnt = c0 + __popc(f[2]) + __popc(f[3]);
-    uint32_t excl, total;
-    lane_prefix(cnt, excl, total);
-    const uint32_t fh0 = h ? f[2] : f[0], fh1 = h ? f[3] : f[1];
+// Escape step for 16 columns of a quarter-chunk row, before the exponent
+// lookup: w0, w1 are their code words, fh0, fh1 their escape flags and src
+// their first escape byte.  Common case: no lane holds more than one escape in
+// its 16 columns.  Then a lane with one escape puts that exponent into slot 15
+// of its own copy of the table, and the ordinary lookup decodes it.  Slot 15
+// is looked up as sign(slot 7) ^ slot 15, and slot 7 as slot 7 ^ sign(slot
+// 15), so this holds when the escaped exponent has the same top bit as T[7],
+// or when the lane has no code 7 to get wrong.  Otherwise the exponents are
+// patched after the lookup.  Warp-uniform control flow.
+__device__ __forceinline__ void decode_exponents_16_esc(const Table &T, uint32_t w0, uint32_t w1, uint32_t fh0,
+                                                        uint32_t fh1, const uint8_t *src, uint32_t (&E)[4]) {
     const uint32_t mine = __popc(fh0) + __popc(fh1);
-    const uint8_t *src = run + excl + (h ? c0 : 0u);
     Table Tl = T;
-    const uint32_t w0 = h ? codes.z : codes.x, w1 = h ? codes.w : codes.y;
     bool ok = mine <= 1u;
     if (mine == 1u) {
         const uint32_t e = *src;
         const uint32_t sign7 = (T.u1 & 0x80000000u) ? 0xFFu : 0u;  // top bit of slot 7
         // a top-bit mismatch only breaks code 7, which is harmless when none of
-        // this lane's 16 codes is 7 (code ^ 8 == 15)
+        // these 16 codes is 7 (code ^ 8 == 15)
         const bool no_code7 = (escape_flags(w0 ^ 0x88888888u) | escape_flags(w1 ^ 0x88888888u)) == 0u;
         ok = ((e ^ sign7) & 0x80u) == 0u || no_code7;
         Tl.u3 = (T.u3 & 0x00FFFFFFu) | ((e ^ sign7) << 24);
@@ -471,6 +460,38 @@ __device__ __forceinline__ uint32_t decode_exponents_half_esc(const Table &T, co
         decode_exponents_half(T, w0, w1, E);
         patch_half(fh0, fh1, src, E);
     }
+}
+
+// Half h of a quarter-chunk with escapes.  The escape run orders a row's 32
+// columns together, so the lane prefix is taken over whole-row counts and the
+// second half starts after the row's first-half escapes.  Returns the warp's
+// escape count over the whole chunk (to advance the run).
+__device__ __forceinline__ uint32_t decode_exponents_half_esc(const Table &T, const uint4 &codes, int h,
+                                                             const uint8_t *run, uint32_t (&E)[4]) {
+    const uint32_t f[4] = {escape_flags(codes.x), escape_flags(codes.y), escape_flags(codes.z),
+                           escape_flags(codes.w)};
+    const uint32_t c0 = __popc(f[0]) + __popc(f[1]);
+    const uint32_t cnt = c0 + __popc(f[2]) + __popc(f[3]);
+    uint32_t excl, total;
+    lane_prefix(cnt, excl, total);
+    decode_exponents_16_esc(T, h ? codes.z : codes.x, h ? codes.w : codes.y, h ? f[2] : f[0], h ? f[3] : f[1],
+                            run + excl + (h ? c0 : 0u), E);
+    return total;
+}
+
+// Both halves of a quarter-chunk with escapes, sharing one lane prefix.
+// Returns the warp's escape count over the chunk.
+__device__ __forceinline__ uint32_t decode_exponents_chunk_esc(const Table &T, const uint4 &codes,
+                                                              const uint8_t *run, uint32_t (&E0)[4],
+                                                              uint32_t (&E1)[4]) {
+    const uint32_t f[4] = {escape_flags(codes.x), escape_flags(codes.y), escape_flags(codes.z),
+                           escape_flags(codes.w)};
+    const uint32_t c0 = __popc(f[0]) + __popc(f[1]);
+    const uint32_t cnt = c0 + __popc(f[2]) + __popc(f[3]);
+    uint32_t excl, total;
+    lane_prefix(cnt, excl, total);
+    decode_exponents_16_esc(T, codes.x, codes.y, f[0], f[1], run + excl, E0);
+    decode_exponents_16_esc(T, codes.z, codes.w, f[2], f[3], run + excl + c0, E1);
     return total;
 }
 

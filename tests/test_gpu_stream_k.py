@@ -21,16 +21,21 @@ def built():
     ensure_built()
 
 
-def _capacity(M):
+def _capacity(plan):
     import torch
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # two GEMV CTAs are resident per SM (288 threads, ~107 KB shared memory)
-    return 2 * sms
+    return torch.cuda.get_device_properties(0).multi_processor_count * plan["ctas_per_sm"]
+
+
+@pytest.fixture(params=["1", "0"], ids=["cta_per_sm", "two_ctas_per_sm"])
+def gemv_kernel(request, monkeypatch):
+    """Both CUDA-core kernels, whichever the planner would pick."""
+    monkeypatch.setenv("W12_GEMV_SM", request.param)
+    return request.param
 
 
 @pytest.mark.parametrize("M", [1, 2])
 @pytest.mark.parametrize("shape", [(12763, 5020), (5000, 17408), (1000, 3000)])
-def test_stream_k_matches_oracle(M, shape, monkeypatch):
+def test_stream_k_matches_oracle(M, shape, gemv_kernel, monkeypatch):
     import torch
     from gpu_util import check_tolerance, dev_to_bits, to_dev_bf16
     n, k = shape
@@ -43,7 +48,7 @@ def test_stream_k_matches_oracle(M, shape, monkeypatch):
         plan = w12.w12_gemm_launch_info(mat.info, M)
         tiles, segs = int(mat.info.tiles), int(mat.info.segs)
         if mode == "1":
-            assert plan["ctas"] == min(_capacity(M), tiles * segs), plan
+            assert plan["ctas"] == min(_capacity(plan), tiles * segs), plan
         else:
             assert plan["ctas"] == tiles * plan["splits"], plan
         y = dev_to_bits(mat.gemm(to_dev_bf16(x)))
@@ -53,7 +58,7 @@ def test_stream_k_matches_oracle(M, shape, monkeypatch):
 
 
 @pytest.mark.parametrize("M", [1, 2])
-def test_stream_k_crosses_group_members(M):
+def test_stream_k_crosses_group_members(M, gemv_kernel):
     """q/k/v-like group whose ranges end inside one member and start in the next."""
     import torch
     from gpu_util import check_tolerance, dev_to_bits, to_dev_bf16
@@ -62,7 +67,7 @@ def test_stream_k_crosses_group_members(M):
     ws = [wl.heavy_tail_weights(n, kk, seed=310 + i) for i, (n, kk) in enumerate(shapes)]
     mats = [W12Weight(w) for w in ws]
     units = sum(int(m.info.tiles) for m in mats) * int(mats[0].info.segs)
-    assert units > _capacity(M)  # more than one unit per CTA, so ranges cross tiles
+    assert units > _capacity(w12.w12_gemm_launch_info(mats[0].info, M))  # ranges cross tiles
     x = wl.activations(M, k, seed=315 + M)
     ys = W12Group(mats).gemm(to_dev_bf16(x))
     w12.w12_check_status()
@@ -71,7 +76,7 @@ def test_stream_k_crosses_group_members(M):
         check_tolerance(dev_to_bits(y), oracle.gemm_f64(x, w), f"member {i} M={M}")
 
 
-def test_stream_k_reproducible_and_counters_reset():
+def test_stream_k_reproducible_and_counters_reset(gemv_kernel):
     import torch
     from gpu_util import dev_to_bits, to_dev_bf16
     w = wl.gaussian_weights(9000, 5120, seed=320)
