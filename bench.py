@@ -32,6 +32,7 @@ METRIC = "W12 decode-GEMM effective weight GB/s & µs/layer at M=1–32; % of HB
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("lossless_bit_weight_encode_gb300/csrc/gemm_tc.cuh",
                   "lossless_bit_weight_encode_gb300/csrc/gemv.cuh",
+                  "lossless_bit_weight_encode_gb300/csrc/gemv_sm.cuh",
                   "lossless_bit_weight_encode_gb300/csrc/w12_device.cuh",
                   "lossless_bit_weight_encode_gb300/csrc/kernels.cu")
 
@@ -438,8 +439,10 @@ def run_w12(args):
     w12.w12_check_status()
     launch_ms = [statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(kp)) for i in range(nl)]
 
+    plan0 = w12.w12_gemm_launch_info(mats[0].info, M)
     kernel_name = "w12_gemm_tc_kernel (Q8 copy)" if args.weights == "q8" else \
-        "w12_gemv_kernel" if w12.w12_gemm_launch_info(mats[0].info, M).get("ntok") <= 4 else "w12_gemm_tc_kernel"
+        "w12_gemm_tc_kernel" if plan0.get("ntok") > 4 else \
+        "w12_gemv_sm_kernel" if plan0.get("ctas_per_sm") == 1 else "w12_gemv_kernel"
     layer_weights = sum(m.N * m.K for m in mats)
     packed = sum(int(m.info.total_bytes) for m in mats)
     alg = [sum(int(mats[i].info.total_bytes) + 2 * M * mats[i].N for i in g) + 2 * M * mats[g[0]].K
