@@ -324,7 +324,17 @@ def run_w12(args):
         names = [n for n, _ in weights]
         mats = [Q8Weight(w) if args.weights == "q8" else W12Weight(w) for _, w in weights]
         xs_host = [wl.activations(M, w.shape[1], seed=wl.activation_seed(args.workload, M)) for _, w in weights]
-        xs = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs_host]
+        # every matrix's x in one device buffer (256-byte aligned slices), so
+        # that the end-to-end run brings a step's inputs in with one copy
+        offs, tot = [], 0
+        for x in xs_host:
+            offs.append(tot)
+            tot += (x.size + 127) // 128 * 128
+        xpack_host = np.zeros(tot, dtype=np.uint16)
+        for o, x in zip(offs, xs_host):
+            xpack_host[o:o + x.size] = x.ravel()
+        xpack = torch.from_numpy(xpack_host.view(np.int16)).cuda().view(torch.bfloat16)
+        xs = [xpack[o:o + x.size].view(x.shape) for o, x in zip(offs, xs_host)]
         wss = [m.workspace(M) for m in mats]
 
         def dense_weights():
@@ -333,7 +343,10 @@ def run_w12(args):
 
         def cpu_weights():
             return weights
-    ys = [torch.empty((M, m.N), dtype=torch.bfloat16, device="cuda") for m in mats]
+    # all outputs in one device buffer: one copy brings a step's results back
+    ypack = torch.empty(sum(M * m.N for m in mats), dtype=torch.bfloat16, device="cuda")
+    yoffs = np.cumsum([0] + [M * m.N for m in mats])
+    ys = [ypack[yoffs[i]:yoffs[i + 1]].view(M, m.N) for i, m in enumerate(mats)]
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     argmax = args.workload == "lmhead"
@@ -489,10 +502,23 @@ def run_w12(args):
     if not args.no_e2e:
         xh = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs_host]
         yh = [torch.empty((M, m.N), dtype=torch.bfloat16).pin_memory() for m in mats]
+        packed = args.workload != "model64" and not argmax
+        if packed:
+            xpack_h = torch.from_numpy(xpack_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+            ypack_h = torch.empty(ypack.numel(), dtype=torch.bfloat16).pin_memory()
         if argmax:
             idx_h = torch.empty(M, dtype=torch.int32).pin_memory()
 
         def estep():
+            if packed:
+                # the step's inputs in, its launches, its outputs out: one copy each way
+                xpack.copy_(xpack_h, non_blocking=True)
+                for fn, c in calls:
+                    rc = fn(*c)
+                    if rc != 0:
+                        raise w12.W12Error(rc, w12.w12_last_error())
+                ypack_h.copy_(ypack, non_blocking=True)
+                return
             # x comes in once per launch (the members of a group share it)
             for (fn, c), g in zip(calls, groups):
                 xs[g[0]].copy_(xh[g[0]], non_blocking=True)
@@ -522,7 +548,7 @@ def run_w12(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e_ms = float(t.item())
         e2e = {"value": round(world * 2.0 * layer_weights / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": int(sum(2 * M * mats[g[0]].K for g in groups)),
+               "h2d_bytes_per_step": int(2 * xpack_h.numel()) if packed else int(sum(2 * M * mats[g[0]].K for g in groups)),
                "d2h_bytes_per_step": int(4 * M) if argmax else int(sum(2 * M * m.N for m in mats)),
                "ms_per_step": round(e_ms, 5)}
 
