@@ -90,3 +90,21 @@ def test_stream_k_reproducible_and_counters_reset(gemv_kernel):
     for _ in range(3):
         assert np.array_equal(dev_to_bits(mat.gemm(x)), y1)
     w12.w12_check_status()
+
+
+def test_kernel_choice(monkeypatch):
+    """One CTA per SM for few tiles with rare escapes; two per SM for
+    escape-heavy weights and for launches with two or more tiles per SM."""
+    import torch
+    monkeypatch.delenv("W12_GEMV_SM", raising=False)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    gauss = W12Weight(wl.gaussian_weights(2048, 1024, seed=330))
+    heavy = W12Weight(wl.heavy_tail_weights(2048, 1024, seed=331))
+    many = W12Weight(wl.gaussian_weights(2 * sms * 128, 256, seed=332))
+    assert gauss.info.n_escapes / (2048 * 1024) <= 2e-4 < heavy.info.n_escapes / (2048 * 1024)
+    for M in (1, 2):
+        assert w12.w12_gemm_launch_info(gauss.info, M)["ctas_per_sm"] == 1
+        assert w12.w12_gemm_launch_info(heavy.info, M)["ctas_per_sm"] == 2
+        assert w12.w12_gemm_launch_info(many.info, M)["ctas_per_sm"] == 2
+    monkeypatch.setenv("W12_GEMV_SM", "1")
+    assert w12.w12_gemm_launch_info(heavy.info, 1)["ctas_per_sm"] == 1
