@@ -502,15 +502,15 @@ def run_w12(args):
     if not args.no_e2e:
         xh = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs_host]
         yh = [torch.empty((M, m.N), dtype=torch.bfloat16).pin_memory() for m in mats]
-        packed = args.workload != "model64" and not argmax
-        if packed:
+        one_copy = args.workload != "model64" and not argmax
+        if one_copy:
             xpack_h = torch.from_numpy(xpack_host.view(np.int16)).view(torch.bfloat16).pin_memory()
             ypack_h = torch.empty(ypack.numel(), dtype=torch.bfloat16).pin_memory()
         if argmax:
             idx_h = torch.empty(M, dtype=torch.int32).pin_memory()
 
         def estep():
-            if packed:
+            if one_copy:
                 # the step's inputs in, its launches, its outputs out: one copy each way
                 xpack.copy_(xpack_h, non_blocking=True)
                 for fn, c in calls:
@@ -548,7 +548,7 @@ def run_w12(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e_ms = float(t.item())
         e2e = {"value": round(world * 2.0 * layer_weights / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": int(2 * xpack_h.numel()) if packed else int(sum(2 * M * mats[g[0]].K for g in groups)),
+               "h2d_bytes_per_step": int(2 * xpack_h.numel()) if one_copy else int(sum(2 * M * mats[g[0]].K for g in groups)),
                "d2h_bytes_per_step": int(4 * M) if argmax else int(sum(2 * M * m.N for m in mats)),
                "ms_per_step": round(e_ms, 5)}
 
