@@ -452,10 +452,12 @@ def run_w12(args):
     w12.w12_check_status()
     launch_ms = [statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(kp)) for i in range(nl)]
 
-    plan0 = w12.w12_gemm_launch_info(mats[0].info, M)
-    kernel_name = "w12_gemm_tc_kernel (Q8 copy)" if args.weights == "q8" else \
-        "w12_gemm_tc_kernel" if plan0.get("ntok") > 4 else \
-        "w12_gemv_sm_kernel" if plan0.get("ctas_per_sm") == 1 else "w12_gemv_kernel"
+    if args.weights == "q8":
+        kernel_name = "w12_gemm_tc_kernel (Q8 copy)"
+    else:
+        plan0 = w12.w12_gemm_launch_info(mats[0].info, M)
+        kernel_name = "w12_gemm_tc_kernel" if plan0.get("ntok") > 4 else \
+            "w12_gemv_sm_kernel" if plan0.get("ctas_per_sm") == 1 else "w12_gemv_kernel"
     layer_weights = sum(m.N * m.K for m in mats)
     packed = sum(int(m.info.total_bytes) for m in mats)
     alg = [sum(int(mats[i].info.total_bytes) + 2 * M * mats[i].N for i in g) + 2 * M * mats[g[0]].K

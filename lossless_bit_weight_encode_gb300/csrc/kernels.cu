@@ -132,11 +132,14 @@ int prepare_gemm(DeviceState &s, std::string *err) {
     const int rc = resident_ctas(k, dev::GemmCfg<NTOK, kStages, ASMEM, Q8>::kThreads,
                                  gemm_smem_bytes<NTOK, ASMEM, Q8>(), s.device, err, &occ);
     if (rc != W12_OK) return rc;
-    // TMEM: each CTA holds 128 of the SM's 512 columns
+    // TMEM: a 16-token CTA holds 128 of the SM's 512 columns, a 32-token CTA
+    // 256; no more CTAs may be resident than their columns allow
+    constexpr int kTmemCap = 512 / dev::GemmCfg<NTOK, kStages, ASMEM, Q8>::kTmemCols;
+    if (occ > kTmemCap) occ = kTmemCap;
     if (Q8)
-        s.q8_occupancy[NTOK == 32] = occ < 4 ? occ : 4;
+        s.q8_occupancy[NTOK == 32] = occ;
     else
-        s.occupancy[NTOK == 32][ASMEM] = occ < 4 ? occ : 4;
+        s.occupancy[NTOK == 32][ASMEM] = occ;
     return W12_OK;
 }
 
