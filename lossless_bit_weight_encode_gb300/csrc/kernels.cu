@@ -254,19 +254,19 @@ bool use_smem_a_operand() {
 // Which CUDA-core kernel: one CTA per SM with sixteen decode warps (gemv_sm.cuh)
 // or two with eight each (gemv.cuh).  The first keeps every warp of an SM busy
 // to the end of a single wave; it pays for finding where its chunks' escapes
-// start, and its long stream-K ranges cost more than the second's extra waves
-// once the tiles fill two CTAs per SM.  Measured (layer step, M = 1 / 2):
-// 114.6 / 129.3 us against 117.3 / 136.0; heavy-tail weights (0.4 % escapes)
-// 194 against 174 us; the LM head 212 against 207 us.  So: one CTA per SM
-// when the tiles are fewer than two per SM and escapes are rare enough that
-// at most ~20 % of quarter-chunks (32 x 32 weights) hold one.  W12_GEMV_SM=0 or
-// 1 forces a kernel.
+// start.  Measured (one GPU, back to back): layer step at M = 1 / 2 110.1 /
+// 124.6 us against 115.7 / 134.2; the LM head 199.0 against 209.1 us; but
+// heavy-tail weights (0.4 % escapes) 180.6 against 174.3 us.  So: one CTA per
+// SM when at most ~20 % of quarter-chunks (32 x 32 weights) hold an escape
+// (2e-4 of the weights; N(0, 0.02) weights: 1.4e-4) and one wave of SM-long
+// ranges covers the launch.  W12_GEMV_SM=0 or 1 forces a kernel.
 bool use_gemv_sm(const w12_info &info, int sm_count) {
     const char *v = std::getenv("W12_GEMV_SM");
     if (v != nullptr && std::strcmp(v, "0") == 0) return false;
     if (v != nullptr && std::strcmp(v, "1") == 0) return true;
     const double density = (double)info.n_escapes / ((double)info.N * (double)info.K);
-    return info.tiles < 2 * (int64_t)sm_count && density <= 2e-4;
+    const int64_t units = info.tiles * info.segs;
+    return density <= 2e-4 && (units + sm_count - 1) / sm_count <= dev::GemvSmCfg<1>::kMaxSegs;
 }
 
 // The GEMV shares a single wave's work as stream-K unit ranges unless
