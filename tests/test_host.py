@@ -162,3 +162,43 @@ def test_q8_rejects_bad_input():
     with pytest.raises(w12.W12Error) as ei:
         w12.w12_q8_blob_info(oracle.encode(wl.gaussian_weights(10, 10, seed=26)))  # a W12 blob
     assert ei.value.status == 5
+
+
+def test_gemm_argument_errors_before_any_device_work():
+    """The GEMM entry points reject bad arguments with the documented codes
+    before they touch a device (the pointers below are never dereferenced)."""
+    import ctypes
+    lib = w12.lib()
+    a = 0x100000  # a 256-byte aligned stand-in for a device pointer
+    info = w12.w12_blob_info(w12.w12_encode_host(wl.gaussian_weights(200, 300, seed=40)))
+    other_k = w12.w12_blob_info(w12.w12_encode_host(wl.gaussian_weights(130, 64, seed=41)))
+    INVALID, SHAPE, ALIGN = 1, 2, 4
+    # w12_gemm: null pointers, token count, alignment
+    assert w12.w12_gemm_ptr(0, a, info, a, 1, a, 1 << 20, None) == INVALID
+    assert w12.w12_gemm_ptr(a, a, info, a, 0, a, 1 << 20, None) == INVALID
+    assert w12.w12_gemm_ptr(a, a, info, a, 33, a, 1 << 20, None) == INVALID
+    assert w12.w12_gemm_ptr(a, a + 16, info, a, 1, a, 1 << 20, None) == ALIGN
+    assert w12.w12_gemm_ptr(a, a, info, a + 1, 1, a, 1 << 20, None) == ALIGN
+    assert w12.w12_gemm_ptr(a, a, info, a, 1, a + 128, 1 << 20, None) == ALIGN
+    out = (ctypes.c_int32 * 4)()
+    assert lib.w12_gemm_launch_info(ctypes.byref(info), 0, out) == INVALID
+    assert lib.w12_gemm_launch_info(ctypes.byref(info), 33, out) == INVALID
+    # grouped launch: member count, shared K, null and misaligned members
+    assert w12.w12_gemm_group_ptr(a, [], [], [], 1, a, 1 << 20, None) == INVALID
+    five = [info] * (w12.MAX_GROUP + 1)
+    assert w12.w12_gemm_group_ptr(a, [a] * 5, five, [a] * 5, 1, a, 1 << 20, None) == INVALID
+    assert w12.w12_gemm_group_ptr(a, [a, a], [info, other_k], [a, a], 1, a, 1 << 20, None) == SHAPE
+    assert w12.w12_gemm_group_ptr(a, [a, 0], [info, info], [a, a], 1, a, 1 << 20, None) == INVALID
+    assert w12.w12_gemm_group_ptr(a, [a, a], [info, info], [a, a + 1], 1, a, 1 << 20, None) == ALIGN
+    assert w12.w12_gemm_group_ptr(a, [a, a], [info, info], [a, a], 40, a, 1 << 20, None) == INVALID
+    # fused argmax: index and value outputs are required and 4-byte aligned
+    assert w12.w12_gemm_argmax_ptr(a, a, info, 1, None, 0, a, a, 1 << 20, None) == INVALID
+    assert w12.w12_gemm_argmax_ptr(a, a, info, 1, None, a + 2, a, a, 1 << 20, None) == ALIGN
+    # allocation-free entry point
+    assert lib.w12_gemm_noalloc(a, a, ctypes.byref(info), None, 1, None) == INVALID
+    assert lib.w12_gemm_noalloc(a, a, ctypes.byref(info), a, 0, None) == INVALID
+    # Q8 copy
+    q8 = w12.w12_q8_blob_info(w12.w12_q8_encode_host(wl.gaussian_weights(200, 300, seed=42)))
+    assert w12.w12_q8_gemm_ptr(0, a, q8, a, 1, a, 1 << 20, None) == INVALID
+    assert w12.w12_q8_gemm_ptr(a, a + 8, q8, a, 1, a, 1 << 20, None) == ALIGN
+    assert w12.w12_last_error() != ""
