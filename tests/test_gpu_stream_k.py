@@ -110,3 +110,22 @@ def test_kernel_choice(monkeypatch):
         assert plan["ctas_per_sm"] == 1 and plan["ctas"] == sms
     monkeypatch.setenv("W12_GEMV_SM", "1")
     assert w12.w12_gemm_launch_info(heavy.info, 1)["ctas_per_sm"] == 1
+
+
+@pytest.mark.parametrize("case", range(10))
+def test_stream_k_random_shapes(case, gemv_kernel):
+    """Seeded random shapes (ragged N and K, one to ~120 segments per row
+    tile, one or two tokens) against the oracle, on both CUDA-core kernels."""
+    import torch
+    from gpu_util import check_tolerance, dev_to_bits, to_dev_bf16
+    rng = np.random.default_rng(1000 + case)
+    k = int(rng.integers(1, 30000))
+    n = int(rng.integers(1, max(2, min(9000, 40_000_000 // k))))
+    M = int(rng.integers(1, 3))
+    gen = wl.heavy_tail_weights if case % 3 == 0 else wl.gaussian_weights
+    w = gen(n, k, seed=1100 + case)
+    x = wl.activations(M, k, seed=1200 + case)
+    y = dev_to_bits(W12Weight(w).gemm(to_dev_bf16(x)))
+    w12.w12_check_status()
+    torch.cuda.synchronize()
+    check_tolerance(y, oracle.gemm_f64(x, w), f"case {case}: {n}x{k} M={M}")
