@@ -264,6 +264,24 @@ def emit(line, args):
             f.write(s + "\n")
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of `value` over the ranks of the default process group (the
+    job takes as long as its slowest replica); `value` itself without one."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_weight_gbs(weights_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job BF16-equivalent weight GB/s: every replica streams the same
+    weights once per step, so the job moves world x 2 bytes per weight."""
+    return world * 2.0 * weights_per_rank / (ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_w12(args):
     import torch
@@ -430,10 +448,7 @@ def run_w12(args):
     barrier()
     ms_total = ev0.elapsed_time(ev1)
     w12.w12_check_status()
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, "cuda")
     ms_step = ms_total / K
 
     # per-launch durations of the GEMM kernel (events around every launch)
@@ -462,7 +477,7 @@ def run_w12(args):
     packed = sum(int(m.info.total_bytes) for m in mats)
     alg = [sum(int(mats[i].info.total_bytes) + 2 * M * mats[i].N for i in g) + 2 * M * mats[g[0]].K
            for g in groups]  # per launch: its blobs, one x, its outputs
-    value = world * 2.0 * layer_weights / (ms_step * 1e-3) / 1e9
+    value = job_weight_gbs(layer_weights, world, ms_step)
     peak, peak_kind = hbm_peak_gbs()
     achieved = sum(alg) / (sum(launch_ms) * 1e-3) / 1e9
     traffic_rec = recorded_traffic()
@@ -544,12 +559,8 @@ def run_w12(args):
         e1.record()
         e1.synchronize()
         w12.w12_check_status()
-        e_ms = e0.elapsed_time(e1) / ke
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": round(world * 2.0 * layer_weights / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, "cuda")
+        e2e = {"value": round(job_weight_gbs(layer_weights, world, e_ms), 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(2 * xpack_h.numel()) if one_copy else int(sum(2 * M * mats[g[0]].K for g in groups)),
                "d2h_bytes_per_step": int(4 * M) if argmax else int(sum(2 * M * m.N for m in mats)),
                "ms_per_step": round(e_ms, 5)}
