@@ -129,3 +129,21 @@ def test_stream_k_random_shapes(case, gemv_kernel):
     w12.w12_check_status()
     torch.cuda.synchronize()
     check_tolerance(y, oracle.gemm_f64(x, w), f"case {case}: {n}x{k} M={M}")
+
+
+@pytest.mark.parametrize("frac", [0.02, 0.10, 1.0])
+@pytest.mark.parametrize("M", [1, 2])
+def test_forced_escapes_on_both_kernels(frac, M, gemv_kernel):
+    """2 %, 10 % and 100 % escapes: staged and unstaged escape runs, lanes
+    with several escapes, and (one CTA per SM) the counts of earlier chunks."""
+    import torch
+    from gpu_util import check_tolerance, dev_to_bits, to_dev_bf16
+    w = wl.forced_escape_weights(640, 4096 + 96, frac, seed=int(frac * 1000) + 10 * M)
+    # huge exponents overflow the sum; keep the weights finite and moderate
+    e = (w >> 7) & 0xFF
+    w = np.where((e > 140) | (e == 255), (w & 0x807F) | np.uint16(130 << 7), w).astype(np.uint16)
+    x = wl.activations(M, w.shape[1], seed=1300 + M)
+    y = dev_to_bits(W12Weight(w).gemm(to_dev_bf16(x)))
+    w12.w12_check_status()
+    torch.cuda.synchronize()
+    check_tolerance(y, oracle.gemm_f64(x, w), f"{frac:.0%} escapes M={M}")
