@@ -9,9 +9,11 @@ an agent doubled speculative decoding speed, and the 10.87x needs context" §The
 mechanisms it found).
 
 Parity status: encode/decode and the fp64 GEMM are pinned by the CPU tests
-(exhaustive BF16 round trip, a hand-worked 2x2 blob, table-optimality and
+(exhaustive BF16 round trip, a hand-worked 2x2 blob, a hand-worked blob whose
+escape bytes and segment headers are listed by hand, table-optimality and
 escape-mass invariants, size closed form, normal-CDF escape rate, numpy
-float64 matmul, one-hot and small-integer exact products).
+float64 matmul, one-hot and small-integer exact products); the Q8 copy and
+its fp64 product by hand-worked rows and products.
 """
 from __future__ import annotations
 

@@ -24,11 +24,15 @@
  * Pins (tests that tie this file to something other than itself):
  *   encode/decode : exhaustive round trip of all 65536 BF16 patterns (the
  *                   "lossless"/"bit-exactly" property), a hand-worked 2x2
- *                   example, table-optimality and escape-mass invariants, the
+ *                   example, a hand-worked blob with five escapes over two
+ *                   quarters, two chunks and two segments (escape bytes,
+ *                   bases, counts and masks listed by hand),
+ *                   table-optimality and escape-mass invariants, the
  *                   size closed form, normal-CDF escape rate on Gaussian data.
  *   gemm_f64      : numpy float64 matmul, one-hot and small-integer exact cases.
  *   q8 encode     : a hand-worked row, the scale/range invariants, the
  *                   half-step rounding bound, ties to even.
+ *   q8 product    : one-hot and small-integer products worked by hand.
  */
 #ifndef W12_ORACLE_H
 #define W12_ORACLE_H

@@ -326,3 +326,76 @@ def test_q8_invariants_and_layout():
     with pytest.raises(ValueError):
         oracle.q8_encode(bad)
     del rng
+
+
+def test_q8_gemm_hand_worked_products():
+    """oracle.q8_gemm_f64 against products worked by hand.  Row 0 has maximum
+    127/64, so its scale is exactly 1/64 and q = [127, 32, 34, -32, 0, -127,
+    0, 2] (as in the row above); row 1 has maximum 127/32 (scale 1/32) and
+    values 1/32, 2.5/32 and 3.5/32, so q = [1, -127, 2, 4, 0, 0, 0, 0] (2.5
+    ties to 2, 3.5 to 4).  A one-hot x picks s[n] q[n, k]; a small-integer x
+    gives sums that are worked out below."""
+    r0 = [127 / 64, 32.5 / 64, 33.5 / 64, -32.5 / 64, 0.0, -127 / 64, 1 / 128, 3 / 128]
+    r1 = [1 / 32, -127 / 32, 2.5 / 32, 3.5 / 32, 0.0, 0.0, 0.0, 0.0]
+    w = wl.to_bf16_bits(np.array([r0, r1], dtype=np.float32))
+    # one-hot x: column k of s q, i.e. q[n, k] / 64 and q[n, k] / 32
+    x = np.zeros((3, 8), dtype=np.uint16)
+    x[0, 1] = x[1, 3] = x[2, 5] = np.uint16(0x3F80)  # 1.0
+    y = oracle.q8_gemm_f64(x, w)
+    assert y.tolist() == [[32 / 64, -127 / 32], [-32 / 64, 4 / 32], [-127 / 64, 0.0]]
+    # x = [1, 2, 0, -1, 3, 1, 5, -2]:
+    #   row 0: 127 + 64 + 0 + 32 + 0 - 127 + 0 - 4 = 92   -> 92 / 64
+    #   row 1: 1 - 254 + 0 - 4 + 0 + 0 + 0 + 0 = -257     -> -257 / 32
+    # x = [-1, 0, 1, 1, 7, 0, 0, 3]:
+    #   row 0: -127 + 0 + 34 - 32 + 0 + 0 + 0 + 6 = -119   -> -119 / 64
+    #   row 1: -1 + 0 + 2 + 4 + 0 + 0 + 0 + 0 = 5          -> 5 / 32
+    xi = np.array([[1, 2, 0, -1, 3, 1, 5, -2], [-1, 0, 1, 1, 7, 0, 0, 3]], dtype=np.float32)
+    y = oracle.q8_gemm_f64(wl.to_bf16_bits(xi), w)
+    assert y.tolist() == [[92 / 64, -257 / 32], [-119 / 64, 5 / 32]]
+
+
+def test_hand_worked_blob_with_escapes():
+    """A 128 x 512 matrix (one tile, two segments) built so that its escapes
+    can be listed by hand.  Each segment holds +0.0 almost everywhere and the
+    fourteen exponents 100..113 twice each, so its table is {0, 100..113} and
+    any other exponent escapes.  The escapes (value 2^(e-127), sign and
+    mantissa 0) are placed so that the quarter -> chunk -> row -> column order
+    differs from plain row-major order:
+      segment 0: e=120 at (5, 3)    quarter 0, chunk 0
+                 e=121 at (33, 40)  quarter 1, chunk 1
+                 e=122 at (60, 5)   quarter 1, chunk 0
+                 e=123 at (60, 1)   quarter 1, chunk 0
+      segment 1: e=124 at (100, 300) quarter 3, chunk 1 of the segment
+    so the escape plane reads 120, 123, 122, 121 | 124."""
+    n, k = 128, 512
+    w = np.zeros((n, k), dtype=np.uint16)
+    for s in range(2):
+        for i in range(14):
+            col = 256 * s + 10 + i
+            w[70 + i, col] = w[90 + i, col] = np.uint16((100 + i) << 7)
+    for (r, c), e in {(5, 3): 120, (33, 40): 121, (60, 5): 122, (60, 1): 123, (100, 300): 124}.items():
+        w[r, c] = np.uint16(e << 7)
+    blob = oracle.encode(w)
+    # geometry: 2 segment headers (64 B, plane padded to 256), 16 chunks
+    assert _hdr(blob, 0x58, 8) == 256 and _hdr(blob, 0x60, 8) == 64
+    assert _hdr(blob, 0x68, 8) == 512 and _hdr(blob, 0x70, 8) == 16 * 6144
+    off_e = 512 + 16 * 6144
+    assert _hdr(blob, 0x78, 8) == off_e and _hdr(blob, 0x80, 8) == 5 and _hdr(blob, 0x88, 8) == 16
+    assert _hdr(blob, 0x90, 8) == blob.size == off_e + 256
+    assert list(blob[off_e:off_e + 16]) == [120, 123, 122, 121, 124] + [0] * 11
+    for s, (base, counts, mask) in enumerate([(0, [1, 3, 0, 0], 0x301), (4, [0, 0, 0, 1], 1 << 25)]):
+        hd = blob[256 + 32 * s:256 + 32 * (s + 1)]
+        assert sorted(int(v) for v in hd[:15]) == sorted([0] + list(range(100, 114))) and hd[15] == 0
+        assert int.from_bytes(bytes(hd[16:20]), "little") == base
+        assert [int.from_bytes(bytes(hd[20 + 2 * q:22 + 2 * q]), "little") for q in range(4)] == counts
+        assert int.from_bytes(bytes(hd[28:32]), "little") == mask
+
+    def code(r, c):
+        chunk = blob[512 + 6144 * (c // 32):512 + 6144 * (c // 32 + 1)]
+        byte = int(chunk[4096 + 16 * r + (c % 32) // 2])
+        return (byte >> 4) if c % 2 else (byte & 15)
+
+    for r, c in [(5, 3), (33, 40), (60, 5), (60, 1), (100, 300)]:
+        assert code(r, c) == 15
+    assert code(70, 10) != 15 and code(0, 0) != 15
+    assert np.array_equal(oracle.decode(blob), w)
