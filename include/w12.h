@@ -328,6 +328,30 @@ int w12_q8_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_q8_info *
 int w12_check_status(void *stream);
 
 /*
+ * Launch options, process-wide (every device and thread sees the same
+ * values).  The library reads no environment variables: a plan changes only
+ * through these calls.  No passage of the pages has a counterpart; they exist
+ * for tuning and for tests that must reach every kernel variant.  Setting an
+ * option while another thread launches is safe but that launch may see the
+ * old or the new value.  Names (default; accepted values):
+ *   gemv_max_m      (2; 0..2)   largest M on the CUDA-core path; 0 sends
+ *                               every M to the tensor cores
+ *   token_tile      (0; 0, 16, 32) tensor-core token tile, 0 = the planner's
+ *   a_operand_smem  (0; 0..1)   1: tensor-core A operand from shared memory
+ *   gemv_sm         (-1; -1..1) CUDA-core kernel: -1 planner, 0 two CTAs per
+ *                               SM, 1 one CTA per SM
+ *   stream_k        (1; 0..1)   0: fixed split-K on the CUDA-core path
+ *   splits          (0; 0..2^20) n > 0: fixed split-K with n splits where the
+ *                               kernel's per-CTA limits allow it
+ *   pdl             (1; 0..1)   programmatic dependent launch on GEMMs
+ *   timeout_ms      (4000; 1..600000) bounded waits give up after this
+ * INVALID_ARG for an unknown name or a value out of range (nothing changes).
+ */
+int w12_set_option(const char *name, int64_t value);
+
+int w12_get_option(const char *name, int64_t *value);
+
+/*
  * Diagnostic: launch one kernel on `stream` that waits on a barrier nothing
  * ever completes, giving up after timeout_us microseconds and recording the
  * timeout in the status word — the same bounded-wait path the GEMM uses, with

@@ -407,6 +407,26 @@ int w12_check_status(void *stream) {
     return guarded([&](std::string &err) { return w12::launch::check_status(stream, &err); });
 }
 
+int w12_set_option(const char *name, int64_t value) {
+    return guarded([&](std::string &err) {
+        if (!name) {
+            err = "name is null";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        return w12::launch::set_option(name, value, &err);
+    });
+}
+
+int w12_get_option(const char *name, int64_t *value) {
+    return guarded([&](std::string &err) {
+        if (!name || !value) {
+            err = "name or value is null";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        return w12::launch::get_option(name, value, &err);
+    });
+}
+
 int w12_selftest_timeout(uint32_t timeout_us, void *stream) {
     return guarded([&](std::string &err) { return w12::launch::selftest_timeout(timeout_us, stream, &err); });
 }

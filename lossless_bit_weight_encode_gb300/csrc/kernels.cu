@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -219,37 +220,56 @@ int device_state(DeviceState **out, std::string *err) {
     return W12_OK;
 }
 
-// One and two tokens run on CUDA cores (W12_GEMV_MAX_M=1 sends two tokens to
-// the tensor cores; four token rows on CUDA cores measured 35 % slower than
-// tcgen05); one token goes to the tensor-core kernel instead when
-// W12_M1_PATH=tc (kept selectable so both stay tested).
-bool use_gemv(int M) {
-    const char *mx = std::getenv("W12_GEMV_MAX_M");  // 1 sends two tokens to the tensor cores
-    const long max_m = mx ? std::strtol(mx, nullptr, 10) : 2;
-    if (M > max_m || M > 2) return false;
-    if (M > 1) return true;
-    const char *v = std::getenv("W12_M1_PATH");
-    return !(v != nullptr && std::strcmp(v, "tc") == 0);
-}
+// Launch options (w12_set_option).  Process-wide, read with relaxed atomics
+// on every call; nothing is taken from the environment.
+struct OptionSlot {
+    const char *name;
+    int64_t def, lo, hi;
+    std::atomic<int64_t> value;
+};
+
+// name, default, smallest and largest accepted value
+OptionSlot g_options[] = {
+    // largest M on the CUDA-core path (0: every M on the tensor cores); four
+    // token rows on CUDA cores measured 35 % slower than tcgen05
+    {"gemv_max_m", 2, 0, 2, {2}},
+    // token tile of the tensor-core kernel: 0 picks (see tc_token_tile)
+    {"token_tile", 0, 0, 32, {0}},
+    // 1: the tensor-core kernel takes its A operand from shared memory
+    {"a_operand_smem", 0, 0, 1, {0}},
+    // CUDA-core kernel: -1 picks, 0 two CTAs per SM, 1 one CTA per SM
+    {"gemv_sm", -1, -1, 1, {-1}},
+    // 0: fixed split-K for the CUDA-core kernel too (no stream-K ranges)
+    {"stream_k", 1, 0, 1, {1}},
+    // 0: the planner picks; n: fixed split-K with n splits where it fits
+    {"splits", 0, 0, 1 << 20, {0}},
+    // 0: launches without programmatic dependent launch
+    {"pdl", 1, 0, 1, {1}},
+    // bounded waits give up after this many milliseconds
+    {"timeout_ms", 4000, 1, 600000, {4000}},
+};
+
+enum OptionId { kOptGemvMaxM, kOptTokenTile, kOptASmem, kOptGemvSm, kOptStreamK, kOptSplits, kOptPdl, kOptTimeout };
+
+int64_t opt(OptionId id) { return g_options[id].value.load(std::memory_order_relaxed); }
+
+// One and two tokens run on CUDA cores unless gemv_max_m says fewer.
+bool use_gemv(int M) { return M <= 2 && M <= opt(kOptGemvMaxM); }
 
 // Token tile of the tensor-core kernel.  32 unless the matrix has enough
 // 128-row tiles for several waves (a 152K-row LM head): two CTAs per SM with
 // the 32-token tile measured 160 us per grouped layer step at M = 4..16
 // against 190 us for three CTAs per SM with the 16-token tile, while the LM
-// head took 268 us with the 16-token tile against 303 us.  W12_NTOK=16 or 32
-// forces one (kept tested).
+// head took 268 us with the 16-token tile against 303 us.  token_tile = 16 or
+// 32 forces one (kept tested); more than 16 tokens always take 32.
 int tc_token_tile(int M, int64_t tiles, int sm_count) {
-    const char *v = std::getenv("W12_NTOK");
-    if (v != nullptr && std::strcmp(v, "32") == 0) return 32;
-    if (M > 16) return 32;
-    if (v != nullptr && std::strcmp(v, "16") == 0) return 16;
+    const int64_t v = opt(kOptTokenTile);
+    if (v == 32 || M > 16) return 32;
+    if (v == 16) return 16;
     return tiles >= 3 * (int64_t)sm_count ? 16 : 32;
 }
 
-bool use_smem_a_operand() {
-    const char *v = std::getenv("W12_A_OPERAND");
-    return v != nullptr && std::strcmp(v, "smem") == 0;
-}
+bool use_smem_a_operand() { return opt(kOptASmem) != 0; }
 
 // Which CUDA-core kernel: one CTA per SM with sixteen decode warps (gemv_sm.cuh)
 // or two with eight each (gemv.cuh).  The first keeps every warp of an SM busy
@@ -259,28 +279,20 @@ bool use_smem_a_operand() {
 // heavy-tail weights (0.4 % escapes) 180.6 against 174.3 us.  So: one CTA per
 // SM when at most ~20 % of quarter-chunks (32 x 32 weights) hold an escape
 // (2e-4 of the weights; N(0, 0.02) weights: 1.4e-4) and one wave of SM-long
-// ranges covers the launch.  W12_GEMV_SM=0 or 1 forces a kernel.
+// ranges covers the launch.  gemv_sm = 0 or 1 forces a kernel.
 bool use_gemv_sm(const w12_info &info, int sm_count) {
-    const char *v = std::getenv("W12_GEMV_SM");
-    if (v != nullptr && std::strcmp(v, "0") == 0) return false;
-    if (v != nullptr && std::strcmp(v, "1") == 0) return true;
+    const int64_t v = opt(kOptGemvSm);
+    if (v >= 0) return v == 1;
     const double density = (double)info.n_escapes / ((double)info.N * (double)info.K);
     const int64_t units = info.tiles * info.segs;
     return density <= 2e-4 && (units + sm_count - 1) / sm_count <= dev::GemvSmCfg<1>::kMaxSegs;
 }
 
 // The GEMV shares a single wave's work as stream-K unit ranges unless
-// W12_STREAMK=0 (then fixed split-K as for the tensor-core kernel).
-bool use_stream_k() {
-    const char *v = std::getenv("W12_STREAMK");
-    return !(v != nullptr && std::strcmp(v, "0") == 0);
-}
+// stream_k = 0 (then fixed split-K as for the tensor-core kernel).
+bool use_stream_k() { return opt(kOptStreamK) != 0; }
 
-uint64_t timeout_ns() {
-    const char *v = std::getenv("W12_TIMEOUT_MS");
-    const long ms = v ? std::strtol(v, nullptr, 10) : 0;
-    return (uint64_t)(ms > 0 ? ms : 4000) * 1000000ull;
-}
+uint64_t timeout_ns() { return (uint64_t)opt(kOptTimeout) * 1000000ull; }
 
 size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -323,7 +335,7 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     const int64_t kMaxSegs = plan->gemv_sm ? dev::GemvSmCfg<1>::kMaxSegs : dev::GemmCfg<16, kStages, false>::kMaxSegs;
     const int64_t capacity = (int64_t)s->sm_count * occ;
     const int64_t tiles = info.tiles, segs = info.segs;
-    const char *forced = std::getenv("W12_SPLITS");  // tuning override: fixed split-K
+    const int64_t forced = opt(kOptSplits);  // tuning override: fixed split-K
     plan->units = 0;
     // one wave of equal contiguous unit ranges (stream-K): no SM idles
     // because the tile count does not divide the resident CTA count
@@ -337,7 +349,7 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     if ((units + sk_ctas - 1) / sk_ctas > max_range) sk_ctas = (units + max_range - 1) / max_range;
     const bool sk_shape = plan->gemv_sm || tiles < capacity;
     // (the device computes unit x ctas products in 32 bits)
-    if (plan->gemv && forced == nullptr && sk_shape && units * sk_ctas < (int64_t(1) << 31) && use_stream_k()) {
+    if (plan->gemv && forced == 0 && sk_shape && units * sk_ctas < (int64_t(1) << 31) && use_stream_k()) {
         const int64_t shortest = units / sk_ctas;  // units of the shortest range
         plan->units = units;
         // most ranges one tile can meet: the one holding its first unit plus
@@ -351,10 +363,7 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
         int64_t per = (segs + splits - 1) / splits;          // segments of the longest CTA
         if (per > kMaxSegs) per = kMaxSegs;
         splits = (segs + per - 1) / per;                      // fewest splits with that length
-        if (forced != nullptr) {
-            const long f = std::strtol(forced, nullptr, 10);
-            if (f >= 1 && f <= segs && (segs + f - 1) / f <= kMaxSegs) splits = f;
-        }
+        if (forced != 0 && forced <= segs && (segs + forced - 1) / forced <= kMaxSegs) splits = forced;
         plan->splits = (int)splits;
         plan->ctas = (int)(tiles * splits);
     }
@@ -394,11 +403,8 @@ namespace {
 // GEMM launches carry the programmatic-stream-serialization attribute: the
 // kernel may start while the previous kernel in the stream finishes; it warms
 // L2 with its first weights and then waits (griddepcontrol.wait) before any
-// other memory access.  W12_PDL=0 turns the attribute off.
-bool use_pdl() {
-    const char *v = std::getenv("W12_PDL");
-    return !(v != nullptr && std::strcmp(v, "0") == 0);
-}
+// other memory access.  The option pdl = 0 turns the attribute off.
+bool use_pdl() { return opt(kOptPdl) != 0; }
 
 template <class... KArgs, class... Args>
 cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
@@ -818,6 +824,31 @@ int gemm_noalloc(const uint16_t *x_dev, const void *blob_dev, const w12_info &in
                                     static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(no-alloc counters)", err);
     return gemm(x_dev, blob_dev, info, y_dev, M, scratch, (size_t)W12_NOALLOC_SCRATCH_BYTES, stream, err);
+}
+
+int set_option(const char *name, int64_t value, std::string *err) {
+    for (OptionSlot &o : g_options) {
+        if (std::strcmp(o.name, name) != 0) continue;
+        if (value < o.lo || value > o.hi || (&o == &g_options[kOptTokenTile] && value != 0 && value != 16 &&
+                                             value != 32)) {
+            *err = std::string("value out of range for option ") + name;
+            return W12_ERR_INVALID_ARG;
+        }
+        o.value.store(value, std::memory_order_relaxed);
+        return W12_OK;
+    }
+    *err = std::string("unknown option ") + name;
+    return W12_ERR_INVALID_ARG;
+}
+
+int get_option(const char *name, int64_t *value, std::string *err) {
+    for (OptionSlot &o : g_options) {
+        if (std::strcmp(o.name, name) != 0) continue;
+        *value = o.value.load(std::memory_order_relaxed);
+        return W12_OK;
+    }
+    *err = std::string("unknown option ") + name;
+    return W12_ERR_INVALID_ARG;
 }
 
 int selftest_timeout(uint32_t timeout_us, void *stream, std::string *err) {

@@ -60,5 +60,8 @@ int encode_device(const uint16_t *w_dev, int64_t N, int64_t K, void *blob_dev, s
 
 int selftest_timeout(uint32_t timeout_us, void *stream, std::string *err);
 
+int set_option(const char *name, int64_t value, std::string *err);
+int get_option(const char *name, int64_t *value, std::string *err);
+
 }  // namespace launch
 }  // namespace w12

@@ -27,7 +27,7 @@ EXPORTED = (
     "w12_blob_info", "w12_blob_validate", "w12_decode", "w12_gemm_workspace_size", "w12_gemm_launch_info",
     "w12_gemm", "w12_gemm_group_workspace_size", "w12_gemm_group", "w12_gemm_argmax_workspace_size", "w12_gemm_argmax", "w12_gemm_noalloc", "w12_encode_workspace_size", "w12_encoded_size_device", "w12_encode_device",
     "w12_q8_encoded_size", "w12_q8_encode_host", "w12_q8_blob_info", "w12_q8_gemm_workspace_size", "w12_q8_gemm",
-    "w12_check_status", "w12_selftest_timeout",
+    "w12_check_status", "w12_selftest_timeout", "w12_set_option", "w12_get_option",
 )
 
 
@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
     L.w12_q8_gemm.argtypes = [vp, vp, ctypes.POINTER(w12_q8_info), vp, i32, vp, sz, vp]
     L.w12_check_status.argtypes = [vp]
     L.w12_selftest_timeout.argtypes = [ctypes.c_uint32, vp]
+    L.w12_set_option.argtypes = [ctypes.c_char_p, i64]
+    L.w12_get_option.argtypes = [ctypes.c_char_p, ctypes.POINTER(i64)]
     for name in EXPORTED[3:]:
         getattr(L, name).restype = i32
     _lib = L
@@ -328,6 +330,37 @@ def w12_q8_gemm_ptr(x_ptr: int, blob_ptr: int, info: w12_q8_info, y_ptr: int, M:
 
 def w12_check_status(stream=None) -> None:
     _check(lib().w12_check_status(_stream_handle(stream)))
+
+
+def w12_set_option(name: str, value: int) -> None:
+    _check(lib().w12_set_option(name.encode(), int(value)))
+
+
+def w12_get_option(name: str) -> int:
+    out = ctypes.c_int64()
+    _check(lib().w12_get_option(name.encode(), ctypes.byref(out)))
+    return out.value
+
+
+class options:
+    """Context manager: set launch options (w12_set_option) for a block and
+    put the previous values back afterwards, e.g.
+    ``with w12.options(token_tile=16, a_operand_smem=1): ...``."""
+
+    def __init__(self, **values):
+        self.values = values
+        self.saved = {}
+
+    def __enter__(self):
+        for name, v in self.values.items():
+            self.saved[name] = w12_get_option(name)
+            w12_set_option(name, v)
+        return self
+
+    def __exit__(self, *exc):
+        for name, v in self.saved.items():
+            w12_set_option(name, v)
+        return False
 
 
 def w12_selftest_timeout(timeout_us: int, stream=None) -> None:

@@ -24,3 +24,21 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture
+def w12_opts():
+    """Setter for the library's launch options (w12_set_option); every option
+    it touched gets its previous value back when the test ends."""
+    from lossless_bit_weight_encode_gb300 import w12
+    saved = {}
+
+    def setopt(**values):
+        for name, v in values.items():
+            if name not in saved:
+                saved[name] = w12.w12_get_option(name)
+            w12.w12_set_option(name, int(v))
+
+    yield setopt
+    for name, v in saved.items():
+        w12.w12_set_option(name, v)

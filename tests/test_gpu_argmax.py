@@ -22,8 +22,8 @@ def built():
 
 
 @pytest.fixture(params=["gemv", "tc"])
-def m1_path(request, monkeypatch):
-    monkeypatch.setenv("W12_M1_PATH", request.param)
+def m1_path(request, w12_opts):
+    w12_opts(gemv_max_m=2 if request.param == "gemv" else 0)
     return request.param
 
 

@@ -22,10 +22,9 @@ def built():
 
 
 @pytest.fixture(params=[(a, t) for a in A_OPERANDS for t in TOKEN_TILES], ids=lambda v: f"{v[0]}-ntok{v[1]}")
-def a_operand(request, monkeypatch):
+def a_operand(request, w12_opts):
     """Every tensor-core variant: A in TMEM or SMEM, 32- or 16-token tile."""
-    monkeypatch.setenv("W12_A_OPERAND", request.param[0])
-    monkeypatch.setenv("W12_NTOK", request.param[1])
+    w12_opts(a_operand_smem=request.param[0] == "smem", token_tile=int(request.param[1]))
     return request.param
 
 
@@ -172,8 +171,8 @@ def test_layer_shapes_sampled_rows(workload, Ms):
 
 
 @pytest.fixture(params=["gemv", "tc"])
-def m1_path(request, monkeypatch):
-    monkeypatch.setenv("W12_M1_PATH", request.param)
+def m1_path(request, w12_opts):
+    w12_opts(gemv_max_m=2 if request.param == "gemv" else 0)
     return request.param
 
 
@@ -212,8 +211,8 @@ def test_one_token_one_hot_exact(m1_path):
 
 
 @pytest.fixture(params=["2", "1"])
-def gemv_max_m(request, monkeypatch):
-    monkeypatch.setenv("W12_GEMV_MAX_M", request.param)
+def gemv_max_m(request, w12_opts):
+    w12_opts(gemv_max_m=int(request.param))
     return int(request.param)
 
 

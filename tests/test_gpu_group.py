@@ -37,9 +37,9 @@ def test_group_matches_oracle(M):
 
 
 @pytest.mark.parametrize("M", [1, 2, 16])
-def test_group_equals_single_launches(M, monkeypatch):
+def test_group_equals_single_launches(M, w12_opts):
     from gpu_util import dev_to_bits, to_dev_bf16
-    monkeypatch.setenv("W12_SPLITS", "4")  # same split count for the group and each matrix
+    w12_opts(splits=4)  # same split count for the group and each matrix
     ws, mats = _mats()
     x = to_dev_bf16(wl.activations(M, 2048, seed=97 + M))
     ys = W12Group(mats).gemm(x)

@@ -27,15 +27,15 @@ def _capacity(plan):
 
 
 @pytest.fixture(params=["1", "0"], ids=["cta_per_sm", "two_ctas_per_sm"])
-def gemv_kernel(request, monkeypatch):
+def gemv_kernel(request, w12_opts):
     """Both CUDA-core kernels, whichever the planner would pick."""
-    monkeypatch.setenv("W12_GEMV_SM", request.param)
+    w12_opts(gemv_sm=int(request.param))
     return request.param
 
 
 @pytest.mark.parametrize("M", [1, 2])
 @pytest.mark.parametrize("shape", [(12763, 5020), (5000, 17408), (1000, 3000)])
-def test_stream_k_matches_oracle(M, shape, gemv_kernel, monkeypatch):
+def test_stream_k_matches_oracle(M, shape, gemv_kernel, w12_opts):
     import torch
     from gpu_util import check_tolerance, dev_to_bits, to_dev_bf16
     n, k = shape
@@ -44,7 +44,7 @@ def test_stream_k_matches_oracle(M, shape, gemv_kernel, monkeypatch):
     ref = oracle.gemm_f64(x, w)
     mat = W12Weight(w)
     for mode in ("1", "0"):
-        monkeypatch.setenv("W12_STREAMK", mode)
+        w12_opts(stream_k=int(mode))
         plan = w12.w12_gemm_launch_info(mat.info, M)
         tiles, segs = int(mat.info.tiles), int(mat.info.segs)
         if mode == "1":
@@ -54,7 +54,7 @@ def test_stream_k_matches_oracle(M, shape, gemv_kernel, monkeypatch):
         y = dev_to_bits(mat.gemm(to_dev_bf16(x)))
         w12.w12_check_status()
         torch.cuda.synchronize()
-        check_tolerance(y, ref, f"{shape} M={M} W12_STREAMK={mode}")
+        check_tolerance(y, ref, f"{shape} M={M} stream_k={mode}")
 
 
 @pytest.mark.parametrize("M", [1, 2])
@@ -92,12 +92,12 @@ def test_stream_k_reproducible_and_counters_reset(gemv_kernel):
     w12.w12_check_status()
 
 
-def test_kernel_choice(monkeypatch):
+def test_kernel_choice(w12_opts):
     """One CTA per SM for weights with rare escapes, whatever the tile count
     (one wave of ranges covers these launches); two per SM for escape-heavy
     weights."""
     import torch
-    monkeypatch.delenv("W12_GEMV_SM", raising=False)
+    w12_opts(gemv_sm=-1)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     gauss = W12Weight(wl.gaussian_weights(2048, 1024, seed=330))
     heavy = W12Weight(wl.heavy_tail_weights(2048, 1024, seed=331))
@@ -108,7 +108,7 @@ def test_kernel_choice(monkeypatch):
         assert w12.w12_gemm_launch_info(heavy.info, M)["ctas_per_sm"] == 2
         plan = w12.w12_gemm_launch_info(many.info, M)
         assert plan["ctas_per_sm"] == 1 and plan["ctas"] == sms
-    monkeypatch.setenv("W12_GEMV_SM", "1")
+    w12_opts(gemv_sm=1)
     assert w12.w12_gemm_launch_info(heavy.info, 1)["ctas_per_sm"] == 1
 
 

@@ -202,3 +202,30 @@ def test_gemm_argument_errors_before_any_device_work():
     assert w12.w12_q8_gemm_ptr(0, a, q8, a, 1, a, 1 << 20, None) == INVALID
     assert w12.w12_q8_gemm_ptr(a, a + 8, q8, a, 1, a, 1 << 20, None) == ALIGN
     assert w12.w12_last_error() != ""
+
+
+def test_launch_options_set_get_and_reject(monkeypatch):
+    """Launch options come only from w12_set_option: unknown names and values
+    out of range are refused (nothing changes), and an environment variable
+    named like an option has no effect."""
+    from lossless_bit_weight_encode_gb300 import w12
+    defaults = {"gemv_max_m": 2, "token_tile": 0, "a_operand_smem": 0, "gemv_sm": -1, "stream_k": 1,
+                "splits": 0, "pdl": 1, "timeout_ms": 4000}
+    for name, v in defaults.items():
+        assert w12.w12_get_option(name) == v, name
+    monkeypatch.setenv("W12_NTOK", "16")
+    monkeypatch.setenv("W12_GEMV_MAX_M", "1")
+    assert w12.w12_get_option("token_tile") == 0 and w12.w12_get_option("gemv_max_m") == 2
+    with w12.options(token_tile=16, gemv_sm=0, timeout_ms=25):
+        assert w12.w12_get_option("token_tile") == 16
+        assert w12.w12_get_option("gemv_sm") == 0 and w12.w12_get_option("timeout_ms") == 25
+    for name, v in defaults.items():
+        assert w12.w12_get_option(name) == v, name
+    for name, bad in [("token_tile", 8), ("token_tile", 33), ("gemv_max_m", 3), ("gemv_sm", -2), ("pdl", 2),
+                      ("timeout_ms", 0), ("no_such_option", 1)]:
+        with pytest.raises(w12.W12Error) as e:
+            w12.w12_set_option(name, bad)
+        assert e.value.status == 1
+    assert w12.w12_get_option("token_tile") == 0
+    with pytest.raises(w12.W12Error):
+        w12.w12_get_option("no_such_option")

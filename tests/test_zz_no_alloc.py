@@ -2,9 +2,12 @@
 (for example a serving engine whose allocator owns all free HBM, or a plug-in
 that must not allocate behind its host framework).  Its scratch is a fixed
 array in the library's static device memory; this checks, through the C ABI,
-that two calls in a row give the same result as w12_gemm with a caller
-workspace, and that a problem needing more scratch than the fixed array is
-refused before anything runs.  Collected last on purpose."""
+that two calls in a row give bit for bit the result of w12_gemm with a
+caller workspace (the same plan and the same fixed split-K order, so a stale
+partial sum or counter left in the shared array would show), that both meet
+the GEMM tolerance against the fp64 oracle, and that a problem needing more
+scratch than the fixed array is refused before anything runs.  Collected
+last on purpose."""
 import ctypes
 
 import numpy as np
@@ -33,18 +36,23 @@ def _noalloc_raw(x, mat, y, M):
                                    (1024, 17408, 32)])
 def test_noalloc_matches_workspace_gemm_twice(n, k, M):
     import torch
-    from gpu_util import bits_to_f64, check_tolerance, dev_to_bits, to_dev_bf16
+    import oracle
+    from gpu_util import check_tolerance, dev_to_bits, to_dev_bf16
     w = wl.heavy_tail_weights(n, k, seed=n + M)
-    x = to_dev_bf16(wl.activations(M, k, seed=k + M))
+    xb = wl.activations(M, k, seed=k + M)
+    x = to_dev_bf16(xb)
     mat = W12Weight(w)
     ref = dev_to_bits(mat.gemm(x))
     w12.w12_check_status()
-    ref64 = bits_to_f64(ref)
+    ref64 = oracle.gemm_f64(xb, w)
+    check_tolerance(ref, ref64, f"w12_gemm {n}x{k} M={M}")
     for _ in range(2):  # two calls in a row share (and reuse) the one scratch array
         y = torch.full((M, n), float("nan"), dtype=torch.bfloat16, device="cuda")
         assert _noalloc_raw(x, mat, y, M) == 0, w12.w12_last_error()
         w12.w12_check_status()
-        check_tolerance(dev_to_bits(y), ref64, f"noalloc {n}x{k} M={M}")
+        got = dev_to_bits(y)
+        assert np.array_equal(got, ref), f"noalloc {n}x{k} M={M} differs from w12_gemm"
+        check_tolerance(got, ref64, f"noalloc {n}x{k} M={M}")
 
 
 def test_noalloc_rejects_oversized_problem():
