@@ -40,11 +40,11 @@ KERNEL_SOURCES = ("lossless_bit_weight_encode_gb300/csrc/gemm_tc.cuh",
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
     ap.add_argument("--m", type=int, default=1, help="tokens per GEMM (1..32)")
-    ap.add_argument("--workload", default="layer", choices=["layer", "heavy", "model64", "lmhead"])
+    ap.add_argument("--workload", default="layer", choices=["layer", "heavy", "model64", "lmhead", "single"])
     ap.add_argument("--weights", default="w12", choices=["w12", "q8"],
                     help="w12: the lossless format; q8: the 8-bit verification copy of the same weights")
     ap.add_argument("--no-group", action="store_true",
@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--no-bf16", action="store_true", help="skip the cuBLAS BF16 comparator")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--no-detail", action="store_true",
+                    help="skip the other configurations (M sweep, heavy tail, single layer, decode) that the "
+                         "default layer run at M=1 adds under detail")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     ap.add_argument("--matrices", default=None,
                     help="comma list of layer matrices to run (profiling only; default all seven)")
@@ -170,6 +173,7 @@ WORKLOAD_TEXT = {
               "exact-argmax epilogue (per-token index and fp32 logit; logits not stored)",
     "model64": "model64: 64 layers of the 27B-class shapes chained in layer order (448 GEMMs, 21.8 G weights, "
                "32.7 GB of W12 resident), weights N(0,0.02) drawn and encoded on the GPU",
+    "single": "single: one 1024x1024 layer, weights N(0,0.02), x[1,1024] N(0,1), PCG64 seed 0 (W then x)",
 }
 
 
@@ -188,9 +192,10 @@ class OracleSample:
         self.blobs = {}
         self.cores = oracle.max_threads(0)
 
-    def run(self, max_seconds, start=0):
+    def run(self, max_seconds, start=0, threads=0):
         """Whole matrices, cycling from `start`, until `max_seconds` of wall
-        time have been spent (at least one matrix)."""
+        time have been spent (at least one matrix); `threads` OpenMP threads
+        (0: all host cores)."""
         done_w, spent, names, i = 0, 0.0, [], start
         while True:
             j = i % len(self.weights)
@@ -198,7 +203,7 @@ class OracleSample:
             if j not in self.blobs:
                 self.blobs[j] = self.oracle.encode(w)  # untimed
             t0 = time.perf_counter()
-            self.oracle.w12_gemm_f64(self.xs[j], self.blobs[j], threads=0)
+            self.oracle.w12_gemm_f64(self.xs[j], self.blobs[j], threads=threads)
             spent += time.perf_counter() - t0
             done_w += w.size
             names.append(name)
@@ -208,7 +213,8 @@ class OracleSample:
         gbs = 2.0 * done_w / spent / 1e9
         sample = (f"{len(names)} layer matrices at M={self.m} ({'+'.join(names[:7])}"
                   f"{'...' if len(names) > 7 else ''}): {done_w / 1e6:.1f} M weights in {spent:.2f} s "
-                  f"(oracle encode untimed; W12 decode + fp64 dot products timed)")
+                  f"(oracle encode untimed; W12 decode + fp64 dot products timed; "
+                  f"{self.oracle.max_threads(threads)} threads)")
         return gbs, sample, done_w, spent
 
 
@@ -225,9 +231,15 @@ def run_reference(args):
     if args.workload == "lmhead":
         name, n, k = wl.LMHEAD_SHAPE
         weights = [(name, wl.gaussian_weights(n, k, seed=wl.weight_seed("lmhead", 0)))]
+    elif args.workload == "single":
+        w1, x1 = wl.single_case()
+        weights = [("single", w1)]
     else:
         weights = list(wl.layer_weights(args.workload))
-    xs = [wl.activations(args.m, w.shape[1], seed=wl.activation_seed(args.workload, args.m)) for _, w in weights]
+    if args.workload == "single" and args.m == 1:
+        xs = [x1]
+    else:
+        xs = [wl.activations(args.m, w.shape[1], seed=wl.activation_seed(args.workload, args.m)) for _, w in weights]
     orc = OracleSample(weights, xs, args.m)
     # one step = one layer matrix (cycling q, k, v, o, gate, up, down): a
     # bounded sample so that K + W steps stay within a few minutes
@@ -238,16 +250,15 @@ def run_reference(args):
             tot_w += w_i
             tot_s += s_i
     value = 2.0 * tot_w / tot_s / 1e9
-    sample = (f"one layer matrix per step, cycling the 7 (q..down) at M={args.m}: {tot_w / 1e6:.1f} M weights "
-              f"in {tot_s:.2f} s over {args.steps} steps (oracle encode untimed)")
+    sample = (f"one matrix per step, cycling {'+'.join(n for n, _ in weights)} at M={args.m}: "
+              f"{tot_w / 1e6:.1f} M weights in {tot_s:.2f} s over {args.steps} steps (oracle encode untimed)")
     layer_w = sum(w.size for _, w in weights)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(2.0 * layer_w / (value * 1e9) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: 27B-class decoder layer, 7 matrices, 340.8 M weights",
-                   "M": args.m, "parallelism": "host cores (OpenMP)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "M": args.m, "parallelism": "host cores (OpenMP)",
                    "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": orc.cores, "kind": "oracle",
                          "sample": sample},
@@ -283,6 +294,198 @@ def job_weight_gbs(weights_per_rank: int, world: int, ms: float) -> float:
 
 
 # ------------------------------------------------------------------ GPU arm
+def bootstrap_median_ci(samples, n_boot: int = 2000, seed: int = 0):
+    """Median of `samples` and a 95 % percentile-bootstrap interval for it."""
+    a = np.asarray(samples, dtype=np.float64)
+    rng = np.random.default_rng(seed)
+    meds = np.median(a[rng.integers(0, a.size, size=(n_boot, a.size))], axis=1)
+    return float(np.median(a)), float(np.percentile(meds, 2.5)), float(np.percentile(meds, 97.5))
+
+
+class LayerStep:
+    """The launches of one step over a list of W12 (or Q8) matrices at M
+    tokens: q/k/v and gate/up grouped when the list is a whole layer (or 64),
+    one launch per matrix otherwise.  Activations and outputs live in one
+    device buffer each, so the end-to-end leg moves them with one copy each
+    way."""
+
+    def __init__(self, mats, names, xs_host, M, grouped, q8=False, argmax=False):
+        import torch
+        from lossless_bit_weight_encode_gb300 import W12Group, w12
+
+        self.w12 = w12
+        self.mats, self.names, self.M = mats, names, M
+        self.xs_host = xs_host
+        offs, tot = [], 0
+        for x in xs_host:
+            offs.append(tot)
+            tot += (x.size + 127) // 128 * 128
+        self.xpack_host = np.zeros(tot, dtype=np.uint16)
+        for o, x in zip(offs, xs_host):
+            self.xpack_host[o:o + x.size] = x.ravel()
+        self.xpack = torch.from_numpy(self.xpack_host.view(np.int16)).cuda().view(torch.bfloat16)
+        self.xs = [self.xpack[o:o + x.size].view(x.shape) for o, x in zip(offs, xs_host)]
+        self.ypack = torch.empty(sum(M * m.N for m in mats), dtype=torch.bfloat16, device="cuda")
+        yoffs = np.cumsum([0] + [M * m.N for m in mats])
+        self.ys = [self.ypack[yoffs[i]:yoffs[i + 1]].view(M, m.N) for i, m in enumerate(mats)]
+        self.argmax = argmax
+        sh = torch.cuda.current_stream().cuda_stream
+        self.keep = []
+        if argmax:
+            self.idx = torch.empty(M, dtype=torch.int32, device="cuda")
+            self.val = torch.empty(M, dtype=torch.float32, device="cuda")
+            self.groups = [[i] for i in range(len(mats))]
+            self.calls = []
+            for i, m in enumerate(mats):
+                ws = m.argmax_workspace(M)
+                self.calls.append((w12.w12_gemm_argmax_ptr,
+                                   (self.xs[i].data_ptr(), m.blob.data_ptr(), m.info, M, None, self.idx.data_ptr(),
+                                    self.val.data_ptr(), ws.data_ptr(), ws.numel(), sh)))
+        else:
+            n7 = len(LAYER_NAMES)
+            if grouped:
+                per_layer = [[0, 1, 2], [3], [4, 5], [6]]
+                self.groups = [[n7 * l + i for i in g] for l in range(len(mats) // n7) for g in per_layer]
+            else:
+                self.groups = [[i] for i in range(len(mats))]
+            self.calls = []
+            for g in self.groups:
+                if len(g) == 1:
+                    i = g[0]
+                    ws = mats[i].workspace(M)
+                    self.calls.append((w12.w12_q8_gemm_ptr if q8 else w12.w12_gemm_ptr,
+                                       (self.xs[i].data_ptr(), mats[i].blob.data_ptr(), mats[i].info,
+                                        self.ys[i].data_ptr(), M, ws.data_ptr(), ws.numel(), sh)))
+                else:
+                    grp = W12Group([mats[i] for i in g])
+                    gws = grp.workspace(M)
+                    self.keep.append((grp, gws))
+                    self.calls.append((w12.w12_gemm_group_ptr,
+                                       (self.xs[g[0]].data_ptr(), [mats[i].blob.data_ptr() for i in g], grp.infos,
+                                        [self.ys[i].data_ptr() for i in g], M, gws.data_ptr(), gws.numel(), sh)))
+        self.launch_names = ["+".join(names[i] for i in g) for g in self.groups]
+        # algorithmic bytes of each launch: its blobs, one x (shared by a
+        # group), its outputs (the argmax keys and results are a few bytes)
+        self.alg = [sum(int(mats[i].info.total_bytes) + (0 if argmax else 2 * M * mats[i].N) for i in g)
+                    + 2 * M * mats[g[0]].K for g in self.groups]
+        self.packed = sum(int(m.info.total_bytes) for m in mats)
+        self.weights = sum(m.N * m.K for m in mats)
+        if q8:
+            self.kernels = ["w12_gemm_tc_kernel (Q8 copy)"] * len(self.groups)
+        else:
+            self.kernels = [w12.w12_gemm_group_launch_info([mats[i].info for i in g], M)["kernel_name"]
+                            for g in self.groups]
+
+    def launch_count(self) -> int:
+        return len(self.calls) * (2 if self.argmax else 1)
+
+    def run(self):
+        for fn, c in self.calls:
+            rc = fn(*c)
+            if rc != 0:
+                raise self.w12.W12Error(rc, self.w12.w12_last_error())
+
+    def run_e2e(self, xpack_h, ypack_h, idx_h):
+        """x in from pinned host memory, the launches, the outputs back."""
+        self.xpack.copy_(xpack_h, non_blocking=True)
+        self.run()
+        if self.argmax:
+            idx_h.copy_(self.idx, non_blocking=True)
+        else:
+            ypack_h.copy_(self.ypack, non_blocking=True)
+
+
+LAYER_NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+
+
+def time_steps(run, K: int) -> float:
+    """ms per call of `run` over K calls between two events on the current stream."""
+    import torch
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        run()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / K
+
+
+def step_samples(run, R: int):
+    """Per-call ms of R consecutive calls (one event between each)."""
+    import torch
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(R + 1)]
+    evs[0].record()
+    for r in range(R):
+        run()
+        evs[r + 1].record()
+    evs[R].synchronize()
+    return [evs[r].elapsed_time(evs[r + 1]) for r in range(R)]
+
+
+def launch_times(step: LayerStep, reps: int):
+    """Mean ms of each launch of the step, events around every launch."""
+    import torch
+    nl = len(step.calls)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(reps)]
+    torch.cuda.synchronize()
+    for k in range(reps):
+        for i, (fn, c) in enumerate(step.calls):
+            evs[k][i].record()
+            rc = fn(*c)
+            if rc != 0:
+                raise step.w12.W12Error(rc, step.w12.w12_last_error())
+        evs[k][nl].record()
+    torch.cuda.synchronize()
+    return [statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(reps)) for i in range(nl)]
+
+
+def cublas_ms(dense, groups, xs, K: int, warmup: int, argmax=False) -> float:
+    """torch.matmul (cuBLAS BF16) over the same shapes, x and grouping."""
+    import torch
+    wts = [torch.cat([dense[i] for i in g], dim=0) if len(g) > 1 else dense[g[0]] for g in groups]
+    xb = [xs[g[0]] for g in groups]
+    outs = [torch.empty((x.shape[0], w.shape[0]), dtype=torch.bfloat16, device="cuda") for x, w in zip(xb, wts)]
+
+    def bstep():
+        for x, wt, o in zip(xb, wts, outs):
+            torch.matmul(x, wt.t(), out=o)
+            if argmax:
+                torch.argmax(o, dim=1)
+
+    for _ in range(warmup):
+        bstep()
+    return time_steps(bstep, K)
+
+
+def dense_dev(weights):
+    import torch
+    return [torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16) for _, w in weights]
+
+
+def sweep_point(mats, weights, xs_host, M, K, warmup, dense, q8=False):
+    """µs per layer step at M tokens, the packed fraction of the HBM peak and
+    the cuBLAS BF16 step on the same shapes and grouping."""
+    peak, _ = hbm_peak_gbs()
+    st = LayerStep(mats, [n for n, _ in weights], xs_host, M, grouped=not q8, q8=q8)
+    for _ in range(warmup):
+        st.run()
+    ms = time_steps(st.run, K)
+    st.w12.w12_check_status()
+    med, lo, hi = bootstrap_median_ci(step_samples(st.run, max(50, K)))
+    st.w12.w12_check_status()
+    out = {"us_per_layer": round(ms * 1e3, 2), "median_us": round(med * 1e3, 2),
+           "ci95_us": [round(lo * 1e3, 2), round(hi * 1e3, 2)],
+           "packed_frac_of_hbm_peak": round(st.packed / (ms * 1e-3) / 1e9 / peak, 4),
+           "kernels": sorted(set(st.kernels))}
+    if dense is not None:
+        b = cublas_ms(dense, st.groups, st.xs, K, warmup)
+        out["bf16_cublas_us"] = round(b * 1e3, 2)
+        out["speedup_vs_bf16"] = round(b / ms, 4)
+    return out
+
+
 def run_w12(args):
     import torch
     import torch.distributed as dist
@@ -297,17 +500,18 @@ def run_w12(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    from lossless_bit_weight_encode_gb300 import Q8Weight, W12Group, W12Weight, w12
+    from lossless_bit_weight_encode_gb300 import Q8Weight, W12Weight, w12
     from lossless_bit_weight_encode_gb300 import build as libbuild
     from lossless_bit_weight_encode_gb300 import workloads as wl
 
     libbuild.build()
     M = args.m
+    K = args.steps
     nshape = len(wl.LAYER_SHAPES)
+    peak, peak_kind = hbm_peak_gbs()
     if args.workload == "model64":
         # 64 layers drawn and encoded on the GPU (W12Weight.from_device); one
-        # activation per shape, shared by every layer; one workspace per shape
-        # (the launches are ordered on one stream)
+        # activation per shape, shared by every layer
         names = [f"L{layer}.{n}" for layer in range(wl.MODEL64_LAYERS) for n, _, _ in wl.LAYER_SHAPES]
         mats = []
         for layer in range(wl.MODEL64_LAYERS):
@@ -317,19 +521,41 @@ def run_w12(args):
                 del w
         xs_shape = [wl.model64_activation(M, i) for i in range(nshape)]
         xs_host = [xs_shape[i % nshape] for i in range(len(mats))]
-        xs_dev = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs_shape]
-        xs = [xs_dev[i % nshape] for i in range(len(mats))]
-        ws_shape = [mats[i].workspace(M) for i in range(nshape)]
-        wss = [ws_shape[i % nshape] for i in range(len(mats))]
+        step = LayerStep(mats, names, xs_host, M, grouped=not args.no_group)
 
         def dense_weights():
-            for layer in range(wl.MODEL64_LAYERS):
-                for idx in range(nshape):
-                    yield wl.model64_weight_dev(layer, idx)
+            return [wl.model64_weight_dev(layer, idx) for layer in range(wl.MODEL64_LAYERS)
+                    for idx in range(nshape)]
 
         def cpu_weights():
             return [(n, wl.model64_weight_dev(0, i).view(torch.int16).cpu().numpy().view(np.uint16))
                     for i, (n, _, _) in enumerate(wl.LAYER_SHAPES)]
+        cpu_xs = xs_shape
+    elif args.workload == "single":
+        # the 1024 x 1024 layer: its 1.5 MB blob fits in L2, so the step
+        # rotates through enough encoded copies (3 x L2) that every call reads
+        # its weights from HBM
+        w, x = wl.single_case()
+        base = W12Weight(w)
+        l2 = torch.cuda.get_device_properties(local).L2_cache_size
+        copies = max(1, -(-3 * l2 // int(base.info.total_bytes)))
+        mats = [base]
+        for _ in range(copies - 1):
+            c = W12Weight.__new__(W12Weight)
+            c.blob_host, c.info, c.N, c.K, c._ws = None, base.info, base.N, base.K, {}
+            c.blob = base.blob.clone()
+            mats.append(c)
+        names = [f"single#{i}" for i in range(copies)]
+        step = LayerStep(mats, names, [x] * copies, M, grouped=False)
+        weights_single = [("single", w)]
+
+        def dense_weights():
+            d = dense_dev(weights_single)[0]
+            return [d.clone() for _ in range(copies)]
+
+        def cpu_weights():
+            return weights_single
+        cpu_xs = [x]
     else:
         if args.workload == "lmhead":
             name, n, k = wl.LMHEAD_SHAPE
@@ -340,91 +566,29 @@ def run_w12(args):
             keep = set(args.matrices.split(","))
             weights = [(n, w) for n, w in weights if n in keep]
         names = [n for n, _ in weights]
-        mats = [Q8Weight(w) if args.weights == "q8" else W12Weight(w) for _, w in weights]
+        q8 = args.weights == "q8"
+        mats = [Q8Weight(w) if q8 else W12Weight(w) for _, w in weights]
         xs_host = [wl.activations(M, w.shape[1], seed=wl.activation_seed(args.workload, M)) for _, w in weights]
-        # every matrix's x in one device buffer (256-byte aligned slices), so
-        # that the end-to-end run brings a step's inputs in with one copy
-        offs, tot = [], 0
-        for x in xs_host:
-            offs.append(tot)
-            tot += (x.size + 127) // 128 * 128
-        xpack_host = np.zeros(tot, dtype=np.uint16)
-        for o, x in zip(offs, xs_host):
-            xpack_host[o:o + x.size] = x.ravel()
-        xpack = torch.from_numpy(xpack_host.view(np.int16)).cuda().view(torch.bfloat16)
-        xs = [xpack[o:o + x.size].view(x.shape) for o, x in zip(offs, xs_host)]
-        wss = [m.workspace(M) for m in mats]
+        whole = args.workload in ("layer", "heavy") and names == list(LAYER_NAMES)
+        step = LayerStep(mats, names, xs_host, M, grouped=whole and not args.no_group and not q8, q8=q8,
+                         argmax=args.workload == "lmhead")
 
         def dense_weights():
-            for _, w in weights:
-                yield torch.from_numpy(w.view(np.int16)).cuda().view(torch.bfloat16)
+            return dense_dev(weights)
 
         def cpu_weights():
             return weights
-    # all outputs in one device buffer: one copy brings a step's results back
-    ypack = torch.empty(sum(M * m.N for m in mats), dtype=torch.bfloat16, device="cuda")
-    yoffs = np.cumsum([0] + [M * m.N for m in mats])
-    ys = [ypack[yoffs[i]:yoffs[i + 1]].view(M, m.N) for i, m in enumerate(mats)]
-    stream = torch.cuda.current_stream()
-    sh = stream.cuda_stream
-    argmax = args.workload == "lmhead"
-    if argmax:
-        # the LM head: GEMM with the fused argmax epilogue (no logits stored)
-        idx = torch.empty(M, dtype=torch.int32, device="cuda")
-        val = torch.empty(M, dtype=torch.float32, device="cuda")
-        aws = [m.argmax_workspace(M) for m in mats]
-        calls = [(x.data_ptr(), m.blob.data_ptr(), m.info, M, None, idx.data_ptr(), val.data_ptr(), ws.data_ptr(),
-                  ws.numel(), sh) for x, m, ws in zip(xs, mats, aws)]
-        launch = w12.w12_gemm_argmax_ptr
-        groups = [[i] for i in range(len(mats))]
-    else:
-        # q, k, v multiply the same x, and so do gate and up: one launch each
-        layer_names = [n for n, _, _ in wl.LAYER_SHAPES]
-        layers = len(mats) // len(layer_names)
-        if args.workload == "model64":
-            whole_layers = True
-        else:
-            whole_layers = args.workload in ("layer", "heavy") and names == layer_names
-        grouped = not args.no_group and args.weights == "w12" and whole_layers
-        per_layer = [[0, 1, 2], [3], [4, 5], [6]]
-        groups = ([[7 * l + i for i in g] for l in range(layers) for g in per_layer] if grouped
-                  else [[i] for i in range(len(mats))])
-        calls = []
-        group_ws = []  # keeps the group workspaces alive for the raw pointers below
-        for g in groups:
-            if len(g) == 1:
-                i = g[0]
-                calls.append((w12.w12_q8_gemm_ptr if args.weights == "q8" else w12.w12_gemm_ptr,
-                              (xs[i].data_ptr(), mats[i].blob.data_ptr(), mats[i].info, ys[i].data_ptr(), M,
-                               wss[i].data_ptr(), wss[i].numel(), sh)))
-            else:
-                grp = W12Group([mats[i] for i in g])
-                gws = grp.workspace(M)
-                group_ws.append((grp, gws))
-                calls.append((w12.w12_gemm_group_ptr,
-                              (xs[g[0]].data_ptr(), [mats[i].blob.data_ptr() for i in g], grp.infos,
-                               [ys[i].data_ptr() for i in g], M, gws.data_ptr(), gws.numel(), sh)))
-    if argmax:
-        calls = [(launch, c) for c in calls]
-        groups = [[i] for i in range(len(mats))]
-    names_launch = ["+".join(names[i] for i in g) for g in groups]
-
-    def step():
-        for fn, c in calls:
-            rc = fn(*c)
-            if rc != 0:
-                raise w12.W12Error(rc, w12.w12_last_error())
+        cpu_xs = xs_host
 
     graph = None
+    run_step = step.run
     if args.graph:
-        step()
+        step.run()
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            step()
+        with torch.cuda.graph(graph, stream=torch.cuda.current_stream()):
+            step.run()
         run_step = graph.replay
-    else:
-        run_step = step
 
     def barrier():
         if world > 1:
@@ -436,146 +600,90 @@ def run_w12(args):
     w12.w12_check_status()
     barrier()
 
-    # main timed region: K steps between two events
-    K = args.steps
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # main timed region: exactly K steps between two events
     with ClockSampler(local) as clocks:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ev0.record()
         for _ in range(K):
             run_step()
         ev1.record()
         ev1.synchronize()
-    barrier()
+        barrier()
+        # per-step samples for the median and its bootstrap interval
+        R = max(50, min(400, K))
+        samples = step_samples(run_step, R)
     ms_total = ev0.elapsed_time(ev1)
     w12.w12_check_status()
     ms_total = max_over_ranks(ms_total, "cuda")
     ms_step = ms_total / K
+    med, lo, hi = bootstrap_median_ci(samples)
 
-    # per-launch durations of the GEMM kernel (events around every launch)
-    nl = len(calls)
-    kp = max(10, min(K, 500 if nl <= 7 else 20))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)] for _ in range(kp)]
-    barrier()
-    for k in range(kp):
-        for i, (fn, c) in enumerate(calls):
-            evs[k][i].record()
-            rc = fn(*c)
-            if rc != 0:
-                raise w12.W12Error(rc, w12.w12_last_error())
-        evs[k][nl].record()
-    torch.cuda.synchronize()
+    # per-launch durations (events around every launch; breaks the overlap
+    # that programmatic dependent launch gives back to back)
+    nl = len(step.calls)
+    launch_ms = launch_times(step, max(10, min(K, 200 if nl <= 7 else 10)))
     w12.w12_check_status()
-    launch_ms = [statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(kp)) for i in range(nl)]
-
-    if args.weights == "q8":
-        kernel_name = "w12_gemm_tc_kernel (Q8 copy)"
-    else:
-        plan0 = w12.w12_gemm_launch_info(mats[0].info, M)
-        kernel_name = "w12_gemm_tc_kernel" if plan0.get("ntok") > 4 else \
-            "w12_gemv_sm_kernel" if plan0.get("ctas_per_sm") == 1 else "w12_gemv_kernel"
-    layer_weights = sum(m.N * m.K for m in mats)
-    packed = sum(int(m.info.total_bytes) for m in mats)
-    alg = [sum(int(mats[i].info.total_bytes) + 2 * M * mats[i].N for i in g) + 2 * M * mats[g[0]].K
-           for g in groups]  # per launch: its blobs, one x, its outputs
-    value = job_weight_gbs(layer_weights, world, ms_step)
-    peak, peak_kind = hbm_peak_gbs()
-    achieved = sum(alg) / (sum(launch_ms) * 1e-3) / 1e9
+    lf = []
+    for i in range(nl):
+        lf.append({"launch": step.launch_names[i], "kernel": step.kernels[i], "us": round(launch_ms[i] * 1e3, 2),
+                   "alg_bytes": int(step.alg[i]),
+                   "frac": round(step.alg[i] / (launch_ms[i] * 1e-3) / 1e9 / peak, 4)})
+    dom = max(range(nl), key=lambda i: launch_ms[i])
+    achieved = step.alg[dom] / (launch_ms[dom] * 1e-3) / 1e9
     traffic_rec = recorded_traffic()
     traffic = None
     if traffic_rec is not None and traffic_rec.get("M") == M and traffic_rec.get("workload") == args.workload:
-        traffic = traffic_rec.get("dram_bytes_per_launch")
+        traffic = (traffic_rec.get("per_launch_dram_bytes") or {}).get(step.launch_names[dom])
 
-    # BF16 comparator (cuBLAS through torch.matmul), same shapes and x
+    # BF16 comparator (cuBLAS through torch.matmul), same shapes, x and grouping
     bf16 = None
     if not args.no_bf16:
-        dense = list(dense_weights())
-        # the same grouping for cuBLAS: one matmul over the concatenated weights
-        wts = [torch.cat([dense[i] for i in g], dim=0) if len(g) > 1 else dense[g[0]] for g in groups]
+        dense = dense_weights()
+        bf16 = cublas_ms(dense, step.groups, step.xs, K, args.warmup, argmax=step.argmax)
         del dense
-        xb = [xs[g[0]] for g in groups]
-        outs = [torch.empty((M, w.shape[0]), dtype=torch.bfloat16, device="cuda") for w in wts]
-
-        def bstep():
-            for x, wt, o in zip(xb, wts, outs):
-                torch.matmul(x, wt.t(), out=o)
-                if argmax:
-                    torch.argmax(o, dim=1)
-
-        for _ in range(args.warmup):
-            bstep()
-        barrier()
-        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        b0.record()
-        for _ in range(K):
-            bstep()
-        b1.record()
-        b1.synchronize()
-        bf16 = b0.elapsed_time(b1) / K
-        del wts, outs
 
     # end to end through the public API with host buffers: x from pinned host
-    # memory in, y back to pinned host memory, every step
+    # memory in, y (or the argmax index) back to pinned host memory, every step
     e2e = None
     if not args.no_e2e:
-        xh = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs_host]
-        yh = [torch.empty((M, m.N), dtype=torch.bfloat16).pin_memory() for m in mats]
-        one_copy = args.workload != "model64" and not argmax
-        if one_copy:
-            xpack_h = torch.from_numpy(xpack_host.view(np.int16)).view(torch.bfloat16).pin_memory()
-            ypack_h = torch.empty(ypack.numel(), dtype=torch.bfloat16).pin_memory()
-        if argmax:
-            idx_h = torch.empty(M, dtype=torch.int32).pin_memory()
+        xpack_h = torch.from_numpy(step.xpack_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+        ypack_h = torch.empty(step.ypack.numel(), dtype=torch.bfloat16).pin_memory()
+        idx_h = torch.empty(M, dtype=torch.int32).pin_memory()
 
         def estep():
-            if one_copy:
-                # the step's inputs in, its launches, its outputs out: one copy each way
-                xpack.copy_(xpack_h, non_blocking=True)
-                for fn, c in calls:
-                    rc = fn(*c)
-                    if rc != 0:
-                        raise w12.W12Error(rc, w12.w12_last_error())
-                ypack_h.copy_(ypack, non_blocking=True)
-                return
-            # x comes in once per launch (the members of a group share it)
-            for (fn, c), g in zip(calls, groups):
-                xs[g[0]].copy_(xh[g[0]], non_blocking=True)
-                rc = fn(*c)
-                if rc != 0:
-                    raise w12.W12Error(rc, w12.w12_last_error())
-                if argmax:
-                    idx_h.copy_(idx, non_blocking=True)
-                else:
-                    for i in g:
-                        yh[i].copy_(ys[i], non_blocking=True)
+            step.run_e2e(xpack_h, ypack_h, idx_h)
 
         for _ in range(args.warmup):
             estep()
         barrier()
-        ke = max(10, min(K, 1000))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(ke):
-            estep()
-        e1.record()
-        e1.synchronize()
+        e_ms = max_over_ranks(time_steps(estep, max(10, min(K, 1000))), "cuda")
         w12.w12_check_status()
-        e_ms = max_over_ranks(e0.elapsed_time(e1) / ke, "cuda")
-        e2e = {"value": round(job_weight_gbs(layer_weights, world, e_ms), 2), "unit": "GB/s",
-               "h2d_bytes_per_step": int(2 * xpack_h.numel()) if one_copy else int(sum(2 * M * mats[g[0]].K for g in groups)),
-               "d2h_bytes_per_step": int(4 * M) if argmax else int(sum(2 * M * m.N for m in mats)),
+        e2e = {"value": round(job_weight_gbs(step.weights, world, e_ms), 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(2 * step.xpack_host.size),
+               "d2h_bytes_per_step": int(4 * M) if step.argmax else int(2 * step.ypack.numel()),
                "ms_per_step": round(e_ms, 5)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        orc = OracleSample(cpu_weights(), xs_host[:nshape] if args.workload == "model64" else xs_host, M)
+        orc = OracleSample(cpu_weights(), cpu_xs, M)
         v, sample, _, _ = orc.run(3.0)
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": orc.cores, "kind": "oracle", "sample": sample}
+        v1, sample1, _, _ = orc.run(1.5, threads=1)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": orc.cores, "kind": "oracle", "sample": sample,
+               "value_1core": round(v1, 4), "sample_1core": sample1}
+
+    detail_extra = {}
+    if rank == 0 and world == 1 and not args.no_detail and args.workload == "layer" and args.weights == "w12" \
+            and not args.matrices and M == 1:
+        detail_extra = run_detail(args, mats, weights, step, bf16)
 
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
         return
     csum = clocks.summary()
+    layers = wl.MODEL64_LAYERS if args.workload == "model64" else 1
+    unit_steps = len(mats) if args.workload == "single" else layers
+    value = job_weight_gbs(step.weights, world, ms_step)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -583,36 +691,115 @@ def run_w12(args):
         "config": {
             "workload": WORKLOAD_TEXT[args.workload],
             "M": M, "global_batch": M * world, "parallelism": f"replicas x{world}",
-            "l2": f"inputs larger than L2: {packed / 1e6:.1f} MB of W12 streamed per step (L2 129 MB)",
+            "l2": (f"inputs larger than L2: {step.packed / 1e6:.1f} MB of W12 streamed per step (L2 129 MB)"
+                   if args.workload != "single" else
+                   f"{len(mats)} encoded copies rotated ({step.packed / 1e6:.1f} MB per step, > 3 x L2)"),
             "launch": ("cuda graph" if graph is not None else "stream") + f" ({nl} launches per step: "
-                      + ", ".join(names_launch[:7]) + ("..." if nl > 7 else "") + ")",
+                      + ", ".join(step.launch_names[:7]) + ("..." if nl > 7 else "") + ")",
         },
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+        "roofline": {"bound": "hbm", "kernel": step.kernels[dom], "launch": step.launch_names[dom],
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": round(sum(alg) / nl),
-                     "kernel": kernel_name, "launch_us": [round(v * 1e3, 2) for v in launch_ms]},
+                     "algorithmic_bytes": int(step.alg[dom]),
+                     "step_frac": round(step.packed / (ms_step * 1e-3) / 1e9 / peak, 4),
+                     "launch_frac": lf},
         "cpu_baseline": cpu,
         "clocks": csum,
         "e2e": e2e,
-        "gpu_launches": K * nl * (2 if argmax else 1),
+        "gpu_launches": K * step.launch_count(),
         "detail": {
-            "us_per_layer": round(ms_step * 1e3 / (wl.MODEL64_LAYERS if args.workload == "model64" else 1), 2),
-            "layers_per_step": wl.MODEL64_LAYERS if args.workload == "model64" else 1,
-            "packed_GBps": round(packed / (ms_step * 1e-3) / 1e9, 1),
-            "packed_frac_of_hbm_peak": round(packed / (ms_step * 1e-3) / 1e9 / peak, 4),
-            "bits_per_weight": round(8.0 * packed / layer_weights, 5),
+            "us_per_layer": round(ms_step * 1e3 / unit_steps, 3),
+            "step_median_us": round(med * 1e3, 2), "step_ci95_us": [round(lo * 1e3, 2), round(hi * 1e3, 2)],
+            "step_samples": len(samples),
+            "layers_per_step": unit_steps,
+            "packed_GBps": round(step.packed / (ms_step * 1e-3) / 1e9, 1),
+            "packed_frac_of_hbm_peak": round(step.packed / (ms_step * 1e-3) / 1e9 / peak, 4),
+            "bits_per_weight": round(8.0 * step.packed / step.weights, 5),
             "n_escapes": int(sum(int(getattr(m.info, "n_escapes", 0)) for m in mats)),
             "weights": args.weights,
-            "per_matrix_us": {n: round(statistics.mean(launch_ms[i::nshape]) * 1e3, 2)
-                              for i, (n, _, _) in enumerate(wl.LAYER_SHAPES)}
-                             if args.workload == "model64" else
-                             {n: round(v * 1e3, 2) for n, v in zip(names_launch, launch_ms)},
-            "bf16_cublas_us_per_layer": round(bf16 * 1e3 / (wl.MODEL64_LAYERS if args.workload == "model64"
-                                                            else 1), 2) if bf16 else None,
+            "per_launch_us": {n: round(v * 1e3, 2) for n, v in zip(step.launch_names[:8], launch_ms[:8])},
+            "bf16_cublas_us_per_layer": round(bf16 * 1e3 / unit_steps, 3) if bf16 else None,
             "speedup_vs_bf16": round(bf16 / ms_step, 4) if bf16 else None,
+            **detail_extra,
         },
     }
     emit(line, args)
+
+
+def run_detail(args, mats, weights, step, bf16_ms):
+    """The other configurations, for the record: the layer at M = 2..32, the
+    heavy-tailed layer at M = 1 and 16, the single 1024 x 1024 layer, and the
+    decode kernel's read + write bandwidth."""
+    import torch
+    from lossless_bit_weight_encode_gb300 import W12Weight, w12
+    from lossless_bit_weight_encode_gb300 import workloads as wl
+
+    peak, _ = hbm_peak_gbs()
+    K = max(args.steps, 50)
+    out = {}
+    dense = dense_dev(weights)
+    sweep = {"1": {"us_per_layer": None}}
+    for M in wl.SWEEP_M:
+        xs = [wl.activations(M, w.shape[1], seed=wl.activation_seed("layer", M)) for _, w in weights]
+        sweep[str(M)] = sweep_point(mats, weights, xs, M, K, args.warmup, dense)
+    del sweep["1"]
+    out["layer_sweep"] = sweep
+    del dense
+
+    # heavy-tailed weights (escape path)
+    hw = list(wl.layer_weights("heavy"))
+    hmats = [W12Weight(w) for _, w in hw]
+    hdense = dense_dev(hw)
+    heavy = {"escape_rate": round(sum(int(m.info.n_escapes) for m in hmats) / sum(m.N * m.K for m in hmats), 6)}
+    for M in wl.HEAVY_M:
+        xs = [wl.activations(M, w.shape[1], seed=wl.activation_seed("heavy", M)) for _, w in hw]
+        heavy[str(M)] = sweep_point(hmats, hw, xs, M, K, args.warmup, hdense)
+    out["heavy"] = heavy
+    del hdense, hmats
+
+    # the single 1024 x 1024 layer at M = 1, L2 defeated by rotating copies
+    w, x = wl.single_case()
+    base = W12Weight(w)
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    copies = max(1, -(-3 * l2 // int(base.info.total_bytes)))
+    blobs = [base.blob] + [base.blob.clone() for _ in range(copies - 1)]
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    yd = torch.empty((1, 1024), dtype=torch.bfloat16, device="cuda")
+    ws = base.workspace(1)
+    sh = torch.cuda.current_stream().cuda_stream
+    it = [0]
+
+    def one():
+        b = blobs[it[0] % copies]
+        it[0] += 1
+        rc = w12.w12_gemm_ptr(xd.data_ptr(), b.data_ptr(), base.info, yd.data_ptr(), 1, ws.data_ptr(), ws.numel(),
+                              sh)
+        if rc != 0:
+            raise w12.W12Error(rc, w12.w12_last_error())
+
+    for _ in range(args.warmup * copies):
+        one()
+    ms = time_steps(one, 4 * copies)
+    med, lo, hi = bootstrap_median_ci(step_samples(one, 4 * copies))
+    w12.w12_check_status()
+    out["single"] = {"shape": "1024x1024", "M": 1, "us": round(ms * 1e3, 3), "median_us": round(med * 1e3, 3),
+                     "ci95_us": [round(lo * 1e3, 3), round(hi * 1e3, 3)], "copies_rotated": copies,
+                     "packed_GBps": round(int(base.info.total_bytes) / (ms * 1e-3) / 1e9, 1),
+                     "kernel": w12.w12_gemm_group_launch_info([base.info], 1)["kernel_name"]}
+    del blobs
+
+    # decode kernel: W12 -> BF16 for the gate matrix (read the blob, write
+    # 2 bytes per weight)
+    gate = mats[LAYER_NAMES.index("gate")]
+    dec = torch.empty((gate.N, gate.K), dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        gate.decode(dec)
+    ms = time_steps(lambda: gate.decode(dec), 50)
+    w12.w12_check_status()
+    rw = int(gate.info.total_bytes) + 2 * gate.N * gate.K
+    out["decode"] = {"matrix": f"gate {gate.N}x{gate.K}", "us": round(ms * 1e3, 2), "read_write_bytes": rw,
+                     "GBps": round(rw / (ms * 1e-3) / 1e9, 1), "frac_of_hbm_peak": round(rw / (ms * 1e-3) / 1e9 / peak, 4)}
+    return out
 
 
 def main():

@@ -179,6 +179,17 @@ int w12_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info *info,
 
 int w12_gemm_group_workspace_size(int count, const w12_info *infos, int M, size_t *bytes);
 
+/*
+ * The plan of a grouped launch (count = 1: of a single w12_gemm): out[0..3]
+ * as w12_gemm_launch_info, out[4] which kernel runs it (W12_KERNEL_*).
+ */
+#define W12_KERNEL_GEMV 0     /* CUDA cores, two CTAs per SM                 */
+#define W12_KERNEL_GEMV_SM 1  /* CUDA cores, one CTA per SM                  */
+#define W12_KERNEL_TC 2       /* tcgen05, several CTAs per SM, fixed split-K */
+#define W12_KERNEL_TC_SM 3    /* tcgen05, one CTA per SM, stream-K ranges    */
+
+int w12_gemm_group_launch_info(int count, const w12_info *infos, int M, int32_t out[5]);
+
 int w12_gemm_group(const uint16_t *x_dev, int count, const void *const *blobs_dev, const w12_info *infos,
                    uint16_t *const *y_devs, int M, void *workspace, size_t ws_bytes, void *stream);
 

@@ -202,6 +202,27 @@ int check_group(int count, const w12_info *infos, std::string &err) {
 }
 }  // namespace
 
+int w12_gemm_group_launch_info(int count, const w12_info *infos, int M, int32_t out[5]) {
+    return guarded([&](std::string &err) {
+        int rc = check_group(count, infos, err);
+        if (rc != W12_OK) return rc;
+        if (!out) {
+            err = "out is null";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        w12::launch::GemmPlan plan;
+        rc = w12::launch::group_plan(count, infos, M, &plan, &err);
+        if (rc == W12_OK) {
+            out[0] = plan.ntok;
+            out[1] = plan.splits;
+            out[2] = plan.ctas;
+            out[3] = plan.ctas_per_sm;
+            out[4] = plan.kernel;
+        }
+        return rc;
+    });
+}
+
 int w12_gemm_group_workspace_size(int count, const w12_info *infos, int M, size_t *bytes) {
     return guarded([&](std::string &err) {
         int rc = check_group(count, infos, err);

@@ -369,6 +369,7 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     }
     const int64_t splits = plan->splits;
     plan->ctas_per_sm = occ;
+    plan->kernel = plan->gemv_sm ? W12_KERNEL_GEMV_SM : plan->gemv ? W12_KERNEL_GEMV : W12_KERNEL_TC;
     const int64_t k8 = (info.K + 7) / 8 * 8;
     plan->ws_counters = 0;
     plan->ws_partials = up256((size_t)tiles * 4);
@@ -487,6 +488,10 @@ int q8_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_q8_info &info
 int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,
          void *workspace, size_t ws_bytes, void *stream, std::string *err) {
     return gemm_impl(x_dev, blob_dev, info, y_dev, nullptr, M, workspace, ws_bytes, stream, err);
+}
+
+int group_plan(int count, const w12_info *infos, int M, GemmPlan *plan, std::string *err) {
+    return plan_gemm(group_info(count, infos), M, plan, err);
 }
 
 int group_workspace_size(int count, const w12_info *infos, int M, size_t *bytes, std::string *err) {

@@ -19,11 +19,14 @@ struct GemmPlan {
     int ctas = 0;           // grid size
     int64_t units = 0;      // stream-K: tiles x segments shared by the ctas (0: fixed split-K)
     int ctas_per_sm = 0;    // resident CTAs per SM the plan assumed
+    int kernel = 0;         // W12_KERNEL_* of include/w12.h
     size_t ws_counters = 0, ws_partials = 0, ws_x = 0;  // workspace offsets
     size_t ws_bytes = 0;
 };
 
 int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, bool q8 = false);
+
+int group_plan(int count, const w12_info *infos, int M, GemmPlan *plan, std::string *err);
 
 int q8_workspace_size(const w12_q8_info &info, int M, size_t *bytes, std::string *err);
 

@@ -25,7 +25,7 @@ STATUS_NAMES = {
 EXPORTED = (
     "w12_last_error", "w12_status_string", "w12_format_version", "w12_encoded_size_host", "w12_encode_host",
     "w12_blob_info", "w12_blob_validate", "w12_decode", "w12_gemm_workspace_size", "w12_gemm_launch_info",
-    "w12_gemm", "w12_gemm_group_workspace_size", "w12_gemm_group", "w12_gemm_argmax_workspace_size", "w12_gemm_argmax", "w12_gemm_noalloc", "w12_encode_workspace_size", "w12_encoded_size_device", "w12_encode_device",
+    "w12_gemm", "w12_gemm_group_workspace_size", "w12_gemm_group", "w12_gemm_group_launch_info", "w12_gemm_argmax_workspace_size", "w12_gemm_argmax", "w12_gemm_noalloc", "w12_encode_workspace_size", "w12_encoded_size_device", "w12_encode_device",
     "w12_q8_encoded_size", "w12_q8_encode_host", "w12_q8_blob_info", "w12_q8_gemm_workspace_size", "w12_q8_gemm",
     "w12_check_status", "w12_selftest_timeout", "w12_set_option", "w12_get_option",
 )
@@ -91,6 +91,7 @@ def lib() -> ctypes.CDLL:
     L.w12_gemm_launch_info.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(ctypes.c_int32)]
     L.w12_gemm.argtypes = [vp, vp, ctypes.POINTER(w12_info), vp, i32, vp, sz, vp]
     L.w12_gemm_group_workspace_size.argtypes = [i32, ctypes.POINTER(w12_info), i32, ctypes.POINTER(sz)]
+    L.w12_gemm_group_launch_info.argtypes = [i32, ctypes.POINTER(w12_info), i32, ctypes.POINTER(ctypes.c_int32)]
     L.w12_gemm_group.argtypes = [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(w12_info), ctypes.POINTER(vp), i32, vp,
                                  sz, vp]
     L.w12_gemm_argmax_workspace_size.argtypes = [ctypes.POINTER(w12_info), i32, ctypes.POINTER(sz)]
@@ -212,6 +213,18 @@ def w12_gemm_group_workspace_size(infos, M: int) -> int:
     out = ctypes.c_size_t()
     _check(lib().w12_gemm_group_workspace_size(len(infos), _infos(infos), int(M), ctypes.byref(out)))
     return out.value
+
+
+KERNEL_NAMES = {0: "w12_gemv_kernel", 1: "w12_gemv_sm_kernel", 2: "w12_gemm_tc_kernel", 3: "w12_gemm_tc_sm_kernel"}
+
+
+def w12_gemm_group_launch_info(infos, M: int) -> dict:
+    """Plan of a grouped launch (one info: a single w12_gemm), with the name
+    of the kernel that runs it."""
+    out = (ctypes.c_int32 * 5)()
+    _check(lib().w12_gemm_group_launch_info(len(infos), _infos(infos), int(M), out))
+    return {"ntok": out[0], "splits": out[1], "ctas": out[2], "ctas_per_sm": out[3], "kernel": out[4],
+            "kernel_name": KERNEL_NAMES.get(out[4], str(out[4]))}
 
 
 def w12_gemm_group_ptr(x_ptr: int, blob_ptrs, infos, y_ptrs, M: int, ws_ptr: int, ws_bytes: int,

@@ -238,3 +238,31 @@ def test_two_token_paths(case, M, gemv_max_m):
     ntok = w12.w12_gemm_launch_info(mat.info, M)["ntok"]
     assert ntok == (2 if M <= gemv_max_m else 32)
     check_tolerance(_gemm(mat, x), oracle.gemm_f64(x, w), f"{case} M={M} ntok={ntok}")
+
+
+@pytest.mark.parametrize("M", [16, 32])
+@pytest.mark.parametrize("kernel", ["tc", "gemv"])
+def test_subnormal_weights_one_hot(M, kernel, w12_opts):
+    """Weights with subnormal BF16 patterns (exponent 0, mantissa != 0, both
+    signs) through a one-hot x: the product must return each weight bit for
+    bit, so subnormal inputs are neither flushed by the tensor pipe nor by
+    the CUDA-core multiply-add, and the fp32 accumulator keeps them."""
+    if kernel == "gemv":
+        M = 2
+        w12_opts(gemv_max_m=2)
+    rng = np.random.default_rng(50 + M)
+    w = wl.gaussian_weights(256, 1024, seed=51)
+    sub = rng.integers(1, 128, size=(256, 1024)).astype(np.uint16) | (rng.integers(0, 2, size=(256, 1024))
+                                                                        .astype(np.uint16) << 15)
+    pick = rng.random((256, 1024)) < 0.5
+    w = np.where(pick, sub, w).astype(np.uint16)
+    ks = np.sort(rng.choice(1024, size=M, replace=False))
+    x = np.zeros((M, 1024), dtype=np.uint16)
+    x[np.arange(M), ks] = 0x3F80  # 1.0
+    mat = W12Weight(w)
+    assert (w12.w12_gemm_launch_info(mat.info, M)["ntok"] <= 2) == (kernel == "gemv")
+    y = _gemm(mat, x)
+    for i, k in enumerate(ks):
+        col = w[:, k]
+        assert np.count_nonzero(((col >> 7) & 0xFF) == 0) > 50
+        assert np.array_equal(y[i], col), f"column {k}: {np.count_nonzero(y[i] != col)} differ"
