@@ -356,6 +356,9 @@ int w12_check_status(void *stream);
  *                               kernel's per-CTA limits allow it
  *   pdl             (1; 0..1)   programmatic dependent launch on GEMMs
  *   timeout_ms      (4000; 1..600000) bounded waits give up after this
+ *   tc_sm           (1; 0..1)   tensor-core path: 1 one CTA per SM walking
+ *                               stream-K ranges (A operand in TMEM), 0 several
+ *                               CTAs per SM with fixed split-K
  * INVALID_ARG for an unknown name or a value out of range (nothing changes).
  */
 int w12_set_option(const char *name, int64_t value);

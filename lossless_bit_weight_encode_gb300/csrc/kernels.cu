@@ -14,6 +14,7 @@
 #include "decode.cuh"
 #include "encode_gpu.cuh"
 #include "gemm_tc.cuh"
+#include "gemm_tc_sm.cuh"
 #include "gemv.cuh"
 #include "gemv_sm.cuh"
 #include "w12_host.hpp"
@@ -77,6 +78,7 @@ struct DeviceState {
     int q8_occupancy[2] = {0, 0};            // [ntok==32], Q8 copy kernels
     int gemv_occupancy[2] = {0, 0};          // GEMV with 1, 2 token rows
     int gemv_sm_occupancy[2] = {0, 0};       // one-CTA-per-SM GEMV with 1, 2 token rows
+    int tc_sm_occupancy[2] = {0, 0};         // one-CTA-per-SM tensor-core kernel, [ntok==32]
 };
 
 DeviceState g_state[kMaxDevices];
@@ -178,6 +180,22 @@ int prepare_gemv_sm(DeviceState &s, std::string *err) {
     return W12_OK;
 }
 
+template <int NTOK>
+int prepare_tc_sm(DeviceState &s, std::string *err) {
+    using C = dev::TcSmCfg<NTOK>;
+    void *k = reinterpret_cast<void *>(&dev::w12_gemm_tc_sm_kernel<NTOK>);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(tc_sm)", err);
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(tc_sm carveout)", err);
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, C::kThreads, (size_t)C::kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(tc_sm)", err);
+    // all 512 TMEM columns: one CTA per SM whatever else would fit
+    s.tc_sm_occupancy[NTOK == 32] = occ < 1 ? occ : 1;
+    return W12_OK;
+}
+
 // Per-device set-up on first use (with that device current).
 int device_state(DeviceState **out, std::string *err) {
     int dev = 0;
@@ -211,6 +229,8 @@ int device_state(DeviceState **out, std::string *err) {
         if (rc == W12_OK) rc = prepare_gemm<32, false>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<16, true>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<32, true>(s, err);
+        if (rc == W12_OK) rc = prepare_tc_sm<16>(s, err);
+        if (rc == W12_OK) rc = prepare_tc_sm<32>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<16, false, true>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<32, false, true>(s, err);
         if (rc != W12_OK) return rc;
@@ -247,9 +267,22 @@ OptionSlot g_options[] = {
     {"pdl", 1, 0, 1, {1}},
     // bounded waits give up after this many milliseconds
     {"timeout_ms", 4000, 1, 600000, {4000}},
+    // tensor-core path: 1 one CTA per SM (stream-K ranges), 0 several CTAs per
+    // SM with fixed split-K
+    {"tc_sm", 1, 0, 1, {1}},
 };
 
-enum OptionId { kOptGemvMaxM, kOptTokenTile, kOptASmem, kOptGemvSm, kOptStreamK, kOptSplits, kOptPdl, kOptTimeout };
+enum OptionId {
+    kOptGemvMaxM,
+    kOptTokenTile,
+    kOptASmem,
+    kOptGemvSm,
+    kOptStreamK,
+    kOptSplits,
+    kOptPdl,
+    kOptTimeout,
+    kOptTcSm
+};
 
 int64_t opt(OptionId id) { return g_options[id].value.load(std::memory_order_relaxed); }
 
@@ -270,6 +303,14 @@ int tc_token_tile(int M, int64_t tiles, int sm_count) {
 }
 
 bool use_smem_a_operand() { return opt(kOptASmem) != 0; }
+
+// The one-CTA-per-SM tensor-core kernel (gemm_tc_sm.cuh) takes its A operand
+// from TMEM only; the shared-memory A variant stays on the several-CTA kernel.
+bool use_tc_sm() { return opt(kOptTcSm) != 0 && !use_smem_a_operand(); }
+
+// Token tile of the one-CTA-per-SM tensor-core kernel: the narrowest MMA
+// (N = 16) that holds M tokens, unless token_tile forces 32.
+int tc_sm_token_tile(int M) { return (M > 16 || opt(kOptTokenTile) == 32) ? 32 : 16; }
 
 // Which CUDA-core kernel: one CTA per SM with sixteen decode warps (gemv_sm.cuh)
 // or two with eight each (gemv.cuh).  The first keeps every warp of an SM busy
@@ -323,16 +364,23 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     if (rc != W12_OK) return rc;
     plan->gemv = !q8 && use_gemv(M);
     plan->gemv_sm = plan->gemv && use_gemv_sm(info, s->sm_count);
-    plan->ntok = plan->gemv ? M : tc_token_tile(M, info.tiles, s->sm_count);
+    plan->tc_sm = !plan->gemv && !q8 && use_tc_sm();
+    plan->ntok = plan->gemv ? M : plan->tc_sm ? tc_sm_token_tile(M) : tc_token_tile(M, info.tiles, s->sm_count);
     const int occ = plan->gemv_sm ? s->gemv_sm_occupancy[M - 1]
                     : plan->gemv  ? s->gemv_occupancy[M - 1]
+                    : plan->tc_sm ? s->tc_sm_occupancy[plan->ntok == 32]
                     : q8          ? s->q8_occupancy[plan->ntok == 32]
                                   : s->occupancy[plan->ntok == 32][use_smem_a_operand()];
     if (occ < 1) {
         *err = "GEMM kernel cannot be resident on this device";
         return W12_ERR_CUDA;
     }
-    const int64_t kMaxSegs = plan->gemv_sm ? dev::GemvSmCfg<1>::kMaxSegs : dev::GemmCfg<16, kStages, false>::kMaxSegs;
+    const int64_t kMaxSegs = plan->gemv_sm ? dev::GemvSmCfg<1>::kMaxSegs
+                             : plan->tc_sm ? dev::TcSmCfg<16>::kMaxSegs
+                                           : dev::GemmCfg<16, kStages, false>::kMaxSegs;
+    static_assert(dev::TcSmCfg<16>::kMaxSegs == dev::TcSmCfg<32>::kMaxSegs &&
+                      dev::TcSmCfg<16>::kMaxPieces == dev::TcSmCfg<32>::kMaxPieces,
+                  "one range limit for both token tiles");
     const int64_t capacity = (int64_t)s->sm_count * occ;
     const int64_t tiles = info.tiles, segs = info.segs;
     const int64_t forced = opt(kOptSplits);  // tuning override: fixed split-K
@@ -344,12 +392,14 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     // the range of a CTA: at most kMaxSegs segment headers and, for the
     // one-CTA-per-SM kernel, at most kMaxPieces tiles; for the two-CTA kernel
     // at most two tiles (a single wave of more CTAs than tiles)
-    const int64_t max_range = plan->gemv_sm ? std::min<int64_t>(kMaxSegs, (dev::GemvSmCfg<1>::kMaxPieces - 1) * segs + 1)
-                                            : kMaxSegs;
+    const int64_t max_range =
+        plan->gemv_sm  ? std::min<int64_t>(kMaxSegs, (dev::GemvSmCfg<1>::kMaxPieces - 1) * segs + 1)
+        : plan->tc_sm ? std::min<int64_t>(kMaxSegs, (dev::TcSmCfg<16>::kMaxPieces - 1) * segs + 1)
+                      : kMaxSegs;
     if ((units + sk_ctas - 1) / sk_ctas > max_range) sk_ctas = (units + max_range - 1) / max_range;
-    const bool sk_shape = plan->gemv_sm || tiles < capacity;
+    const bool sk_shape = plan->gemv_sm || plan->tc_sm || tiles < capacity;
     // (the device computes unit x ctas products in 32 bits)
-    if (plan->gemv && forced == 0 && sk_shape && units * sk_ctas < (int64_t(1) << 31) && use_stream_k()) {
+    if ((plan->gemv || plan->tc_sm) && forced == 0 && sk_shape && units * sk_ctas < (int64_t(1) << 31) && use_stream_k()) {
         const int64_t shortest = units / sk_ctas;  // units of the shortest range
         plan->units = units;
         // most ranges one tile can meet: the one holding its first unit plus
@@ -369,7 +419,10 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     }
     const int64_t splits = plan->splits;
     plan->ctas_per_sm = occ;
-    plan->kernel = plan->gemv_sm ? W12_KERNEL_GEMV_SM : plan->gemv ? W12_KERNEL_GEMV : W12_KERNEL_TC;
+    plan->kernel = plan->gemv_sm ? W12_KERNEL_GEMV_SM
+                   : plan->gemv  ? W12_KERNEL_GEMV
+                   : plan->tc_sm ? W12_KERNEL_TC_SM
+                                 : W12_KERNEL_TC;
     const int64_t k8 = (info.K + 7) / 8 * 8;
     plan->ws_counters = 0;
     plan->ws_partials = up256((size_t)tiles * 4);
@@ -632,6 +685,14 @@ int gemm_impl(const uint16_t *x_dev, int count, const void *const *blobs, const 
         else
             e = launch_overlapped(dev::w12_gemv_kernel<kGemvStages, kGemvChunks, 2>, grid, dim3(GemvC<2>::kThreads),
                                   (size_t)GemvC<2>::kSmemBytes, st, p, tm);
+    } else if (plan.tc_sm) {
+        const dim3 grid = plan.units > 0 ? dim3((unsigned)plan.ctas, 1u) : dim3((unsigned)plan.splits, (unsigned)info.tiles);
+        if (plan.ntok == 16)
+            e = launch_overlapped(dev::w12_gemm_tc_sm_kernel<16>, grid, dim3(dev::TcSmCfg<16>::kThreads),
+                                  (size_t)dev::TcSmCfg<16>::kSmemBytes, st, p, tm);
+        else
+            e = launch_overlapped(dev::w12_gemm_tc_sm_kernel<32>, grid, dim3(dev::TcSmCfg<32>::kThreads),
+                                  (size_t)dev::TcSmCfg<32>::kSmemBytes, st, p, tm);
     } else if (q8) {
         e = plan.ntok == 16 ? launch_gemm_kernel<16, false, true>(p, tm, plan.splits, info.tiles, st)
                             : launch_gemm_kernel<32, false, true>(p, tm, plan.splits, info.tiles, st);

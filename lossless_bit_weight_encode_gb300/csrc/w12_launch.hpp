@@ -14,6 +14,7 @@ namespace launch {
 struct GemmPlan {
     bool gemv = false;      // one token on CUDA cores instead of tensor cores
     bool gemv_sm = false;   // the CUDA-core kernel with one CTA per SM
+    bool tc_sm = false;     // the tensor-core kernel with one CTA per SM
     int ntok = 16;          // MMA token width (16 or 32)
     int splits = 1;         // CTAs per tile along K (stream-K: the most CTAs sharing a tile)
     int ctas = 0;           // grid size

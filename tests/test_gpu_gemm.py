@@ -11,8 +11,10 @@ from lossless_bit_weight_encode_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-A_OPERANDS = ["tmem", "smem"]
-TOKEN_TILES = ["32", "16"]
+# tensor-core variants: (kernel, A operand, token tile); "sm" is the
+# one-CTA-per-SM kernel (A in TMEM), "multi" the several-CTA kernel
+TC_VARIANTS = [("sm", "tmem", "32"), ("sm", "tmem", "16"), ("multi", "tmem", "32"), ("multi", "tmem", "16"),
+               ("multi", "smem", "32"), ("multi", "smem", "16")]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -21,10 +23,12 @@ def built():
     ensure_built()
 
 
-@pytest.fixture(params=[(a, t) for a in A_OPERANDS for t in TOKEN_TILES], ids=lambda v: f"{v[0]}-ntok{v[1]}")
+@pytest.fixture(params=TC_VARIANTS, ids=lambda v: f"{v[0]}-{v[1]}-ntok{v[2]}")
 def a_operand(request, w12_opts):
-    """Every tensor-core variant: A in TMEM or SMEM, 32- or 16-token tile."""
-    w12_opts(a_operand_smem=request.param[0] == "smem", token_tile=int(request.param[1]))
+    """Every tensor-core variant: one CTA per SM or several, A in TMEM or
+    SMEM, 32- or 16-token tile."""
+    kernel, a, ntok = request.param
+    w12_opts(tc_sm=kernel == "sm", a_operand_smem=a == "smem", token_tile=int(ntok))
     return request.param
 
 

@@ -43,8 +43,10 @@ def test_single_layer_encode_and_decode_bit_exact(case):
 PATHS = {
     "gemv_sm": dict(gemv_sm=1),
     "gemv": dict(gemv_sm=0),
-    "tc32": dict(gemv_max_m=0, token_tile=32),
-    "tc16": dict(gemv_max_m=0, token_tile=16),
+    "tc_sm32": dict(gemv_max_m=0, token_tile=32),
+    "tc_sm16": dict(gemv_max_m=0, token_tile=16),
+    "tc32": dict(gemv_max_m=0, token_tile=32, tc_sm=0),
+    "tc16": dict(gemv_max_m=0, token_tile=16, tc_sm=0),
     "tc32_smem_a": dict(gemv_max_m=0, token_tile=32, a_operand_smem=1),
 }
 

@@ -210,7 +210,7 @@ def test_launch_options_set_get_and_reject(monkeypatch):
     named like an option has no effect."""
     from lossless_bit_weight_encode_gb300 import w12
     defaults = {"gemv_max_m": 2, "token_tile": 0, "a_operand_smem": 0, "gemv_sm": -1, "stream_k": 1,
-                "splits": 0, "pdl": 1, "timeout_ms": 4000}
+                "splits": 0, "pdl": 1, "timeout_ms": 4000, "tc_sm": 1}
     for name, v in defaults.items():
         assert w12.w12_get_option(name) == v, name
     monkeypatch.setenv("W12_NTOK", "16")
