@@ -474,11 +474,13 @@ def sweep_point(mats, weights, xs_host, M, K, warmup, dense, q8=False):
     ms = time_steps(st.run, K)
     st.w12.w12_check_status()
     med, lo, hi = bootstrap_median_ci(step_samples(st.run, max(50, K)))
+    lt = launch_times(st, 20)
     st.w12.w12_check_status()
     out = {"us_per_layer": round(ms * 1e3, 2), "median_us": round(med * 1e3, 2),
            "ci95_us": [round(lo * 1e3, 2), round(hi * 1e3, 2)],
            "packed_frac_of_hbm_peak": round(st.packed / (ms * 1e-3) / 1e9 / peak, 4),
-           "kernels": sorted(set(st.kernels))}
+           "kernels": sorted(set(st.kernels)),
+           "per_launch_us": {n: round(v * 1e3, 2) for n, v in zip(st.launch_names, lt)}}
     if dense is not None:
         b = cublas_ms(dense, st.groups, st.xs, K, warmup)
         out["bf16_cublas_us"] = round(b * 1e3, 2)

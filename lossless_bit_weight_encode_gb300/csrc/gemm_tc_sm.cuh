@@ -16,24 +16,29 @@
 // stream-K range of (tile, segment) units, so one wave covers the launch
 // with equal work per SM whatever the tile count.
 //
-// Warp roles (704 threads):
+// Warp roles (736 threads):
 //   warps 0-15  decode: warp w handles rows 32q..32q+31 (q = w mod 4, the TMEM
 //               lanes its warp may touch) and chunks 2j, 2j+1 of each segment
 //               (j = w / 4); per stage a thread reads its row's S bytes and
 //               codes of its two chunks from SMEM, decodes 64 weights,
 //               patches escapes and stores them as 32 columns of BF16 pairs
 //               into a TMEM A slot (one slot per segment, 128 columns);
-//   warp 16     producer: cp.async.bulk for the segment headers and each
-//               weight stage; per segment cp.async.bulk.tensor for the x tile
-//               (four 64-column boxes, 128-byte swizzle) and cp.async.bulk for
-//               the escape bytes;
+//   warp 16     weight producer: cp.async.bulk for the segment headers, each
+//               weight stage and each segment's escape bytes (their own ring,
+//               one slot deeper than the weight ring, so the weight stage is
+//               free as soon as the decoders have read it and an escape slot
+//               is known free when the following weight stage is);
 //   warp 17     allocates TMEM (all 512 columns); one lane issues the 16
 //               MMAs of a segment (K = 16 each) into the piece's accumulator
 //               and tcgen05.commit;
 //   warps 18-21 epilogue: one warp per TMEM lane quarter drains a finished
 //               piece's accumulator (two accumulators alternate, so the MMAs
 //               of the next piece do not wait) and writes y, or the piece's
-//               partial-sum slot when the tile is shared with other CTAs.
+//               partial-sum slot when the tile is shared with other CTAs;
+//   warp 22     x loader: per segment cp.async.bulk.tensor for the x tile
+//               (four 64-column boxes, 128-byte swizzle) into a ring of its
+//               own, whose slots the MMAs free; kept apart from the weight
+//               producer so that no weight stage waits for an MMA.
 // A range's first and last pieces may share their tile; their arrivals are
 // made once at the end and the last arrival adds the tile's slots in slot
 // order, so results repeat run to run.  Every wait is bounded: on expiry the
@@ -54,12 +59,16 @@ struct TcSmCfg {
     static constexpr int kMmaWarp = 17;
     static constexpr int kEpiWarp0 = 18;  // warps 18..21 cover lane quarters 2, 3, 0, 1
     static constexpr int kEpiWarps = 4;
-    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+    static constexpr int kXWarp = 22;
+    static constexpr int kThreads = (kXWarp + 1) * 32;
+    static constexpr int kFinishThreads = (kDecWarps + kEpiWarps) * 32;  // share the split-K finish
     static constexpr int kStages = 3;                            // weight ring: one segment per stage
+    static constexpr int kL2Ahead = 3;                           // segments pulled into L2 ahead of the ring
     static constexpr int kWBytes = kChunksPerSeg * kChunkBytes;  // 48 KB
     static constexpr int kXBoxBytes = NTOK * 128;                // 64 columns x NTOK tokens
     static constexpr int kXBytes = 4 * kXBoxBytes;               // x tile of one segment
-    static constexpr int kSegSlots = NTOK == 32 ? 3 : 4;         // x + escapes, one segment each
+    static constexpr int kXSlots = 4;                            // x ring
+    static constexpr int kESlots = 4;                            // escape-byte ring, one deeper than the weights
     static constexpr int kEscCap = 2048;
     static constexpr int kASlots = 3;                            // TMEM A slots, one segment each
     static constexpr int kMaxSegs = 192;                         // units (segments) of one CTA
@@ -68,13 +77,13 @@ struct TcSmCfg {
     static constexpr int kDCol = 0;                              // accumulators at columns 0 and 32
     static constexpr int kACol = 64;                             // A slot s at 64 + 128 s
     static constexpr int kOffX = 0;                              // 1024-aligned (swizzle atoms)
-    static constexpr int kOffW = kOffX + kSegSlots * kXBytes;
+    static constexpr int kOffW = kOffX + kXSlots * kXBytes;
     static constexpr int kOffEsc = kOffW + kStages * kWBytes;
-    static constexpr int kOffHdr = kOffEsc + kSegSlots * kEscCap;
+    static constexpr int kOffHdr = kOffEsc + kESlots * kEscCap;
     static constexpr int kOffBars = kOffHdr + kMaxSegs * kSegHdrBytes;
-    // wfull[S], wempty[S], sfull[X], sempty[X], afull[A], aempty[A], dfull[2],
-    // dempty[2], hdr, drain, epi_in, epi_out
-    static constexpr int kNumBars = 2 * kStages + 2 * kSegSlots + 2 * kASlots + 4 + 4;
+    // wfull[S], wempty[S], efull[E], xfull[X], xempty[X], afull[A],
+    // aempty[A], dfull[2], dempty[2], hdr, drain, epi_in, epi_out
+    static constexpr int kNumBars = 2 * kStages + kESlots + 2 * kXSlots + 2 * kASlots + 4 + 4;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
     static constexpr int kOffPieces = kOffMisc + 64;
     static constexpr int kSmemBytes = kOffPieces + kMaxPieces * (int)sizeof(Piece) + 1024;  // + alignment slack
@@ -83,20 +92,22 @@ struct TcSmCfg {
     static_assert(kOffW % 128 == 0 && kOffEsc % 16 == 0 && kOffHdr % 16 == 0, "copy destinations aligned");
     static_assert(kACol + kASlots * 128 <= kTmemCols && kDCol + 64 <= kACol, "TMEM columns");
     static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM must fit");
+    static_assert(kESlots == kStages + 1, "an escape slot is reused once the next weight stage is released");
 };
 
 struct TcSmBars {
-    uint64_t *wfull, *wempty, *sfull, *sempty, *afull, *aempty, *dfull, *dempty, *hdr, *drain, *epi_in, *epi_out;
+    uint64_t *wfull, *wempty, *efull, *xfull, *xempty, *afull, *aempty, *dfull, *dempty, *hdr, *drain, *epi_in,
+        *epi_out;
 };
 
-// ------------------------------------------------------------------ producer
+// ------------------------------------------------------------------ producers
+// Weights: the segment headers of the whole range, then per segment its
+// packed chunks (one stage) and its escape bytes (one escape slot; only the
+// headers decide them, so they need nothing from the other rings).
 template <class C>
-__device__ void tcsm_producer(const GemmGroup &g, const Piece *pieces, int npieces, const CUtensorMap *tmap,
-                              uint8_t *smem, const TcSmBars &b, volatile uint32_t *abort_flag, uint64_t deadline) {
+__device__ void tcsm_producer(const GemmGroup &g, const Piece *pieces, int npieces, uint8_t *smem,
+                              const TcSmBars &b, volatile uint32_t *abort_flag, uint64_t deadline) {
     uint8_t *hdr = smem + C::kOffHdr;
-    prefetch_tmap(tmap);
-
-    // the segment headers of every piece, one after another, on one phase
     uint32_t hbytes = 0;
     for (int k = 0; k < npieces; ++k) hbytes += (uint32_t)(pieces[k].s1 - pieces[k].s0) * kSegHdrBytes;
     mbar_arrive_expect_tx(b.hdr, hbytes);
@@ -108,18 +119,23 @@ __device__ void tcsm_producer(const GemmGroup &g, const Piece *pieces, int npiec
         off += (int)n;
     }
 
-    bool hdr_ready = false, failed = false, stop = false;
-    int gw = 0, gx = 0;  // weight stages and x slots issued (one each per segment)
+    // the L2 cursor runs kL2Ahead segments ahead of the weight issue (the
+    // first two segments were warmed before the grid wait)
+    SegCursor l2 = seg_cursor(pieces, npieces);
+    for (int i = 0; i < C::kL2Ahead; ++i) seg_cursor_next<kChunkBytes>(g, pieces, npieces, l2, i >= 2);
+
+    bool hdr_ready = false, failed = false;
+    int gw = 0, ge = 0;  // weight stages and escape slots issued (one each per segment)
     int hseg = 0;        // headers of the earlier pieces
-    for (int k = 0; !stop && k < npieces; ++k) {
+    for (int k = 0; !failed && k < npieces; ++k) {
         const Piece &pc = pieces[k];
         const GemmParams &p = g.m[pc.member];
         for (int sg = pc.s0; sg < pc.s1; ++sg) {
             const int chunk = sg * kChunksPerSeg;
             const int nch = min(kChunksPerSeg, p.chunks - chunk);
-            const int wslot = gw % C::kStages;
+            const int wslot = gw % C::kStages, eslot = ge % C::kESlots;
             if (gw >= C::kStages && !mbar_wait(b.wempty + wslot, (uint32_t)(gw / C::kStages - 1) & 1u, deadline)) {
-                failed = stop = true;
+                failed = true;
                 break;
             }
             mbar_arrive_expect_tx(b.wfull + wslot, (uint32_t)(nch * kChunkBytes));
@@ -127,55 +143,83 @@ __device__ void tcsm_producer(const GemmGroup &g, const Piece *pieces, int npiec
                      p.blob + p.off_w + (uint64_t)(pc.tile * p.chunks + chunk) * kChunkBytes,
                      (uint32_t)(nch * kChunkBytes), b.wfull + wslot);
             ++gw;
-            // the segment's x tile (no header needed), then its escapes; the
-            // one arrival comes last so the phase cannot complete early
-            const int xslot = gx % C::kSegSlots;
-            if (gx >= C::kSegSlots &&
-                !mbar_wait(b.sempty + xslot, (uint32_t)(gx / C::kSegSlots - 1) & 1u, deadline)) {
-                failed = stop = true;
-                break;
-            }
-            mbar_expect_tx(b.sfull + xslot, (uint32_t)C::kXBytes);
-            uint8_t *xs = smem + C::kOffX + xslot * C::kXBytes;
-#pragma unroll
-            for (int bx = 0; bx < 4; ++bx)
-                tma_load_2d(xs + bx * C::kXBoxBytes, tmap, chunk * kChunkK + bx * 64, 0, b.sfull + xslot);
-            ++gx;
+            seg_cursor_next<kChunkBytes>(g, pieces, npieces, l2, true);
             if (!hdr_ready) {
                 if (!mbar_wait(b.hdr, 0, deadline)) {
-                    mbar_arrive(b.sfull + xslot);  // lets the phase end once x has landed
-                    failed = stop = true;
+                    failed = true;
                     break;
                 }
                 hdr_ready = true;
             }
+            // escape slot gs mod kESlots last held segment gs - kESlots; every
+            // decoder finished it before loading segment gs - kESlots + 1,
+            // whose weight stage this thread has just seen released (the ring
+            // is one stage shorter than the escape slots), so it is free
             const uint4 meta = *reinterpret_cast<const uint4 *>(hdr + (hseg + sg - pc.s0) * kSegHdrBytes + 16);
             const uint32_t base = meta.x;
             const uint32_t total = seg_escape_total(meta);
             if (escapes_staged<C>(total)) {
                 const uint32_t src0 = base & ~15u;
                 const uint32_t ebytes = ((base + total + 15u) & ~15u) - src0;
-                mbar_expect_tx(b.sfull + xslot, ebytes);
-                bulk_g2s(smem + C::kOffEsc + xslot * C::kEscCap, p.blob + p.off_esc + src0, ebytes,
-                         b.sfull + xslot);
+                mbar_arrive_expect_tx(b.efull + eslot, ebytes);
+                bulk_g2s(smem + C::kOffEsc + eslot * C::kEscCap, p.blob + p.off_esc + src0, ebytes, b.efull + eslot);
+            } else {
+                mbar_arrive(b.efull + eslot);
             }
-            mbar_arrive(b.sfull + xslot);
+            ++ge;
             if (*abort_flag) {
-                stop = true;
+                failed = true;
                 break;
             }
         }
         hseg += pc.s1 - pc.s0;
     }
-    if (failed) raise_timeout(group_status(g), abort_flag);
-    if (*abort_flag) {
+    if (failed && !*abort_flag) raise_timeout(group_status(g), abort_flag);
+    if (failed) {
         // let every copy still in flight land before the CTA can exit
         const uint64_t drain_deadline = globaltimer_ns() + 1000000000ull;
         for (int st = max(0, gw - C::kStages); st < gw; ++st)
             mbar_wait(b.wfull + st % C::kStages, (uint32_t)(st / C::kStages) & 1u, drain_deadline);
-        for (int sx = max(0, gx - C::kSegSlots); sx < gx; ++sx)
-            mbar_wait(b.sfull + sx % C::kSegSlots, (uint32_t)(sx / C::kSegSlots) & 1u, drain_deadline);
         mbar_wait(b.hdr, 0, drain_deadline);
+        for (int se = max(0, ge - C::kESlots); se < ge; ++se)
+            mbar_wait(b.efull + se % C::kESlots, (uint32_t)(se / C::kESlots) & 1u, drain_deadline);
+    }
+}
+
+// x: per segment the 256-column tile of the token rows (four 64-column boxes,
+// 128-byte swizzle, rows past M and columns past K zero-filled by the tensor
+// copy); a slot is free again once the MMAs that read it have completed.
+template <class C>
+__device__ void tcsm_x_loader(const GemmGroup &g, const Piece *pieces, int npieces, const CUtensorMap *tmap,
+                              uint8_t *smem, const TcSmBars &b, volatile uint32_t *abort_flag, uint64_t deadline) {
+    prefetch_tmap(tmap);
+    bool failed = false;
+    int gs = 0;
+    for (int k = 0; !failed && k < npieces; ++k) {
+        const Piece &pc = pieces[k];
+        for (int sg = pc.s0; sg < pc.s1; ++sg) {
+            const int xslot = gs % C::kXSlots;
+            if (gs >= C::kXSlots && !mbar_wait(b.xempty + xslot, (uint32_t)(gs / C::kXSlots - 1) & 1u, deadline)) {
+                failed = true;
+                break;
+            }
+            mbar_arrive_expect_tx(b.xfull + xslot, (uint32_t)C::kXBytes);
+            uint8_t *xs = smem + C::kOffX + xslot * C::kXBytes;
+#pragma unroll
+            for (int bx = 0; bx < 4; ++bx)
+                tma_load_2d(xs + bx * C::kXBoxBytes, tmap, sg * kSegK + bx * 64, 0, b.xfull + xslot);
+            ++gs;
+            if (*abort_flag) {
+                failed = true;
+                break;
+            }
+        }
+    }
+    if (*abort_flag || failed) {
+        if (!*abort_flag) raise_timeout(group_status(g), abort_flag);
+        const uint64_t drain_deadline = globaltimer_ns() + 1000000000ull;
+        for (int sx = max(0, gs - C::kXSlots); sx < gs; ++sx)
+            mbar_wait(b.xfull + sx % C::kXSlots, (uint32_t)(sx / C::kXSlots) & 1u, drain_deadline);
     }
 }
 
@@ -204,22 +248,36 @@ __device__ void tcsm_mma(const GemmGroup &g, const Piece *pieces, int npieces, u
         const uint32_t d_taddr = tmem_base + (uint32_t)(C::kDCol + 32 * dbuf);
         for (int sg = pc.s0; sg < pc.s1; ++sg, ++gs) {
             const int nch = min(kChunksPerSeg, p.chunks - sg * kChunksPerSeg);
-            const int xslot = gs % C::kSegSlots, aslot = gs % C::kASlots;
-            if (!mbar_wait(b.sfull + xslot, (uint32_t)(gs / C::kSegSlots) & 1u, deadline) ||
+            const int xslot = gs % C::kXSlots, aslot = gs % C::kASlots;
+            if (!mbar_wait(b.xfull + xslot, (uint32_t)(gs / C::kXSlots) & 1u, deadline) ||
                 !mbar_wait(b.afull + aslot, (uint32_t)(gs / C::kASlots) & 1u, deadline)) {
                 failed = true;
                 break;
             }
             tc_fence_after();
-            const uint32_t xs = smem_u32(smem + C::kOffX + xslot * C::kXBytes);
+            // one descriptor per segment: a k-block's B starts kb / 4 boxes and
+            // 32 (kb mod 4) bytes further on, i.e. a constant added to the
+            // descriptor's start-address field (16-byte units, no carry: shared
+            // addresses stay below 2^18)
+            const uint64_t bdesc0 = smem_desc(smem_u32(smem + C::kOffX + xslot * C::kXBytes), 16u, 1024u, 2u);
             const uint32_t a_taddr = tmem_base + (uint32_t)(C::kACol + 128 * aslot);
-            for (int kb = 0; kb < 2 * nch; ++kb) {
-                const uint64_t bdesc =
-                    smem_desc(xs + (uint32_t)(kb >> 2) * C::kXBoxBytes + (uint32_t)(kb & 3) * 32u, 16u, 1024u, 2u);
-                mma_tmem_a(d_taddr, a_taddr + (uint32_t)(8 * kb), bdesc, idesc, (sg > pc.s0 || kb > 0) ? 1u : 0u);
+            const uint32_t acc0 = sg > pc.s0 ? 1u : 0u;
+            if (nch == kChunksPerSeg) {
+                // the common full segment: sixteen MMAs with constant offsets,
+                // so the issuing thread spends its issue slots on MMAs
+#pragma unroll
+                for (int kb = 0; kb < 2 * kChunksPerSeg; ++kb)
+                    mma_tmem_a(d_taddr, a_taddr + (uint32_t)(8 * kb),
+                               bdesc0 + (uint64_t)((kb >> 2) * (C::kXBoxBytes >> 4) + (kb & 3) * 2), idesc,
+                               kb > 0 ? 1u : acc0);
+            } else {
+                for (int kb = 0; kb < 2 * nch; ++kb)
+                    mma_tmem_a(d_taddr, a_taddr + (uint32_t)(8 * kb),
+                               bdesc0 + (uint64_t)((kb >> 2) * (C::kXBoxBytes >> 4) + (kb & 3) * 2), idesc,
+                               kb > 0 ? 1u : acc0);
             }
             mma_commit(b.aempty + aslot);
-            mma_commit(b.sempty + xslot);
+            mma_commit(b.xempty + xslot);
             if (*abort_flag) {
                 failed = true;
                 break;
@@ -231,6 +289,59 @@ __device__ void tcsm_mma(const GemmGroup &g, const Piece *pieces, int npieces, u
     // before TMEM can be freed every issued MMA must have completed
     mma_commit(b.drain);
     mbar_wait(b.drain, 0, globaltimer_ns() + 1000000000ull);
+}
+
+// ------------------------------------------------------------------ finish
+// The tiles whose last arrival this CTA made: each output adds the tile's
+// partial-sum slots in slot order (reproducible run to run) and is rounded to
+// BF16.  The decode and epilogue warps (kFinishThreads, reducer id rid) share
+// the outputs, four per thread per batch with up to four slots each, so that
+// up to sixteen loads per thread are in flight: this runs at the very end of
+// the kernel, when every load waits behind the weight stream of the SMs still
+// working.
+template <class C>
+__device__ void tcsm_finish(const GemmGroup &g, const Piece *pieces, int npieces, volatile uint32_t *last_flags,
+                            int rid) {
+    constexpr int kN = C::kFinishThreads;
+    for (int e = 0; e < 2; ++e) {
+        if (last_flags[e] == 0) continue;
+        const Piece &pc = pieces[e == 0 ? 0 : npieces - 1];
+        const GemmParams &p = g.m[pc.member];
+        const int total = p.M * kTileRows;
+        const int64_t stride = (int64_t)p.M * p.Npad;
+        const float *base = p.partials + pc.tile * kTileRows;
+        // a warp's 32 outputs share one token (kN and 128 are multiples of 32)
+        for (int o0 = rid; o0 < total; o0 += 4 * kN) {
+            float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int sp0 = 0; sp0 < pc.count; sp0 += 4) {
+                float v[4][4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int bb = 0; bb < 4; ++bb) {
+                        const int o = o0 + bb * kN;
+                        v[u][bb] = (sp0 + u < pc.count && o < total)
+                                       ? __ldcg(base + (int64_t)(sp0 + u) * stride + (int64_t)(o / kTileRows) * p.Npad +
+                                                o % kTileRows)
+                                       : 0.0f;
+                    }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int bb = 0; bb < 4; ++bb)
+                        if (sp0 + u < pc.count) s[bb] += v[u][bb];
+            }
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb) {
+                const int o = o0 + bb * kN;
+                if (o >= total) break;  // the same for the whole warp
+                const int t = o / kTileRows;
+                const int64_t n = pc.tile * kTileRows + o % kTileRows;
+                if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(s[bb]);
+                if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(s[bb], (uint32_t)n) : 0ull);
+            }
+        }
+    }
 }
 
 // ------------------------------------------------------------------ decoders
@@ -257,7 +368,8 @@ __device__ __forceinline__ void decode_chunk_to_tmem(const Table &T, const uint4
 
 template <class C>
 __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces, uint8_t *smem, const TcSmBars &b,
-                            volatile uint32_t *abort_flag, uint32_t tmem_base, uint64_t deadline) {
+                            volatile uint32_t *abort_flag, volatile uint32_t *last_flags, uint32_t tmem_base,
+                            uint64_t deadline) {
     const int warp = threadIdx.x >> 5;
     const int q = warp & 3;       // TMEM lane quarter = rows 32q..32q+31
     const int j = warp >> 2;      // chunks 2j, 2j+1 of each segment
@@ -270,7 +382,6 @@ __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces
     bool ok = warp_wait(b.hdr, 0, deadline);
     int gs = 0;     // segments of the range so far
     int hseg = 0;   // headers of the earlier pieces
-    int pend = -1;  // A slot whose stores still await their handshake
     for (int k = 0; ok && k < npieces; ++k) {
         const Piece &pc = pieces[k];
         const GemmParams &p = g.m[pc.member];
@@ -280,7 +391,7 @@ __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces
             const Table T = make_table(*reinterpret_cast<const uint4 *>(hp));
             const uint4 meta = *reinterpret_cast<const uint4 *>(hp + 16);
             const uint32_t mask_q = (meta.w >> (8 * q)) & 0xFFu;
-            const int xslot = gs % C::kSegSlots, wslot = gs % C::kStages;
+            const int eslot = gs % C::kESlots, wslot = gs % C::kStages;
             if (!(ok = warp_wait(b.wfull + wslot, (uint32_t)(gs / C::kStages) & 1u, deadline))) break;
             const int ca = 2 * j;
             const bool va = ca < nch, vb = ca + 1 < nch;  // chunks past a ragged K end are absent
@@ -299,9 +410,6 @@ __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces
             }
             const uint32_t esc_a = va ? (mask_q >> ca) & 1u : 0u, esc_b = vb ? (mask_q >> (ca + 1)) & 1u : 0u;
             const uint8_t *run = nullptr;
-            // every decoder waits for the segment slot before it releases it:
-            // an early release could count toward the slot's previous use
-            bool have_slot = false;
             if (esc_a | esc_b) {
                 // the quarter's escapes run chunk by chunk; find where chunk 2j's
                 // start from whichever end of the quarter has fewer chunks to
@@ -321,40 +429,33 @@ __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces
                         if ((mask_q >> c) & 1u) after += stage_chunk_escapes(sw, c);
                     pos += qc_mine - after;
                 }
-                if (!(ok = warp_wait(b.sfull + xslot, (uint32_t)(gs / C::kSegSlots) & 1u, deadline))) break;
-                have_slot = true;
+                if (!(ok = warp_wait(b.efull + eslot, (uint32_t)(gs / C::kESlots) & 1u, deadline))) break;
                 if (escapes_staged<C>(seg_escape_total(meta)))
-                    run = smem + C::kOffEsc + xslot * C::kEscCap + (meta.x & 15u) + pos;
+                    run = smem + C::kOffEsc + eslot * C::kEscCap + (meta.x & 15u) + pos;
                 else
                     run = p.blob + p.off_esc + meta.x + pos;
             }
             warp_arrive(b.wempty + wslot);  // this warp is done with the stage's bytes
 
-            // the previous segment's stores: wait for them, then hand the slot
-            // to the MMA warp (one segment late, so that the store latency
-            // overlaps this segment's loads)
-            if (pend >= 0) {
-                tmem_wait_st();
-                tc_fence_before();
-                warp_arrive(b.afull + pend);
-                pend = -1;
-            }
             const int aslot = gs % C::kASlots;
             if (gs >= C::kASlots &&
                 !(ok = warp_wait(b.aempty + aslot, (uint32_t)(gs / C::kASlots - 1) & 1u, deadline)))
                 break;
             tc_fence_after();
-            // each chunk goes to TMEM as soon as it is decoded: 16 columns of
-            // BF16 pairs, the chunk's 32 weights in column order
+            // a chunk goes to TMEM as 16 columns of BF16 pairs, its 32 weights
+            // in column order
             const uint32_t ta = a_lane + (uint32_t)(128 * aslot);
+            // (each chunk is stored as soon as it is decoded: decoding both
+            // chunks first and storing them together measured slower)
             if (va) decode_chunk_to_tmem(T, a0, a1, acd, esc_a != 0u, run, ta);
             if (vb) decode_chunk_to_tmem(T, b0, b1, bcd, esc_b != 0u, run, ta + 16u);
-            if (!have_slot && !(ok = warp_wait(b.sfull + xslot, (uint32_t)(gs / C::kSegSlots) & 1u, deadline))) {
-                pend = aslot;
-                break;
-            }
-            warp_arrive(b.sempty + xslot);  // done with this segment's escapes
-            pend = aslot;
+            // hand the slot to the MMA warp once the stores have landed (doing
+            // this one segment later, to overlap the store latency with the
+            // next loads, measured slower: the MMAs then start a segment later
+            // and the decoders wait for the slot three segments on)
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(b.afull + aslot);
             if (*abort_flag) {
                 ok = false;
                 break;
@@ -362,12 +463,18 @@ __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces
         }
         hseg += pc.s1 - pc.s0;
     }
-    if (pend >= 0) {
-        tmem_wait_st();
-        tc_fence_before();
-        if (ok) warp_arrive(b.afull + pend);
+    if (!ok) {
+        tmem_wait_st();  // no store of this warp may still be in flight when TMEM is freed
+        if (lane == 0) raise_timeout(group_status(g), abort_flag);
+        return;
     }
-    if (!ok && lane == 0) raise_timeout(group_status(g), abort_flag);
+    // help add up the tiles this CTA completes, once the epilogue has made
+    // the arrivals
+    if (!warp_wait(b.epi_out, 0, deadline)) {
+        if (lane == 0) raise_timeout(group_status(g), abort_flag);
+        return;
+    }
+    tcsm_finish<C>(g, pieces, npieces, last_flags, (int)threadIdx.x);
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -429,25 +536,32 @@ __device__ void tcsm_epilogue(const GemmGroup &g, const Piece *pieces, int npiec
     const int ka = 0, kb = npieces - 1;
     const bool sa = npieces > 0 && pieces[ka].count > 1;
     const bool sb = kb > ka && pieces[kb].count > 1;
-    if (!(sa || sb)) return;
 
     // split-K arrivals, once at the end: the mbarrier arrive/wait pair orders
     // the four warps' partial stores before one thread's release fence, which
-    // with the increments after it publishes them
+    // with the increments after it publishes them.  The leader then releases
+    // the decode warps, which help add up the tiles this CTA completed.
     __syncwarp();
     const bool leader = warp == C::kEpiWarp0 && lane == 0;
     if (lane == 0) mbar_arrive(b.epi_in);
     if (leader) {
         if (mbar_wait(b.epi_in, 0, deadline)) {
-            fence_acq_rel_gpu();
-            uint32_t oa = 0, ob = 0;
-            if (sa) oa = arrive_relaxed(g.m[pieces[ka].member].counters + pieces[ka].tile);
-            if (sb) ob = arrive_relaxed(g.m[pieces[kb].member].counters + pieces[kb].tile);
-            const bool la = sa && oa == (uint32_t)(pieces[ka].count - 1);
-            const bool lb = sb && ob == (uint32_t)(pieces[kb].count - 1);
+            bool la = false, lb = false;
+            if (sa || sb) {
+                fence_acq_rel_gpu();
+                uint32_t oa = 0, ob = 0;
+                if (sa) oa = arrive_relaxed(g.m[pieces[ka].member].counters + pieces[ka].tile);
+                if (sb) ob = arrive_relaxed(g.m[pieces[kb].member].counters + pieces[kb].tile);
+                la = sa && oa == (uint32_t)(pieces[ka].count - 1);
+                lb = sb && ob == (uint32_t)(pieces[kb].count - 1);
+                if (la || lb) fence_acq_rel_gpu();
+                // every CTA of a completed tile has arrived: its counter is
+                // free for the next call
+                if (la) g.m[pieces[ka].member].counters[pieces[ka].tile] = 0u;
+                if (lb) g.m[pieces[kb].member].counters[pieces[kb].tile] = 0u;
+            }
             last_flags[0] = la ? 1u : 0u;
             last_flags[1] = lb ? 1u : 0u;
-            if (la || lb) fence_acq_rel_gpu();
             mbar_arrive(b.epi_out);
         } else {
             raise_timeout(group_status(g), abort_flag);
@@ -457,29 +571,7 @@ __device__ void tcsm_epilogue(const GemmGroup &g, const Piece *pieces, int npiec
         if (lane == 0) raise_timeout(group_status(g), abort_flag);
         return;
     }
-    for (int e = 0; e < 2; ++e) {
-        if (last_flags[e] == 0) continue;
-        const Piece &pc = pieces[e == 0 ? ka : kb];
-        const GemmParams &p = g.m[pc.member];
-        const int64_t n = pc.tile * kTileRows + r;
-        const int64_t stride = (int64_t)p.M * p.Npad;
-        for (int t = 0; t < p.M; ++t) {
-            const float *src = p.partials + (int64_t)t * p.Npad + (n < p.N ? n : pc.tile * kTileRows);
-            float s = 0.0f;
-            for (int sp = 0; sp < pc.count; sp += 8) {
-                float v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (sp + u < pc.count) v[u] = __ldcg(src + (int64_t)(sp + u) * stride);
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (sp + u < pc.count) s += v[u];
-            }
-            if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(s);
-            if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(s, (uint32_t)n) : 0ull);
-        }
-        if (leader) p.counters[pc.tile] = 0u;  // ready for the next call
-    }
+    tcsm_finish<C>(g, pieces, npieces, last_flags, (int)threadIdx.x - (C::kEpiWarp0 - C::kDecWarps) * 32);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -493,9 +585,10 @@ __global__ void __launch_bounds__(TcSmCfg<NTOK>::kThreads, 1)
     TcSmBars b;
     b.wfull = bars;
     b.wempty = b.wfull + C::kStages;
-    b.sfull = b.wempty + C::kStages;
-    b.sempty = b.sfull + C::kSegSlots;
-    b.afull = b.sempty + C::kSegSlots;
+    b.efull = b.wempty + C::kStages;
+    b.xfull = b.efull + C::kESlots;
+    b.xempty = b.xfull + C::kXSlots;
+    b.afull = b.xempty + C::kXSlots;
     b.aempty = b.afull + C::kASlots;
     b.dfull = b.aempty + C::kASlots;
     b.dempty = b.dfull + 2;
@@ -518,9 +611,10 @@ __global__ void __launch_bounds__(TcSmCfg<NTOK>::kThreads, 1)
             mbar_init(b.wfull + i, 1);
             mbar_init(b.wempty + i, C::kDecWarps);
         }
-        for (int i = 0; i < C::kSegSlots; ++i) {
-            mbar_init(b.sfull + i, 1);
-            mbar_init(b.sempty + i, C::kDecWarps + 1);  // decoders done with the escapes + MMAs done with x
+        for (int i = 0; i < C::kESlots; ++i) mbar_init(b.efull + i, 1);
+        for (int i = 0; i < C::kXSlots; ++i) {
+            mbar_init(b.xfull + i, 1);
+            mbar_init(b.xempty + i, 1);  // the MMAs that read the slot have completed
         }
         for (int i = 0; i < C::kASlots; ++i) {
             mbar_init(b.afull + i, C::kDecWarps);
@@ -557,14 +651,16 @@ __global__ void __launch_bounds__(TcSmCfg<NTOK>::kThreads, 1)
     pdl_wait();
 
     if (warp == C::kProdWarp) {
-        if ((threadIdx.x & 31) == 0) tcsm_producer<C>(grp, pieces, np, &tmap_x, smem, b, abort_flag, deadline);
+        if ((threadIdx.x & 31) == 0) tcsm_producer<C>(grp, pieces, np, smem, b, abort_flag, deadline);
+    } else if (warp == C::kXWarp) {
+        if ((threadIdx.x & 31) == 0) tcsm_x_loader<C>(grp, pieces, np, &tmap_x, smem, b, abort_flag, deadline);
     } else if (warp == C::kMmaWarp) {
         if ((threadIdx.x & 31) == 0) tcsm_mma<C>(grp, pieces, np, smem, b, abort_flag, tmem_base, deadline);
         __syncwarp();
-    } else if (warp >= C::kEpiWarp0) {
+    } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiWarps) {
         tcsm_epilogue<C>(grp, pieces, np, b, abort_flag, last_flags, tmem_base, deadline);
     } else {
-        tcsm_decode<C>(grp, pieces, np, smem, b, abort_flag, tmem_base, deadline);
+        tcsm_decode<C>(grp, pieces, np, smem, b, abort_flag, last_flags, tmem_base, deadline);
     }
     tc_fence_before();
     __syncthreads();

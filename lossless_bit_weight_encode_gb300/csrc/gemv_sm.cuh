@@ -39,6 +39,7 @@ struct GemvSmCfg {
     static constexpr int kDecWarps = 16;
     static constexpr int kThreads = (kDecWarps + 1) * 32;
     static constexpr int kStages = 4;
+    static constexpr int kL2Ahead = 3;                          // segments pulled into L2 ahead of the ring
     static constexpr int kWBytes = kChunksPerSeg * kChunkBytes;  // one segment per stage
     static constexpr int kXbBytes = MT * kSegK * 2;             // one segment of x, [MT][256] BF16
     // x + escape slots, one segment each, as deep as the weight ring: with two
@@ -72,6 +73,19 @@ __device__ __forceinline__ uint32_t chunk_escapes(const uint4 &cd) {
     return __reduce_add_sync(0xFFFFFFFFu, n);
 }
 
+// The 32 weights of one chunk (BF16 pairs in column order) against x at xs.
+template <int MT>
+__device__ __forceinline__ void dot32_bf(const uint32_t (&w)[16], uint32_t xs, float (&acc)[MT][4]) {
+    uint32_t lo[8], hi[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        lo[i] = w[i];
+        hi[i] = w[8 + i];
+    }
+    dot16_bf<MT>(lo, xs, acc);
+    dot16_bf<MT>(hi, xs + 32u, acc);
+}
+
 // ------------------------------------------------------------------ producer
 template <class C>
 __device__ void gemv_sm_producer(const GemmGroup &g, const Piece *pieces, int npieces, const CUtensorMap *tmap,
@@ -91,6 +105,11 @@ __device__ void gemv_sm_producer(const GemmGroup &g, const Piece *pieces, int np
         bulk_g2s(hdr + off, p.blob + p.off_seg + (uint64_t)(pc.tile * p.segs + pc.s0) * kSegHdrBytes, n, b.hdr);
         off += (int)n;
     }
+
+    // the L2 cursor runs kL2Ahead segments ahead of the weight issue (the
+    // first two segments were warmed before the grid wait)
+    SegCursor l2 = seg_cursor(pieces, npieces);
+    for (int i = 0; i < C::kL2Ahead; ++i) seg_cursor_next<kChunkBytes>(g, pieces, npieces, l2, i >= 2);
 
     bool hdr_ready = false, failed = false, stop = false;
     int gst = 0, gseg = 0;  // weight stages and segment slots issued (one each per segment)
@@ -112,6 +131,7 @@ __device__ void gemv_sm_producer(const GemmGroup &g, const Piece *pieces, int np
                      p.blob + p.off_w + (uint64_t)(pc.tile * p.chunks + chunk) * kChunkBytes,
                      (uint32_t)(nch * kChunkBytes), b.wfull + slot);
             ++gst;
+            seg_cursor_next<kChunkBytes>(g, pieces, npieces, l2, true);
             // the segment's x (no header needed), then its escapes; the one
             // arrival comes last so the phase cannot complete early
             const int sslot = gseg % C::kSegSlots;
@@ -257,17 +277,26 @@ __device__ void gemv_sm_decode(const GemmGroup &g, const Piece *pieces, int npie
             warp_arrive(b.wempty + slot);
 
             const uint32_t xs = xb0 + (uint32_t)(sslot * C::kXbBytes);
-            if (va) {
-                uint32_t o0[8], o1[8];
-                decode_chunk(T, a0, a1, acd, esc_a != 0u, run, o0, o1);
-                dot16_bf<MT>(o0, xs, acc);
-                dot16_bf<MT>(o1, xs + 32u, acc);
-            }
-            if (vb) {
-                uint32_t o0[8], o1[8];
-                decode_chunk(T, b0, b1, bcd, esc_b != 0u, run, o0, o1);
-                dot16_bf<MT>(o0, xs + (uint32_t)(kChunkK * 2), acc);
-                dot16_bf<MT>(o1, xs + (uint32_t)(kChunkK * 2) + 32u, acc);
+            if (vb && (esc_a | esc_b) == 0u) {
+                // common case: both chunks present, no escapes; one
+                // straight-line block of 32 independent lookup/assembly chains
+                uint32_t wa[16], wb[16];
+                decode_pair_plain(T, a0, a1, acd, b0, b1, bcd, wa, wb);
+                dot32_bf<MT>(wa, xs, acc);
+                dot32_bf<MT>(wb, xs + (uint32_t)(kChunkK * 2), acc);
+            } else {
+                if (va) {
+                    uint32_t o0[8], o1[8];
+                    decode_chunk(T, a0, a1, acd, esc_a != 0u, run, o0, o1);
+                    dot16_bf<MT>(o0, xs, acc);
+                    dot16_bf<MT>(o1, xs + 32u, acc);
+                }
+                if (vb) {
+                    uint32_t o0[8], o1[8];
+                    decode_chunk(T, b0, b1, bcd, esc_b != 0u, run, o0, o1);
+                    dot16_bf<MT>(o0, xs + (uint32_t)(kChunkK * 2), acc);
+                    dot16_bf<MT>(o1, xs + (uint32_t)(kChunkK * 2) + 32u, acc);
+                }
             }
             warp_arrive(b.sempty + sslot);  // done with this segment's x and escapes
         }

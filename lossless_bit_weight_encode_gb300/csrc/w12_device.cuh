@@ -384,6 +384,29 @@ __device__ __forceinline__ void assemble_half(const uint4 &s, const uint32_t (&E
     }
 }
 
+// Two escape-free chunks of this thread's row: chunk a into va (16 words of
+// BF16 pairs), chunk b into vb.
+__device__ __forceinline__ void decode_pair_plain(const Table &T, const uint4 &a0, const uint4 &a1,
+                                                  const uint4 &acd, const uint4 &b0, const uint4 &b1,
+                                                  const uint4 &bcd, uint32_t (&va)[16], uint32_t (&vb)[16]) {
+    uint32_t Ea0[4], Ea1[4], Eb0[4], Eb1[4];
+    decode_exponents_half(T, acd.x, acd.y, Ea0);
+    decode_exponents_half(T, acd.z, acd.w, Ea1);
+    decode_exponents_half(T, bcd.x, bcd.y, Eb0);
+    decode_exponents_half(T, bcd.z, bcd.w, Eb1);
+    const uint32_t Sa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t Sb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t ea = j < 4 ? Ea0[j & 3] : Ea1[j & 3];
+        const uint32_t eb = j < 4 ? Eb0[j & 3] : Eb1[j & 3];
+        va[2 * j] = rotr1(prmt(Sa[j], ea, 0x5140u));
+        va[2 * j + 1] = rotr1(prmt(Sa[j], ea, 0x7362u));
+        vb[2 * j] = rotr1(prmt(Sb[j], eb, 0x5140u));
+        vb[2 * j + 1] = rotr1(prmt(Sb[j], eb, 0x7362u));
+    }
+}
+
 // Exclusive prefix over the lanes of `cnt` and the warp total.  When no lane
 // holds more than one escape (the common case) a ballot gives both; else a
 // shuffle scan.

@@ -200,7 +200,7 @@ def test_one_token_paths(case, m1_path):
         w = np.where((e > 140) | (e == 255), (w & 0x807F) | np.uint16(130 << 7), w).astype(np.uint16)
     x = wl.activations(1, w.shape[1], seed=35)
     mat = W12Weight(w)
-    assert w12.w12_gemm_launch_info(mat.info, 1)["ntok"] == (1 if m1_path == "gemv" else 32)
+    assert w12.w12_gemm_launch_info(mat.info, 1)["ntok"] == (1 if m1_path == "gemv" else 16)
     check_tolerance(_gemm(mat, x), oracle.gemm_f64(x, w), f"{case} {m1_path}")
 
 
@@ -240,7 +240,7 @@ def test_two_token_paths(case, M, gemv_max_m):
     x = wl.activations(M, w.shape[1], seed=45 + M)
     mat = W12Weight(w)
     ntok = w12.w12_gemm_launch_info(mat.info, M)["ntok"]
-    assert ntok == (2 if M <= gemv_max_m else 32)
+    assert ntok == (2 if M <= gemv_max_m else 16)
     check_tolerance(_gemm(mat, x), oracle.gemm_f64(x, w), f"{case} M={M} ntok={ntok}")
 
 
