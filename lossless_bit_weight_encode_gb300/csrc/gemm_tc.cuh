@@ -271,36 +271,6 @@ __device__ __forceinline__ void prefetch_pieces(const GemmGroup &g, const Piece 
     }
 }
 
-// A cursor over a CTA's segments in range order, used to pull the packed
-// chunks of a segment into L2 some distance ahead of the shared-memory ring:
-// the ring's bulk copy of that segment then reads L2, not HBM, so each slot
-// spends less time in flight and the SM keeps more bytes on the way than its
-// shared memory could hold.
-struct SegCursor {
-    int k;   // piece
-    int sg;  // segment within the piece's tile
-};
-
-__device__ __forceinline__ SegCursor seg_cursor(const Piece *pieces, int npieces) {
-    return SegCursor{0, npieces > 0 ? pieces[0].s0 : 0};
-}
-
-// Prefetch (when `fetch`) the cursor's segment into L2, then move to the next.
-template <int kChunkB>
-__device__ __forceinline__ void seg_cursor_next(const GemmGroup &g, const Piece *pieces, int npieces, SegCursor &c,
-                                                bool fetch) {
-    if (c.k >= npieces) return;
-    const Piece &pc = pieces[c.k];
-    if (fetch) {
-        const GemmParams &p = g.m[pc.member];
-        const int chunk = c.sg * kChunksPerSeg;
-        const int nch = min(kChunksPerSeg, p.chunks - chunk);
-        const uint8_t *w = p.blob + p.off_w + (uint64_t)(pc.tile * p.chunks + chunk) * kChunkB;
-        for (int c0 = 0; c0 < nch; c0 += 4) prefetch_l2(w + c0 * kChunkB, (uint32_t)(min(4, nch - c0) * kChunkB));
-    }
-    if (++c.sg == pc.s1 && ++c.k < npieces) c.sg = pieces[c.k].s0;
-}
-
 // ------------------------------------------------------------------ producer
 template <class C>
 __device__ void gemm_producer(const GemmParams &p, const CUtensorMap *tmap, uint8_t *smem, const Bars &b,

@@ -61,9 +61,7 @@ struct TcSmCfg {
     static constexpr int kEpiWarps = 4;
     static constexpr int kXWarp = 22;
     static constexpr int kThreads = (kXWarp + 1) * 32;
-    static constexpr int kFinishThreads = (kDecWarps + kEpiWarps) * 32;  // share the split-K finish
     static constexpr int kStages = 3;                            // weight ring: one segment per stage
-    static constexpr int kL2Ahead = 3;                           // segments pulled into L2 ahead of the ring
     static constexpr int kWBytes = kChunksPerSeg * kChunkBytes;  // 48 KB
     static constexpr int kXBoxBytes = NTOK * 128;                // 64 columns x NTOK tokens
     static constexpr int kXBytes = 4 * kXBoxBytes;               // x tile of one segment
@@ -108,6 +106,7 @@ template <class C>
 __device__ void tcsm_producer(const GemmGroup &g, const Piece *pieces, int npieces, uint8_t *smem,
                               const TcSmBars &b, volatile uint32_t *abort_flag, uint64_t deadline) {
     uint8_t *hdr = smem + C::kOffHdr;
+    const uint64_t stream_policy = policy_evict_first();  // the weights are read once
     uint32_t hbytes = 0;
     for (int k = 0; k < npieces; ++k) hbytes += (uint32_t)(pieces[k].s1 - pieces[k].s0) * kSegHdrBytes;
     mbar_arrive_expect_tx(b.hdr, hbytes);
@@ -118,11 +117,6 @@ __device__ void tcsm_producer(const GemmGroup &g, const Piece *pieces, int npiec
         bulk_g2s(hdr + off, p.blob + p.off_seg + (uint64_t)(pc.tile * p.segs + pc.s0) * kSegHdrBytes, n, b.hdr);
         off += (int)n;
     }
-
-    // the L2 cursor runs kL2Ahead segments ahead of the weight issue (the
-    // first two segments were warmed before the grid wait)
-    SegCursor l2 = seg_cursor(pieces, npieces);
-    for (int i = 0; i < C::kL2Ahead; ++i) seg_cursor_next<kChunkBytes>(g, pieces, npieces, l2, i >= 2);
 
     bool hdr_ready = false, failed = false;
     int gw = 0, ge = 0;  // weight stages and escape slots issued (one each per segment)
@@ -139,11 +133,10 @@ __device__ void tcsm_producer(const GemmGroup &g, const Piece *pieces, int npiec
                 break;
             }
             mbar_arrive_expect_tx(b.wfull + wslot, (uint32_t)(nch * kChunkBytes));
-            bulk_g2s(smem + C::kOffW + wslot * C::kWBytes,
-                     p.blob + p.off_w + (uint64_t)(pc.tile * p.chunks + chunk) * kChunkBytes,
-                     (uint32_t)(nch * kChunkBytes), b.wfull + wslot);
+            bulk_g2s_hint(smem + C::kOffW + wslot * C::kWBytes,
+                          p.blob + p.off_w + (uint64_t)(pc.tile * p.chunks + chunk) * kChunkBytes,
+                          (uint32_t)(nch * kChunkBytes), b.wfull + wslot, stream_policy);
             ++gw;
-            seg_cursor_next<kChunkBytes>(g, pieces, npieces, l2, true);
             if (!hdr_ready) {
                 if (!mbar_wait(b.hdr, 0, deadline)) {
                     failed = true;
@@ -291,59 +284,6 @@ __device__ void tcsm_mma(const GemmGroup &g, const Piece *pieces, int npieces, u
     mbar_wait(b.drain, 0, globaltimer_ns() + 1000000000ull);
 }
 
-// ------------------------------------------------------------------ finish
-// The tiles whose last arrival this CTA made: each output adds the tile's
-// partial-sum slots in slot order (reproducible run to run) and is rounded to
-// BF16.  The decode and epilogue warps (kFinishThreads, reducer id rid) share
-// the outputs, four per thread per batch with up to four slots each, so that
-// up to sixteen loads per thread are in flight: this runs at the very end of
-// the kernel, when every load waits behind the weight stream of the SMs still
-// working.
-template <class C>
-__device__ void tcsm_finish(const GemmGroup &g, const Piece *pieces, int npieces, volatile uint32_t *last_flags,
-                            int rid) {
-    constexpr int kN = C::kFinishThreads;
-    for (int e = 0; e < 2; ++e) {
-        if (last_flags[e] == 0) continue;
-        const Piece &pc = pieces[e == 0 ? 0 : npieces - 1];
-        const GemmParams &p = g.m[pc.member];
-        const int total = p.M * kTileRows;
-        const int64_t stride = (int64_t)p.M * p.Npad;
-        const float *base = p.partials + pc.tile * kTileRows;
-        // a warp's 32 outputs share one token (kN and 128 are multiples of 32)
-        for (int o0 = rid; o0 < total; o0 += 4 * kN) {
-            float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            for (int sp0 = 0; sp0 < pc.count; sp0 += 4) {
-                float v[4][4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int bb = 0; bb < 4; ++bb) {
-                        const int o = o0 + bb * kN;
-                        v[u][bb] = (sp0 + u < pc.count && o < total)
-                                       ? __ldcg(base + (int64_t)(sp0 + u) * stride + (int64_t)(o / kTileRows) * p.Npad +
-                                                o % kTileRows)
-                                       : 0.0f;
-                    }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int bb = 0; bb < 4; ++bb)
-                        if (sp0 + u < pc.count) s[bb] += v[u][bb];
-            }
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) {
-                const int o = o0 + bb * kN;
-                if (o >= total) break;  // the same for the whole warp
-                const int t = o / kTileRows;
-                const int64_t n = pc.tile * kTileRows + o % kTileRows;
-                if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(s[bb]);
-                if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(s[bb], (uint32_t)n) : 0ull);
-            }
-        }
-    }
-}
-
 // ------------------------------------------------------------------ decoders
 // Escapes of quarter-chunk c of the stage in weight slot `slot` (this warp's
 // rows): the warp total, from the chunk's codes.
@@ -368,8 +308,7 @@ __device__ __forceinline__ void decode_chunk_to_tmem(const Table &T, const uint4
 
 template <class C>
 __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces, uint8_t *smem, const TcSmBars &b,
-                            volatile uint32_t *abort_flag, volatile uint32_t *last_flags, uint32_t tmem_base,
-                            uint64_t deadline) {
+                            volatile uint32_t *abort_flag, uint32_t tmem_base, uint64_t deadline) {
     const int warp = threadIdx.x >> 5;
     const int q = warp & 3;       // TMEM lane quarter = rows 32q..32q+31
     const int j = warp >> 2;      // chunks 2j, 2j+1 of each segment
@@ -466,39 +405,132 @@ __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces
     if (!ok) {
         tmem_wait_st();  // no store of this warp may still be in flight when TMEM is freed
         if (lane == 0) raise_timeout(group_status(g), abort_flag);
-        return;
     }
-    // help add up the tiles this CTA completes, once the epilogue has made
-    // the arrivals
-    if (!warp_wait(b.epi_out, 0, deadline)) {
-        if (lane == 0) raise_timeout(group_status(g), abort_flag);
-        return;
-    }
-    tcsm_finish<C>(g, pieces, npieces, last_flags, (int)threadIdx.x);
 }
 
 // ------------------------------------------------------------------ epilogue
-// One warp per TMEM lane quarter: for each piece, wait for its accumulator,
+// The four epilogue warps meet on an mbarrier pair (in: four arrivals, out:
+// the leader's) at most twice per launch; `use` counts the meetings so the
+// phases line up.
+struct EpiSync {
+    uint64_t *in, *out;
+    int use;
+};
+
+// Add the partial-sum slots of a tile in slot order (run-to-run reproducible)
+// and store the BF16 result: row r of the tile, tokens 0..M-1.  The slot
+// `own` (or none, when own < 0) comes from `acc` instead of memory.  Eight
+// tokens' loads of a slot are in flight together.
+template <int NT>
+__device__ __forceinline__ void tcsm_reduce_row(const GemmParams &p, const Piece &pc, int r, int own,
+                                                float (&acc)[NT]) {
+    constexpr int kB = 8;  // tokens per batch (register budget of the epilogue)
+    const int64_t n = pc.tile * kTileRows + r;
+    const float *src = p.partials + (n < p.N ? n : pc.tile * kTileRows);
+    if (own == 0) {
+        // this CTA holds slot 0 (the usual case: it computed the tile's first
+        // segments at the end of its range): add the other slots onto the
+        // registers in slot order, sixteen tokens' loads in flight at a time
+        for (int sp = 1; sp < pc.count; ++sp) {
+#pragma unroll
+            for (int t0 = 0; t0 < NT; t0 += 16) {
+                if (t0 >= p.M) break;
+                float v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    v[u] = t0 + u < p.M ? __ldcg(src + ((int64_t)sp * p.M + t0 + u) * p.Npad) : 0.0f;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) acc[t0 + u] += v[u];
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t >= p.M) break;
+            if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(acc[t]);
+            if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(acc[t], (uint32_t)n) : 0ull);
+        }
+        return;
+    }
+#pragma unroll
+    for (int t0 = 0; t0 < NT; t0 += kB) {
+        if (t0 >= p.M) break;
+        float s[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) s[u] = 0.0f;
+        for (int sp = 0; sp < pc.count; ++sp) {
+            float v[kB];
+            if (sp == own) {
+#pragma unroll
+                for (int u = 0; u < kB; ++u) v[u] = acc[t0 + u];
+            } else {
+#pragma unroll
+                for (int u = 0; u < kB; ++u)
+                    v[u] = t0 + u < p.M ? __ldcg(src + ((int64_t)sp * p.M + t0 + u) * p.Npad) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < kB; ++u) s[u] += v[u];
+        }
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const int t = t0 + u;
+            if (t >= p.M) break;
+            if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(s[u]);
+            if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(s[u], (uint32_t)n) : 0ull);
+        }
+    }
+}
+
+// One warp per TMEM lane quarter.  For each piece: wait for its accumulator,
 // read this quarter's 32 rows x NTOK tokens, release the accumulator, then
-// store y (the CTA owns the tile) or the piece's partial-sum slot.  After the
-// last piece, the shared first and last pieces arrive on their tiles'
-// counters, and the last arrival of a tile adds its slots in slot order.
+//   - a whole tile: store y;
+//   - a shared tile that is not the range's last piece (it was computed
+//     early, while the CTAs sharing it are still busy): store the partial-sum
+//     slot and arrive on the tile's counter at once (a release fence, then one
+//     atomic add), adding the tile up if this was the last arrival;
+//   - the range's last piece, shared: the other CTAs normally arrived long
+//     ago, so first look (acquire load of the counter): if they all have,
+//     add their slots to this accumulator, still in registers, and store y,
+//     with no partial store, fence or atomic on the kernel's tail; otherwise
+//     store the slot and arrive as above.
+// The last arrival of a tile resets its counter for the next call.
 template <class C>
 __device__ void tcsm_epilogue(const GemmGroup &g, const Piece *pieces, int npieces, const TcSmBars &b,
-                              volatile uint32_t *abort_flag, volatile uint32_t *last_flags, uint32_t tmem_base,
+                              volatile uint32_t *abort_flag, volatile uint32_t *flag, uint32_t tmem_base,
                               uint64_t deadline) {
     constexpr int NT = C::kNtok;
     const int warp = threadIdx.x >> 5;
     const int q = warp & 3;
     const int lane = threadIdx.x & 31;
     const int r = 32 * q + lane;
+    const bool leader = warp == C::kEpiWarp0 && lane == 0;
     const uint32_t d_lane = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)C::kDCol;
-    bool ok = true;
+    EpiSync sy{b.epi_in, b.epi_out, 0};
+    // all four warps meet; the leader runs `lead` in between and writes its
+    // result to *flag, which every warp reads after the meeting
+    auto meet = [&](auto lead) -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sy.in);
+        if (leader) {
+            if (mbar_wait(sy.in, (uint32_t)sy.use & 1u, deadline)) {
+                *flag = lead() ? 1u : 0u;
+                mbar_arrive(sy.out);
+            } else {
+                raise_timeout(group_status(g), abort_flag);
+            }
+        }
+        const bool ok = warp_wait(sy.out, (uint32_t)sy.use & 1u, deadline);
+        ++sy.use;
+        return ok;
+    };
     for (int k = 0; k < npieces; ++k) {
         const Piece &pc = pieces[k];
         const GemmParams &p = g.m[pc.member];
         const int dbuf = k & 1;
-        if (!(ok = warp_wait(b.dfull + dbuf, (uint32_t)(k >> 1) & 1u, deadline))) break;
+        bool ok = warp_wait(b.dfull + dbuf, (uint32_t)(k >> 1) & 1u, deadline);
+        if (!ok) {
+            if (lane == 0) raise_timeout(group_status(g), abort_flag);
+            return;
+        }
         tc_fence_after();
         float acc[NT];
         {
@@ -524,54 +556,34 @@ __device__ void tcsm_epilogue(const GemmGroup &g, const Piece *pieces, int npiec
             }
             continue;
         }
+        uint32_t *counter = p.counters + pc.tile;
+        if (k == npieces - 1) {
+            // everyone else in already?  Then add up straight from registers
+            ok = meet([&] { return load_acquire_gpu(counter) == (uint32_t)(pc.count - 1); });
+            if (!ok) return;
+            if (*flag) {
+                tcsm_reduce_row<NT>(p, pc, r, pc.idx, acc);
+                if (leader) *counter = 0u;  // every CTA of the tile has arrived
+                continue;
+            }
+        }
+        // store this piece's slot, then arrive: the mbarrier meeting orders the
+        // four warps' stores before the leader's release fence
 #pragma unroll
         for (int t = 0; t < NT; ++t)
             if (t < p.M) __stcg(p.partials + ((int64_t)pc.idx * p.M + t) * p.Npad + n, acc[t]);
-    }
-    if (!ok) {
-        if (lane == 0) raise_timeout(group_status(g), abort_flag);
-        return;
-    }
-    // the pieces that share their tile: the first and the last (one when equal)
-    const int ka = 0, kb = npieces - 1;
-    const bool sa = npieces > 0 && pieces[ka].count > 1;
-    const bool sb = kb > ka && pieces[kb].count > 1;
-
-    // split-K arrivals, once at the end: the mbarrier arrive/wait pair orders
-    // the four warps' partial stores before one thread's release fence, which
-    // with the increments after it publishes them.  The leader then releases
-    // the decode warps, which help add up the tiles this CTA completed.
-    __syncwarp();
-    const bool leader = warp == C::kEpiWarp0 && lane == 0;
-    if (lane == 0) mbar_arrive(b.epi_in);
-    if (leader) {
-        if (mbar_wait(b.epi_in, 0, deadline)) {
-            bool la = false, lb = false;
-            if (sa || sb) {
-                fence_acq_rel_gpu();
-                uint32_t oa = 0, ob = 0;
-                if (sa) oa = arrive_relaxed(g.m[pieces[ka].member].counters + pieces[ka].tile);
-                if (sb) ob = arrive_relaxed(g.m[pieces[kb].member].counters + pieces[kb].tile);
-                la = sa && oa == (uint32_t)(pieces[ka].count - 1);
-                lb = sb && ob == (uint32_t)(pieces[kb].count - 1);
-                if (la || lb) fence_acq_rel_gpu();
-                // every CTA of a completed tile has arrived: its counter is
-                // free for the next call
-                if (la) g.m[pieces[ka].member].counters[pieces[ka].tile] = 0u;
-                if (lb) g.m[pieces[kb].member].counters[pieces[kb].tile] = 0u;
-            }
-            last_flags[0] = la ? 1u : 0u;
-            last_flags[1] = lb ? 1u : 0u;
-            mbar_arrive(b.epi_out);
-        } else {
-            raise_timeout(group_status(g), abort_flag);
+        ok = meet([&] {
+            fence_acq_rel_gpu();
+            const bool last = arrive_relaxed(counter) == (uint32_t)(pc.count - 1);
+            if (last) fence_acq_rel_gpu();
+            return last;
+        });
+        if (!ok) return;
+        if (*flag) {
+            tcsm_reduce_row<NT>(p, pc, r, -1, acc);
+            if (leader) *counter = 0u;
         }
     }
-    if (!warp_wait(b.epi_out, 0, deadline)) {
-        if (lane == 0) raise_timeout(group_status(g), abort_flag);
-        return;
-    }
-    tcsm_finish<C>(g, pieces, npieces, last_flags, (int)threadIdx.x - (C::kEpiWarp0 - C::kDecWarps) * 32);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -660,7 +672,7 @@ __global__ void __launch_bounds__(TcSmCfg<NTOK>::kThreads, 1)
     } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiWarps) {
         tcsm_epilogue<C>(grp, pieces, np, b, abort_flag, last_flags, tmem_base, deadline);
     } else {
-        tcsm_decode<C>(grp, pieces, np, smem, b, abort_flag, last_flags, tmem_base, deadline);
+        tcsm_decode<C>(grp, pieces, np, smem, b, abort_flag, tmem_base, deadline);
     }
     tc_fence_before();
     __syncthreads();

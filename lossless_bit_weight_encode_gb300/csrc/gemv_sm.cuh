@@ -39,7 +39,6 @@ struct GemvSmCfg {
     static constexpr int kDecWarps = 16;
     static constexpr int kThreads = (kDecWarps + 1) * 32;
     static constexpr int kStages = 4;
-    static constexpr int kL2Ahead = 3;                          // segments pulled into L2 ahead of the ring
     static constexpr int kWBytes = kChunksPerSeg * kChunkBytes;  // one segment per stage
     static constexpr int kXbBytes = MT * kSegK * 2;             // one segment of x, [MT][256] BF16
     // x + escape slots, one segment each, as deep as the weight ring: with two
@@ -92,6 +91,7 @@ __device__ void gemv_sm_producer(const GemmGroup &g, const Piece *pieces, int np
                                  uint8_t *smem, const GemvBars &b, volatile uint32_t *abort_flag,
                                  uint64_t deadline) {
     uint8_t *hdr = smem + C::kOffHdr;
+    const uint64_t stream_policy = policy_evict_first();  // the weights are read once
     prefetch_tmap(tmap);
 
     // the segment headers of every piece, one after another, on one phase
@@ -105,11 +105,6 @@ __device__ void gemv_sm_producer(const GemmGroup &g, const Piece *pieces, int np
         bulk_g2s(hdr + off, p.blob + p.off_seg + (uint64_t)(pc.tile * p.segs + pc.s0) * kSegHdrBytes, n, b.hdr);
         off += (int)n;
     }
-
-    // the L2 cursor runs kL2Ahead segments ahead of the weight issue (the
-    // first two segments were warmed before the grid wait)
-    SegCursor l2 = seg_cursor(pieces, npieces);
-    for (int i = 0; i < C::kL2Ahead; ++i) seg_cursor_next<kChunkBytes>(g, pieces, npieces, l2, i >= 2);
 
     bool hdr_ready = false, failed = false, stop = false;
     int gst = 0, gseg = 0;  // weight stages and segment slots issued (one each per segment)
@@ -127,11 +122,10 @@ __device__ void gemv_sm_producer(const GemmGroup &g, const Piece *pieces, int np
                 break;
             }
             mbar_arrive_expect_tx(b.wfull + slot, (uint32_t)(nch * kChunkBytes));
-            bulk_g2s(smem + C::kOffW + slot * C::kWBytes,
-                     p.blob + p.off_w + (uint64_t)(pc.tile * p.chunks + chunk) * kChunkBytes,
-                     (uint32_t)(nch * kChunkBytes), b.wfull + slot);
+            bulk_g2s_hint(smem + C::kOffW + slot * C::kWBytes,
+                          p.blob + p.off_w + (uint64_t)(pc.tile * p.chunks + chunk) * kChunkBytes,
+                          (uint32_t)(nch * kChunkBytes), b.wfull + slot, stream_policy);
             ++gst;
-            seg_cursor_next<kChunkBytes>(g, pieces, npieces, l2, true);
             // the segment's x (no header needed), then its escapes; the one
             // arrival comes last so the phase cannot complete early
             const int sslot = gseg % C::kSegSlots;

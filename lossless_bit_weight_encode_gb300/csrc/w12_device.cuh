@@ -131,6 +131,25 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// L2 policy for data read once (the weight stream): its lines are the first
+// to go, so that small data read again later (x, split-K partial sums, segment
+// headers) stays in L2.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// As bulk_g2s, with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared (coordinates in elements, x first).
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int32_t x, int32_t y, uint64_t *bar) {
     asm volatile(
@@ -539,6 +558,14 @@ __device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t *counter) {
     uint32_t old;
     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
     return old;
+}
+
+// Acquire load of a split-K counter at GPU scope: a value showing that the
+// other CTAs of a tile have arrived also makes their partial sums visible.
+__device__ __forceinline__ uint32_t load_acquire_gpu(const uint32_t *counter) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    return v;
 }
 
 // The same split into its parts, for a thread that arrives on several
