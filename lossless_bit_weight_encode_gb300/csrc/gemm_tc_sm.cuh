@@ -61,6 +61,7 @@ struct TcSmCfg {
     static constexpr int kEpiWarps = 4;
     static constexpr int kXWarp = 22;
     static constexpr int kThreads = (kXWarp + 1) * 32;
+    static constexpr int kFinishThreads = (kDecWarps + kEpiWarps) * 32;  // share a split-K finish
     static constexpr int kStages = 3;                            // weight ring: one segment per stage
     static constexpr int kWBytes = kChunksPerSeg * kChunkBytes;  // 48 KB
     static constexpr int kXBoxBytes = NTOK * 128;                // 64 columns x NTOK tokens
@@ -80,8 +81,8 @@ struct TcSmCfg {
     static constexpr int kOffHdr = kOffEsc + kESlots * kEscCap;
     static constexpr int kOffBars = kOffHdr + kMaxSegs * kSegHdrBytes;
     // wfull[S], wempty[S], efull[E], xfull[X], xempty[X], afull[A],
-    // aempty[A], dfull[2], dempty[2], hdr, drain, epi_in, epi_out
-    static constexpr int kNumBars = 2 * kStages + kESlots + 2 * kXSlots + 2 * kASlots + 4 + 4;
+    // aempty[A], dfull[2], dempty[2], hdr, drain, epi_in, epi_out, fin
+    static constexpr int kNumBars = 2 * kStages + kESlots + 2 * kXSlots + 2 * kASlots + 4 + 5;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
     static constexpr int kOffPieces = kOffMisc + 64;
     static constexpr int kSmemBytes = kOffPieces + kMaxPieces * (int)sizeof(Piece) + 1024;  // + alignment slack
@@ -95,7 +96,7 @@ struct TcSmCfg {
 
 struct TcSmBars {
     uint64_t *wfull, *wempty, *efull, *xfull, *xempty, *afull, *aempty, *dfull, *dempty, *hdr, *drain, *epi_in,
-        *epi_out;
+        *epi_out, *fin;
 };
 
 // ------------------------------------------------------------------ producers
@@ -284,6 +285,76 @@ __device__ void tcsm_mma(const GemmGroup &g, const Piece *pieces, int npieces, u
     mbar_wait(b.drain, 0, globaltimer_ns() + 1000000000ull);
 }
 
+// ------------------------------------------------------------------ finish
+// A tile whose last arrival this CTA made at the end of its range, added up
+// from memory: every output adds the tile's slots in slot order (reproducible
+// run to run) and is rounded to BF16.  The decode and epilogue warps share
+// the outputs (reducer id rid of kFinishThreads), four per thread per batch
+// with up to four slots each in flight: at the end of the kernel every load
+// waits behind the weight stream of the SMs still working.
+template <class C>
+__device__ void tcsm_finish(const GemmParams &p, const Piece &pc, int rid) {
+    constexpr int kN = C::kFinishThreads;
+    const int total = p.M * kTileRows;
+    const int64_t stride = (int64_t)p.M * p.Npad;
+    const float *base = p.partials + pc.tile * kTileRows;
+    // a warp's 32 outputs share one token (kN and 128 are multiples of 32)
+    for (int o0 = rid; o0 < total; o0 += 4 * kN) {
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int sp0 = 0; sp0 < pc.count; sp0 += 4) {
+            float v[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) {
+                    const int o = o0 + bb * kN;
+                    v[u][bb] = (sp0 + u < pc.count && o < total)
+                                   ? __ldcg(base + (int64_t)(sp0 + u) * stride + (int64_t)(o / kTileRows) * p.Npad +
+                                            o % kTileRows)
+                                   : 0.0f;
+                }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb)
+                    if (sp0 + u < pc.count) s[bb] += v[u][bb];
+        }
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+            const int o = o0 + bb * kN;
+            if (o >= total) break;  // the same for the whole warp
+            const int t = o / kTileRows;
+            const int64_t n = pc.tile * kTileRows + o % kTileRows;
+            if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(s[bb]);
+            if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(s[bb], (uint32_t)n) : 0ull);
+        }
+    }
+}
+
+// The range's tiles that this CTA completed as their last arrival: bit 0 the
+// first piece's tile, bit 1 the last piece's.
+template <class C>
+__device__ __noinline__ void tcsm_finish_all(const GemmGroup &g, const Piece *pieces, int npieces, int mask,
+                                             int rid) {
+    if (mask & 1) tcsm_finish<C>(g.m[pieces[0].member], pieces[0], rid);
+    if (mask & 2) tcsm_finish<C>(g.m[pieces[npieces - 1].member], pieces[npieces - 1], rid);
+}
+
+// The decode warps after their last segment: the epilogue says, once per
+// launch, whether tiles of the range must be added up from memory, and then
+// every decode warp helps.  Kept out of line: what the decode loop keeps live
+// for code after it costs the loop registers, and it measured slower inline.
+template <class C>
+__device__ __noinline__ void tcsm_decoder_finish(const GemmGroup &g, const Piece *pieces, int npieces, uint64_t *fin,
+                                                 volatile int *fin_mask, volatile uint32_t *abort_flag,
+                                                 uint64_t deadline) {
+    if (!warp_wait(fin, 0, deadline)) {
+        if ((threadIdx.x & 31) == 0) raise_timeout(group_status(g), abort_flag);
+        return;
+    }
+    tcsm_finish_all<C>(g, pieces, npieces, *fin_mask, (int)threadIdx.x);
+}
+
 // ------------------------------------------------------------------ decoders
 // Escapes of quarter-chunk c of the stage in weight slot `slot` (this warp's
 // rows): the warp total, from the chunk's codes.
@@ -308,7 +379,8 @@ __device__ __forceinline__ void decode_chunk_to_tmem(const Table &T, const uint4
 
 template <class C>
 __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces, uint8_t *smem, const TcSmBars &b,
-                            volatile uint32_t *abort_flag, uint32_t tmem_base, uint64_t deadline) {
+                            volatile uint32_t *abort_flag, volatile int *fin_mask, uint32_t tmem_base,
+                            uint64_t deadline) {
     const int warp = threadIdx.x >> 5;
     const int q = warp & 3;       // TMEM lane quarter = rows 32q..32q+31
     const int j = warp >> 2;      // chunks 2j, 2j+1 of each segment
@@ -405,7 +477,9 @@ __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces
     if (!ok) {
         tmem_wait_st();  // no store of this warp may still be in flight when TMEM is freed
         if (lane == 0) raise_timeout(group_status(g), abort_flag);
+        return;
     }
+    tcsm_decoder_finish<C>(g, pieces, npieces, b.fin, fin_mask, abort_flag, deadline);
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -486,17 +560,19 @@ __device__ __forceinline__ void tcsm_reduce_row(const GemmParams &p, const Piece
 //   - a shared tile that is not the range's last piece (it was computed
 //     early, while the CTAs sharing it are still busy): store the partial-sum
 //     slot and arrive on the tile's counter at once (a release fence, then one
-//     atomic add), adding the tile up if this was the last arrival;
+//     atomic add);
 //   - the range's last piece, shared: the other CTAs normally arrived long
 //     ago, so first look (acquire load of the counter): if they all have,
 //     add their slots to this accumulator, still in registers, and store y,
 //     with no partial store, fence or atomic on the kernel's tail; otherwise
 //     store the slot and arrive as above.
-// The last arrival of a tile resets its counter for the next call.
+// The last arrival of a tile resets its counter for the next call; a tile it
+// must add up from memory is left for the end of the range, where the decode
+// warps (done by then) share the loads.
 template <class C>
 __device__ void tcsm_epilogue(const GemmGroup &g, const Piece *pieces, int npieces, const TcSmBars &b,
-                              volatile uint32_t *abort_flag, volatile uint32_t *flag, uint32_t tmem_base,
-                              uint64_t deadline) {
+                              volatile uint32_t *abort_flag, volatile uint32_t *flag, volatile int *fin_mask,
+                              uint32_t tmem_base, uint64_t deadline) {
     constexpr int NT = C::kNtok;
     const int warp = threadIdx.x >> 5;
     const int q = warp & 3;
@@ -579,11 +655,21 @@ __device__ void tcsm_epilogue(const GemmGroup &g, const Piece *pieces, int npiec
             return last;
         });
         if (!ok) return;
-        if (*flag) {
-            tcsm_reduce_row<NT>(p, pc, r, -1, acc);
-            if (leader) *counter = 0u;
+        // last arrival: the tile is added up from memory at the end of the
+        // range, by the decode and epilogue warps together (even a first
+        // piece's tile: its sharers arrive at the ends of their ranges, so
+        // this is near the end anyway)
+        if (*flag && leader) {
+            *counter = 0u;
+            *fin_mask |= k == 0 ? 1 : 2;
         }
     }
+    // tell the decode warps whether there is a finish to share (exactly once
+    // per launch, also when there is nothing to do)
+    __syncwarp();
+    if (leader) mbar_arrive(b.fin);
+    if (!warp_wait(b.fin, 0, deadline)) return;
+    tcsm_finish_all<C>(g, pieces, npieces, *fin_mask, (int)threadIdx.x - (C::kEpiWarp0 - C::kDecWarps) * 32);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -608,11 +694,13 @@ __global__ void __launch_bounds__(TcSmCfg<NTOK>::kThreads, 1)
     b.drain = b.hdr + 1;
     b.epi_in = b.drain + 1;
     b.epi_out = b.epi_in + 1;
+    b.fin = b.epi_out + 1;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     uint32_t *tmem_slot = misc;
     volatile uint32_t *abort_flag = misc + 1;
     volatile uint32_t *npieces = misc + 2;
-    volatile uint32_t *last_flags = misc + 4;  // [2]
+    volatile uint32_t *last_flags = misc + 4;  // the epilogue leader's word to the other epilogue warps
+    volatile int *fin_mask = reinterpret_cast<volatile int *>(misc + 5);  // tiles to add up at the end
     Piece *pieces = reinterpret_cast<Piece *>(smem + C::kOffPieces);
 
     const int warp = threadIdx.x >> 5;
@@ -640,8 +728,10 @@ __global__ void __launch_bounds__(TcSmCfg<NTOK>::kThreads, 1)
         mbar_init(b.drain, 1);
         mbar_init(b.epi_in, C::kEpiWarps);
         mbar_init(b.epi_out, 1);
+        mbar_init(b.fin, 1);
         *abort_flag = 0u;
-        last_flags[0] = last_flags[1] = 0u;
+        last_flags[0] = 0u;
+        *fin_mask = 0;
         // this CTA's pieces (the planner keeps them within kMaxPieces)
         CtaWork w = cta_work(grp);
         uint32_t n = 0;
@@ -670,9 +760,9 @@ __global__ void __launch_bounds__(TcSmCfg<NTOK>::kThreads, 1)
         if ((threadIdx.x & 31) == 0) tcsm_mma<C>(grp, pieces, np, smem, b, abort_flag, tmem_base, deadline);
         __syncwarp();
     } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiWarps) {
-        tcsm_epilogue<C>(grp, pieces, np, b, abort_flag, last_flags, tmem_base, deadline);
+        tcsm_epilogue<C>(grp, pieces, np, b, abort_flag, last_flags, fin_mask, tmem_base, deadline);
     } else {
-        tcsm_decode<C>(grp, pieces, np, smem, b, abort_flag, tmem_base, deadline);
+        tcsm_decode<C>(grp, pieces, np, smem, b, abort_flag, fin_mask, tmem_base, deadline);
     }
     tc_fence_before();
     __syncthreads();
