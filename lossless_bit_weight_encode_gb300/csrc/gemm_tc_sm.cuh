@@ -356,12 +356,6 @@ __device__ __noinline__ void tcsm_decoder_finish(const GemmGroup &g, const Piece
 }
 
 // ------------------------------------------------------------------ decoders
-// Escapes of quarter-chunk c of the stage in weight slot `slot` (this warp's
-// rows): the warp total, from the chunk's codes.
-__device__ __forceinline__ uint32_t stage_chunk_escapes(uint32_t s_row_slot, int c) {
-    return chunk_escapes(lds128(s_row_slot + (uint32_t)(c * kChunkBytes) + 2u * kSlabBytes));
-}
-
 // Decode one chunk of this thread's row and store its 32 weights as 16 TMEM
 // columns of BF16 pairs (column c: weights 2c, 2c + 1) at taddr.
 __device__ __forceinline__ void decode_chunk_to_tmem(const Table &T, const uint4 &s0, const uint4 &s1,
@@ -422,24 +416,7 @@ __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces
             const uint32_t esc_a = va ? (mask_q >> ca) & 1u : 0u, esc_b = vb ? (mask_q >> (ca + 1)) & 1u : 0u;
             const uint8_t *run = nullptr;
             if (esc_a | esc_b) {
-                // the quarter's escapes run chunk by chunk; find where chunk 2j's
-                // start from whichever end of the quarter has fewer chunks to
-                // count: the earlier chunks (j < 2), or the quarter's total
-                // minus this and the later chunks (j >= 2)
-                const uint32_t qc0 = meta.y & 0xFFFFu, qc1 = meta.y >> 16, qc2 = meta.z & 0xFFFFu;
-                const uint32_t qc_mine = ((q < 2 ? meta.y : meta.z) >> (16 * (q & 1))) & 0xFFFFu;
-                uint32_t pos = (q > 0 ? qc0 : 0u) + (q > 1 ? qc1 : 0u) + (q > 2 ? qc2 : 0u);
-                if (j < 2) {
-                    for (int c = 0; c < ca; ++c)
-                        if ((mask_q >> c) & 1u) pos += stage_chunk_escapes(sw, c);
-                } else {
-                    uint32_t after = 0;
-                    if (esc_a) after += chunk_escapes(acd);
-                    if (esc_b) after += chunk_escapes(bcd);
-                    for (int c = ca + 2; c < nch; ++c)
-                        if ((mask_q >> c) & 1u) after += stage_chunk_escapes(sw, c);
-                    pos += qc_mine - after;
-                }
+                const uint32_t pos = quarter_chunk_escape_pos(meta, q, j, mask_q, nch, acd, bcd, esc_a, esc_b, sw);
                 if (!(ok = warp_wait(b.efull + eslot, (uint32_t)(gs / C::kESlots) & 1u, deadline))) break;
                 if (escapes_staged<C>(seg_escape_total(meta)))
                     run = smem + C::kOffEsc + eslot * C::kEscCap + (meta.x & 15u) + pos;

@@ -72,6 +72,35 @@ __device__ __forceinline__ uint32_t chunk_escapes(const uint4 &cd) {
     return __reduce_add_sync(0xFFFFFFFFu, n);
 }
 
+// Where the escapes of chunk 2j of quarter q start in the segment's escape
+// run, relative to the run's first byte, for a warp that decodes chunks 2j
+// and 2j + 1 of a segment staged at shared address sw + 16 * row (this
+// thread's row).  The run orders a quarter's escapes chunk by chunk and the
+// header holds only each quarter's total, so the warp counts escape codes:
+// of the earlier chunks (j < 2), or of its own and the later chunks, taken
+// from the quarter's total (j >= 2) -- whichever end has fewer chunks; the
+// segment's mask skips chunks without escapes.  acd / bcd are the codes of
+// the warp's chunks, esc_a / esc_b whether they hold escapes.
+__device__ __forceinline__ uint32_t quarter_chunk_escape_pos(const uint4 &meta, int q, int j, uint32_t mask_q,
+                                                             int nch, const uint4 &acd, const uint4 &bcd,
+                                                             uint32_t esc_a, uint32_t esc_b, uint32_t sw) {
+    const uint32_t qc0 = meta.y & 0xFFFFu, qc1 = meta.y >> 16, qc2 = meta.z & 0xFFFFu;
+    const uint32_t qc_mine = ((q < 2 ? meta.y : meta.z) >> (16 * (q & 1))) & 0xFFFFu;
+    uint32_t pos = (q > 0 ? qc0 : 0u) + (q > 1 ? qc1 : 0u) + (q > 2 ? qc2 : 0u);
+    const int ca = 2 * j;
+    if (j < 2) {
+        for (int c = 0; c < ca; ++c)
+            if ((mask_q >> c) & 1u) pos += chunk_escapes(lds128(sw + (uint32_t)(c * kChunkBytes) + 2u * kSlabBytes));
+        return pos;
+    }
+    uint32_t after = 0;
+    if (esc_a) after += chunk_escapes(acd);
+    if (esc_b) after += chunk_escapes(bcd);
+    for (int c = ca + 2; c < nch; ++c)
+        if ((mask_q >> c) & 1u) after += chunk_escapes(lds128(sw + (uint32_t)(c * kChunkBytes) + 2u * kSlabBytes));
+    return pos + qc_mine - after;
+}
+
 // The 32 weights of one chunk (BF16 pairs in column order) against x at xs.
 template <int MT>
 __device__ __forceinline__ void dot32_bf(const uint32_t (&w)[16], uint32_t xs, float (&acc)[MT][4]) {
@@ -255,14 +284,8 @@ __device__ void gemv_sm_decode(const GemmGroup &g, const Piece *pieces, int npie
             const uint32_t esc_a = va ? (mask_q >> ca) & 1u : 0u, esc_b = vb ? (mask_q >> (ca + 1)) & 1u : 0u;
             const uint8_t *run = nullptr;
             if (esc_a | esc_b) {
-                // this quarter's escapes are ordered chunk by chunk: skip those
-                // of the segment's earlier chunks, counted from their codes
-                const uint32_t qc0 = meta.y & 0xFFFFu, qc1 = meta.y >> 16, qc2 = meta.z & 0xFFFFu;
-                uint32_t pos = (q > 0 ? qc0 : 0u) + (q > 1 ? qc1 : 0u) + (q > 2 ? qc2 : 0u);
-                for (int c = 0; c < ca; ++c)
-                    if ((mask_q >> c) & 1u)
-                        pos += chunk_escapes(lds128(s_row + (uint32_t)(slot * C::kWBytes + c * kChunkBytes) +
-                                                    2 * kSlabBytes));
+                const uint32_t pos = quarter_chunk_escape_pos(meta, q, j, mask_q, nch, acd, bcd, esc_a, esc_b,
+                                                              s_row + (uint32_t)(slot * C::kWBytes));
                 if (escapes_staged<C>(seg_escape_total(meta)))
                     run = smem + C::kOffEsc + sslot * C::kEscCap + (meta.x & 15u) + pos;
                 else

@@ -314,19 +314,18 @@ int tc_sm_token_tile(int M) { return (M > 16 || opt(kOptTokenTile) == 32) ? 32 :
 
 // Which CUDA-core kernel: one CTA per SM with sixteen decode warps (gemv_sm.cuh)
 // or two with eight each (gemv.cuh).  The first keeps every warp of an SM busy
-// to the end of a single wave; it pays for finding where its chunks' escapes
-// start.  Measured (one GPU, back to back): layer step at M = 1 / 2 110.1 /
-// 124.6 us against 115.7 / 134.2; the LM head 199.0 against 209.1 us; but
-// heavy-tail weights (0.4 % escapes) 180.6 against 174.3 us.  So: one CTA per
-// SM when at most ~20 % of quarter-chunks (32 x 32 weights) hold an escape
-// (2e-4 of the weights; N(0, 0.02) weights: 1.4e-4) and one wave of SM-long
-// ranges covers the launch.  gemv_sm = 0 or 1 forces a kernel.
+// to the end of a single wave.  Measured (one GPU, back to back): layer step at
+// M = 1 / 2 110.1 / 124.6 us against 115.7 / 134.2; the LM head 199.0 against
+// 209.1 us; heavy-tail weights (0.4 % escapes, nearly every quarter-chunk
+// holding some) 169.1 / 187.9 against 175.2 / 191.7 us once each warp finds
+// its escapes' offset from the nearer end of its quarter.  So one CTA per SM
+// whenever one wave of ranges of at most kMaxSegs segments covers the launch;
+// gemv_sm = 0 or 1 forces a kernel.
 bool use_gemv_sm(const w12_info &info, int sm_count) {
     const int64_t v = opt(kOptGemvSm);
     if (v >= 0) return v == 1;
-    const double density = (double)info.n_escapes / ((double)info.N * (double)info.K);
     const int64_t units = info.tiles * info.segs;
-    return density <= 2e-4 && (units + sm_count - 1) / sm_count <= dev::GemvSmCfg<1>::kMaxSegs;
+    return (units + sm_count - 1) / sm_count <= dev::GemvSmCfg<1>::kMaxSegs;
 }
 
 // The GEMV shares a single wave's work as stream-K unit ranges unless

@@ -93,23 +93,22 @@ def test_stream_k_reproducible_and_counters_reset(gemv_kernel):
 
 
 def test_kernel_choice(w12_opts):
-    """One CTA per SM for weights with rare escapes, whatever the tile count
-    (one wave of ranges covers these launches); two per SM for escape-heavy
-    weights."""
+    """One CTA per SM whenever one wave of ranges covers the launch, for
+    Gaussian and escape-heavy weights alike, whatever the tile count."""
     import torch
     w12_opts(gemv_sm=-1)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     gauss = W12Weight(wl.gaussian_weights(2048, 1024, seed=330))
     heavy = W12Weight(wl.heavy_tail_weights(2048, 1024, seed=331))
     many = W12Weight(wl.gaussian_weights(3 * sms * 128, 512, seed=332))
-    assert gauss.info.n_escapes / (2048 * 1024) <= 2e-4 < heavy.info.n_escapes / (2048 * 1024)
+    assert heavy.info.n_escapes / (2048 * 1024) > 2e-3
     for M in (1, 2):
         assert w12.w12_gemm_launch_info(gauss.info, M)["ctas_per_sm"] == 1
-        assert w12.w12_gemm_launch_info(heavy.info, M)["ctas_per_sm"] == 2
+        assert w12.w12_gemm_launch_info(heavy.info, M)["ctas_per_sm"] == 1
         plan = w12.w12_gemm_launch_info(many.info, M)
         assert plan["ctas_per_sm"] == 1 and plan["ctas"] == sms
-    w12_opts(gemv_sm=1)
-    assert w12.w12_gemm_launch_info(heavy.info, 1)["ctas_per_sm"] == 1
+    w12_opts(gemv_sm=0)
+    assert w12.w12_gemm_launch_info(heavy.info, 1)["ctas_per_sm"] == 2
 
 
 @pytest.mark.parametrize("case", range(10))
