@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--no-detail", action="store_true",
                     help="skip the other configurations (M sweep, heavy tail, single layer, decode) that the "
                          "default layer run at M=1 adds under detail")
+    ap.add_argument("--opt", action="append", default=[], metavar="NAME=VALUE",
+                    help="set a library launch option (w12_set_option) for the run, e.g. --opt tc_sm=0; repeatable")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
     ap.add_argument("--matrices", default=None,
                     help="comma list of layer matrices to run (profiling only; default all seven)")
@@ -507,6 +509,9 @@ def run_w12(args):
     from lossless_bit_weight_encode_gb300 import workloads as wl
 
     libbuild.build()
+    for o in args.opt:
+        name, _, value = o.partition("=")
+        w12.w12_set_option(name, int(value))
     M = args.m
     K = args.steps
     nshape = len(wl.LAYER_SHAPES)
@@ -693,6 +698,7 @@ def run_w12(args):
         "config": {
             "workload": WORKLOAD_TEXT[args.workload],
             "M": M, "global_batch": M * world, "parallelism": f"replicas x{world}",
+            **({"options": args.opt} if args.opt else {}),
             "l2": (f"inputs larger than L2: {step.packed / 1e6:.1f} MB of W12 streamed per step (L2 129 MB)"
                    if args.workload != "single" else
                    f"{len(mats)} encoded copies rotated ({step.packed / 1e6:.1f} MB per step, > 3 x L2)"),
