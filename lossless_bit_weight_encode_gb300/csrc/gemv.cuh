@@ -60,6 +60,7 @@ struct GemvCfg {
 
 struct GemvBars {
     uint64_t *wfull, *wempty, *sfull, *sempty, *hdr, *red, *red_empty, *epi_in, *epi_out;
+    uint64_t *first_done, *prod_done;  // used by the one-CTA-per-SM kernel only
 };
 
 // acc[t][j] += w * x[t] over 16 columns for each token t, with x as BF16 (16

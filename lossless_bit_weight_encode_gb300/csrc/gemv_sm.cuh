@@ -55,8 +55,9 @@ struct GemvSmCfg {
     static constexpr int kOffHdr = kOffEsc + kSegSlots * kEscCap;
     static constexpr int kOffRed = kOffHdr + kMaxSegs * kSegHdrBytes;  // [3][MT][128] fp32
     static constexpr int kOffBars = kOffRed + 3 * MT * kTileRows * 4;
-    // wfull[S], wempty[S], sfull[2], sempty[2], hdr, red, red_empty, epi_in, epi_out
-    static constexpr int kNumBars = 2 * kStages + 2 * kSegSlots + 5;
+    // wfull[S], wempty[S], sfull[S], sempty[S], hdr, red, red_empty, epi_in,
+    // epi_out, first_done, prod_done
+    static constexpr int kNumBars = 2 * kStages + 2 * kSegSlots + 7;
     static constexpr int kOffMisc = kOffBars + kNumBars * 8;
     static constexpr int kOffPieces = kOffMisc + 64;
     static constexpr int kSmemBytes = kOffPieces + kMaxPieces * (int)sizeof(Piece) + 128;  // + base alignment slack
@@ -115,10 +116,27 @@ __device__ __forceinline__ void dot32_bf(const uint32_t (&w)[16], uint32_t xs, f
 }
 
 // ------------------------------------------------------------------ producer
+// The arrival of a range's first piece on its tile's counter, made by the
+// producer as soon as the decode warps have stored the piece's partial sums
+// (first_done), so that the decode warps never wait for the fence and atomic
+// round trip.  The CTAs sharing that tile are still busy with their own
+// ranges, so this is rarely the last arrival; if it is, the tile is added up at
+// the end of the range (bit 0 of fin_mask).
+__device__ __forceinline__ void gemv_first_arrival(const GemmGroup &g, const Piece &pc, volatile int *fin_mask) {
+    uint32_t *counter = g.m[pc.member].counters + pc.tile;
+    fence_acq_rel_gpu();
+    if (arrive_relaxed(counter) == (uint32_t)(pc.count - 1)) {
+        fence_acq_rel_gpu();
+        *counter = 0u;  // every CTA of the tile has arrived
+        atomicOr(const_cast<int *>(fin_mask), 1);  // thread 0 may set bit 1 at the same time
+    }
+}
+
 template <class C>
 __device__ void gemv_sm_producer(const GemmGroup &g, const Piece *pieces, int npieces, const CUtensorMap *tmap,
                                  uint8_t *smem, const GemvBars &b, volatile uint32_t *abort_flag,
-                                 uint64_t deadline) {
+                                 volatile int *fin_mask, uint64_t deadline) {
+    bool first_pending = npieces > 1 && pieces[0].count > 1;
     uint8_t *hdr = smem + C::kOffHdr;
     const uint64_t stream_policy = policy_evict_first();  // the weights are read once
     prefetch_tmap(tmap);
@@ -185,6 +203,10 @@ __device__ void gemv_sm_producer(const GemmGroup &g, const Piece *pieces, int np
                          b.sfull + sslot);
             }
             mbar_arrive(b.sfull + sslot);
+            if (first_pending && mbar_test_wait(b.first_done, 0)) {
+                gemv_first_arrival(g, pieces[0], fin_mask);
+                first_pending = false;
+            }
             if (*abort_flag) {
                 stop = true;
                 break;
@@ -192,6 +214,13 @@ __device__ void gemv_sm_producer(const GemmGroup &g, const Piece *pieces, int np
         }
         hseg += pc.s1 - pc.s0;
     }
+    if (first_pending && !failed && !*abort_flag) {
+        if (mbar_wait(b.first_done, 0, deadline))
+            gemv_first_arrival(g, pieces[0], fin_mask);
+        else
+            failed = true;
+    }
+    mbar_arrive(b.prod_done);  // bit 0 of fin_mask is final
     if (failed) raise_timeout(group_status(g), abort_flag);
     if (*abort_flag) {
         const uint64_t drain_deadline = globaltimer_ns() + 1000000000ull;
@@ -232,8 +261,8 @@ __device__ __forceinline__ void decode_chunk(const Table &T, const uint4 &s0, co
 // end, and the last arrival adds the tile's slots in slot order.
 template <class C>
 __device__ void gemv_sm_decode(const GemmGroup &g, const Piece *pieces, int npieces, uint8_t *smem,
-                               const GemvBars &b, volatile uint32_t *abort_flag, volatile uint32_t *last_flags,
-                               uint64_t deadline) {
+                               const GemvBars &b, volatile uint32_t *abort_flag, volatile uint32_t *flag,
+                               volatile int *fin_mask, uint64_t deadline) {
     constexpr int MT = C::kMT;
     const int warp = threadIdx.x >> 5;
     const int q = warp & 3;       // rows 32q..32q+31
@@ -247,6 +276,25 @@ __device__ void gemv_sm_decode(const GemmGroup &g, const Piece *pieces, int npie
     const uint32_t xb0 = smem_u32(smem + C::kOffXb) + (uint32_t)(2 * j * kChunkK) * 2u;
     float *red = reinterpret_cast<float *>(smem + C::kOffRed);
 
+    // the four j = 0 warps (one per row quarter) meet on an mbarrier pair at
+    // most twice per launch; thread 0 runs `lead` in between and writes its
+    // result to *flag, which they all read after the meeting
+    int meets = 0;
+    auto meet = [&](auto lead) -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b.epi_in);
+        if (threadIdx.x == 0) {
+            if (mbar_wait(b.epi_in, (uint32_t)meets & 1u, deadline)) {
+                *flag = lead() ? 1u : 0u;
+                mbar_arrive(b.epi_out);
+            } else {
+                raise_timeout(group_status(g), abort_flag);
+            }
+        }
+        const bool met = warp_wait(b.epi_out, (uint32_t)meets & 1u, deadline);
+        ++meets;
+        return met;
+    };
     bool ok = warp_wait(b.hdr, 0, deadline);
     int gst = 0;   // stages consumed
     int hseg = 0;  // headers of the earlier pieces
@@ -353,50 +401,68 @@ __device__ void gemv_sm_decode(const GemmGroup &g, const Piece *pieces, int npie
             }
             continue;
         }
+        uint32_t *counter = p.counters + pc.tile;
+        if (k == npieces - 1) {
+            // the range's last piece: the CTAs sharing its tile normally
+            // arrived long ago (at the start of their ranges); then add their
+            // slots to this piece's sums, still in registers, in slot order
+            ok = meet([&] { return load_acquire_gpu(counter) == (uint32_t)(pc.count - 1); });
+            if (!ok) break;
+            if (*flag) {
+                const float *src = p.partials + (n < p.N ? n : pc.tile * kTileRows);
+                const int64_t stride = (int64_t)p.M * p.Npad;
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    if (t >= p.M) continue;
+                    float s = 0.0f;
+                    for (int sp = 0; sp < pc.count; ++sp)
+                        s += sp == pc.idx ? total[t] : __ldcg(src + (int64_t)t * p.Npad + (int64_t)sp * stride);
+                    if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(s);
+                    if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(s, (uint32_t)n) : 0ull);
+                }
+                if (threadIdx.x == 0) *counter = 0u;  // every CTA of the tile has arrived
+                continue;
+            }
+        }
 #pragma unroll
         for (int t = 0; t < MT; ++t)
             if (t < p.M) __stcg(p.partials + ((int64_t)pc.idx * p.M + t) * p.Npad + n, total[t]);
+        if (k < npieces - 1) {
+            // the first piece: the producer arrives for it once all four warps
+            // have stored their rows (the mbarrier orders the stores first)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b.first_done);
+            continue;
+        }
+        // the last piece, others still missing: arrive now
+        ok = meet([&] {
+            fence_acq_rel_gpu();
+            const bool last = arrive_relaxed(counter) == (uint32_t)(pc.count - 1);
+            if (last) {
+                fence_acq_rel_gpu();
+                *counter = 0u;
+                atomicOr(const_cast<int *>(fin_mask), 2);
+            }
+            return last;
+        });
+        if (!ok) break;
     }
     if (!ok) {
         if (lane == 0) raise_timeout(group_status(g), abort_flag);
         return;
     }
-    // the pieces that share their tile: the first and the last (one when equal)
-    const int ka = 0, kb = npieces - 1;
-    const bool sa = npieces > 0 && pieces[ka].count > 1;
-    const bool sb = kb > ka && pieces[kb].count > 1;
-    if (j > 0 || !(sa || sb)) return;
+    if (j > 0) return;
 
-    // ---- split-K arrivals, once at the end: the mbarrier arrive/wait pair
-    // orders every partial store before thread 0's release fence, which with
-    // the increments after it publishes them
-    __syncwarp();
-    if (lane == 0) mbar_arrive(b.epi_in);
-    if (threadIdx.x == 0) {
-        if (mbar_wait(b.epi_in, 0, deadline)) {
-            fence_acq_rel_gpu();
-            uint32_t oa = 0, ob = 0;
-            if (sa) oa = arrive_relaxed(g.m[pieces[ka].member].counters + pieces[ka].tile);
-            if (sb) ob = arrive_relaxed(g.m[pieces[kb].member].counters + pieces[kb].tile);
-            const bool la = sa && oa == (uint32_t)(pieces[ka].count - 1);
-            const bool lb = sb && ob == (uint32_t)(pieces[kb].count - 1);
-            last_flags[0] = la ? 1u : 0u;
-            last_flags[1] = lb ? 1u : 0u;
-            if (la || lb) fence_acq_rel_gpu();
-            mbar_arrive(b.epi_out);
-        } else {
-            raise_timeout(group_status(g), abort_flag);
-        }
-    }
-    if (!warp_wait(b.epi_out, 0, deadline)) {
+    // ---- tiles this CTA completed as the last arrival, added up from memory
+    // in slot order (the producer's word on the first piece comes first)
+    if (!warp_wait(b.prod_done, 0, deadline)) {
         if (lane == 0) raise_timeout(group_status(g), abort_flag);
         return;
     }
+    const int mask = *fin_mask;
     for (int e = 0; e < 2; ++e) {
-        if (last_flags[e] == 0) continue;
-        // the last arrival adds the tile's slots in ascending order, up to
-        // eight loads in flight at a time
-        const Piece &pc = pieces[e == 0 ? ka : kb];
+        if (!((mask >> e) & 1)) continue;
+        const Piece &pc = pieces[e == 0 ? 0 : npieces - 1];
         const GemmParams &p = g.m[pc.member];
         const int64_t n = pc.tile * kTileRows + r;
 #pragma unroll
@@ -417,7 +483,6 @@ __device__ void gemv_sm_decode(const GemmGroup &g, const Piece *pieces, int npie
             if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(s);
             if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(s, (uint32_t)n) : 0ull);
         }
-        if (threadIdx.x == 0) p.counters[pc.tile] = 0u;  // ready for the next call
     }
 }
 
@@ -439,10 +504,13 @@ __global__ void __launch_bounds__(GemvSmCfg<MT>::kThreads, 1)
     b.red_empty = b.red + 1;
     b.epi_in = b.red_empty + 1;
     b.epi_out = b.epi_in + 1;
+    b.first_done = b.epi_out + 1;
+    b.prod_done = b.first_done + 1;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile uint32_t *abort_flag = misc + 1;
     volatile uint32_t *npieces = misc + 2;
-    volatile uint32_t *last_flags = misc + 4;  // [2]
+    volatile uint32_t *flag = misc + 4;  // thread 0's word to the j = 0 warps
+    volatile int *fin_mask = reinterpret_cast<volatile int *>(misc + 5);  // tiles to add up at the end
     Piece *pieces = reinterpret_cast<Piece *>(smem + C::kOffPieces);
 
     const int warp = threadIdx.x >> 5;
@@ -462,6 +530,10 @@ __global__ void __launch_bounds__(GemvSmCfg<MT>::kThreads, 1)
         mbar_init(b.red_empty, 4);
         mbar_init(b.epi_in, 4);
         mbar_init(b.epi_out, 1);
+        mbar_init(b.first_done, 4);
+        mbar_init(b.prod_done, 1);
+        *flag = 0u;
+        *fin_mask = 0;
         *abort_flag = 0u;
         // this CTA's pieces (the planner keeps them within kMaxPieces)
         CtaWork w = cta_work(grp);
@@ -476,9 +548,9 @@ __global__ void __launch_bounds__(GemvSmCfg<MT>::kThreads, 1)
     if (warp == C::kDecWarps && (threadIdx.x & 31) == 0) prefetch_pieces<kChunkBytes, true>(grp, pieces, np);
     pdl_wait();
     if (warp == C::kDecWarps) {
-        if ((threadIdx.x & 31) == 0) gemv_sm_producer<C>(grp, pieces, np, &tmap_x, smem, b, abort_flag, deadline);
+        if ((threadIdx.x & 31) == 0) gemv_sm_producer<C>(grp, pieces, np, &tmap_x, smem, b, abort_flag, fin_mask, deadline);
     } else {
-        gemv_sm_decode<C>(grp, pieces, np, smem, b, abort_flag, last_flags, deadline);
+        gemv_sm_decode<C>(grp, pieces, np, smem, b, abort_flag, flag, fin_mask, deadline);
     }
 }
 
