@@ -51,9 +51,11 @@
 namespace w12 {
 namespace dev {
 
-template <int NTOK>
+template <int NTOK, bool Q8 = false>
 struct TcSmCfg {
     static constexpr int kNtok = NTOK;
+    static constexpr bool kQ8 = Q8;                              // weights: the Q8 copy instead of W12
+    static constexpr int kChunkB = Q8 ? q8::kChunkBytes : kChunkBytes;
     static constexpr int kDecWarps = 16;
     static constexpr int kProdWarp = 16;
     static constexpr int kMmaWarp = 17;
@@ -62,12 +64,14 @@ struct TcSmCfg {
     static constexpr int kXWarp = 22;
     static constexpr int kThreads = (kXWarp + 1) * 32;
     static constexpr int kFinishThreads = (kDecWarps + kEpiWarps) * 32;  // share a split-K finish
-    static constexpr int kStages = 3;                            // weight ring: one segment per stage
-    static constexpr int kWBytes = kChunksPerSeg * kChunkBytes;  // 48 KB
+    // weight ring: one segment per stage (48 KB of W12, three deep; 32 KB of
+    // Q8, four deep)
+    static constexpr int kStages = Q8 ? 4 : 3;
+    static constexpr int kWBytes = kChunksPerSeg * kChunkB;
     static constexpr int kXBoxBytes = NTOK * 128;                // 64 columns x NTOK tokens
     static constexpr int kXBytes = 4 * kXBoxBytes;               // x tile of one segment
     static constexpr int kXSlots = 4;                            // x ring
-    static constexpr int kESlots = 4;                            // escape-byte ring, one deeper than the weights
+    static constexpr int kESlots = Q8 ? 1 : kStages + 1;         // escape-byte ring, one deeper than the weights
     static constexpr int kEscCap = 2048;
     static constexpr int kASlots = 3;                            // TMEM A slots, one segment each
     static constexpr int kMaxSegs = 192;                         // units (segments) of one CTA
@@ -91,7 +95,7 @@ struct TcSmCfg {
     static_assert(kOffW % 128 == 0 && kOffEsc % 16 == 0 && kOffHdr % 16 == 0, "copy destinations aligned");
     static_assert(kACol + kASlots * 128 <= kTmemCols && kDCol + 64 <= kACol, "TMEM columns");
     static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM must fit");
-    static_assert(kESlots == kStages + 1, "an escape slot is reused once the next weight stage is released");
+    static_assert(Q8 || kESlots == kStages + 1, "an escape slot is reused once the next weight stage is released");
 };
 
 struct TcSmBars {
@@ -109,9 +113,10 @@ __device__ void tcsm_producer(const GemmGroup &g, const Piece *pieces, int npiec
     uint8_t *hdr = smem + C::kOffHdr;
     const uint64_t stream_policy = policy_evict_first();  // the weights are read once
     uint32_t hbytes = 0;
-    for (int k = 0; k < npieces; ++k) hbytes += (uint32_t)(pieces[k].s1 - pieces[k].s0) * kSegHdrBytes;
-    mbar_arrive_expect_tx(b.hdr, hbytes);
-    for (int k = 0, off = 0; k < npieces; ++k) {
+    if constexpr (!C::kQ8)
+        for (int k = 0; k < npieces; ++k) hbytes += (uint32_t)(pieces[k].s1 - pieces[k].s0) * kSegHdrBytes;
+    mbar_arrive_expect_tx(b.hdr, hbytes);  // a Q8 copy has no segment headers
+    for (int k = 0, off = 0; !C::kQ8 && k < npieces; ++k) {
         const Piece &pc = pieces[k];
         const GemmParams &p = g.m[pc.member];
         const uint32_t n = (uint32_t)(pc.s1 - pc.s0) * kSegHdrBytes;
@@ -133,11 +138,18 @@ __device__ void tcsm_producer(const GemmGroup &g, const Piece *pieces, int npiec
                 failed = true;
                 break;
             }
-            mbar_arrive_expect_tx(b.wfull + wslot, (uint32_t)(nch * kChunkBytes));
+            mbar_arrive_expect_tx(b.wfull + wslot, (uint32_t)(nch * C::kChunkB));
             bulk_g2s_hint(smem + C::kOffW + wslot * C::kWBytes,
-                          p.blob + p.off_w + (uint64_t)(pc.tile * p.chunks + chunk) * kChunkBytes,
-                          (uint32_t)(nch * kChunkBytes), b.wfull + wslot, stream_policy);
+                          p.blob + p.off_w + (uint64_t)(pc.tile * p.chunks + chunk) * C::kChunkB,
+                          (uint32_t)(nch * C::kChunkB), b.wfull + wslot, stream_policy);
             ++gw;
+            if constexpr (C::kQ8) {
+                if (*abort_flag) {
+                    failed = true;
+                    break;
+                }
+                continue;  // no headers, no escapes
+            }
             if (!hdr_ready) {
                 if (!mbar_wait(b.hdr, 0, deadline)) {
                     failed = true;
@@ -325,6 +337,7 @@ __device__ void tcsm_finish(const GemmParams &p, const Piece &pc, int rid) {
             if (o >= total) break;  // the same for the whole warp
             const int t = o / kTileRows;
             const int64_t n = pc.tile * kTileRows + o % kTileRows;
+            if constexpr (C::kQ8) s[bb] *= p.scales[n];  // the Q8 copy's row scale (pad rows: 0)
             if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(s[bb]);
             if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(s[bb], (uint32_t)n) : 0ull);
         }
@@ -459,6 +472,85 @@ __device__ void tcsm_decode(const GemmGroup &g, const Piece *pieces, int npieces
     tcsm_decoder_finish<C>(g, pieces, npieces, b.fin, fin_mask, abort_flag, deadline);
 }
 
+// The Q8 copy: chunk 2j and 2j + 1 of this thread's row as 16 int8 per slab,
+// turned into BF16 exactly (|q| <= 127) and stored like the W12 weights.
+template <class C>
+__device__ void tcsm_decode_q8(const GemmGroup &g, const Piece *pieces, int npieces, uint8_t *smem,
+                               const TcSmBars &b, volatile uint32_t *abort_flag, volatile int *fin_mask,
+                               uint32_t tmem_base, uint64_t deadline) {
+    const int warp = threadIdx.x >> 5;
+    const int q = warp & 3;
+    const int j = warp >> 2;
+    const int lane = threadIdx.x & 31;
+    const int r = 32 * q + lane;
+    const uint32_t s_row = smem_u32(smem + C::kOffW) + (uint32_t)(16 * r);
+    const uint32_t a_lane = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(C::kACol + 32 * j);
+    bool ok = true;
+    int gs = 0;
+    for (int k = 0; ok && k < npieces; ++k) {
+        const Piece &pc = pieces[k];
+        const GemmParams &p = g.m[pc.member];
+        for (int sg = pc.s0; sg < pc.s1; ++sg, ++gs) {
+            const int nch = min(kChunksPerSeg, p.chunks - sg * kChunksPerSeg);
+            const int wslot = gs % C::kStages, aslot = gs % C::kASlots;
+            if (!(ok = warp_wait(b.wfull + wslot, (uint32_t)(gs / C::kStages) & 1u, deadline))) break;
+            const int ca = 2 * j;
+            const bool va = ca < nch, vb = ca + 1 < nch;
+            const uint32_t sa = s_row + (uint32_t)(wslot * C::kWBytes + ca * C::kChunkB);
+            uint4 a0{}, a1{}, b0{}, b1{};
+            if (va) {
+                a0 = lds128(sa);
+                a1 = lds128(sa + kSlabBytes);
+            }
+            if (vb) {
+                b0 = lds128(sa + C::kChunkB);
+                b1 = lds128(sa + C::kChunkB + kSlabBytes);
+            }
+            warp_arrive(b.wempty + wslot);
+            if (gs >= C::kASlots &&
+                !(ok = warp_wait(b.aempty + aslot, (uint32_t)(gs / C::kASlots - 1) & 1u, deadline)))
+                break;
+            tc_fence_after();
+            const uint32_t ta = a_lane + (uint32_t)(128 * aslot);
+            if (va) {
+                uint32_t lo[8], hi[8], v[16];
+                q8_half(a0, lo);
+                q8_half(a1, hi);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[i] = lo[i];
+                    v[8 + i] = hi[i];
+                }
+                tmem_st16(ta, v);
+            }
+            if (vb) {
+                uint32_t lo[8], hi[8], v[16];
+                q8_half(b0, lo);
+                q8_half(b1, hi);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[i] = lo[i];
+                    v[8 + i] = hi[i];
+                }
+                tmem_st16(ta + 16u, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(b.afull + aslot);
+            if (*abort_flag) {
+                ok = false;
+                break;
+            }
+        }
+    }
+    if (!ok) {
+        tmem_wait_st();
+        if (lane == 0) raise_timeout(group_status(g), abort_flag);
+        return;
+    }
+    tcsm_decoder_finish<C>(g, pieces, npieces, b.fin, fin_mask, abort_flag, deadline);
+}
+
 // ------------------------------------------------------------------ epilogue
 // The four epilogue warps meet on an mbarrier pair (in: four arrivals, out:
 // the leader's) at most twice per launch; `use` counts the meetings so the
@@ -472,11 +564,12 @@ struct EpiSync {
 // and store the BF16 result: row r of the tile, tokens 0..M-1.  The slot
 // `own` (or none, when own < 0) comes from `acc` instead of memory.  Eight
 // tokens' loads of a slot are in flight together.
-template <int NT>
+template <int NT, bool Q8>
 __device__ __forceinline__ void tcsm_reduce_row(const GemmParams &p, const Piece &pc, int r, int own,
                                                 float (&acc)[NT]) {
     constexpr int kB = 8;  // tokens per batch (register budget of the epilogue)
     const int64_t n = pc.tile * kTileRows + r;
+    const float sc = Q8 ? p.scales[n] : 1.0f;  // the Q8 copy's row scale (pad rows: 0)
     const float *src = p.partials + (n < p.N ? n : pc.tile * kTileRows);
     if (own == 0) {
         // this CTA holds slot 0 (the usual case: it computed the tile's first
@@ -497,8 +590,9 @@ __device__ __forceinline__ void tcsm_reduce_row(const GemmParams &p, const Piece
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             if (t >= p.M) break;
-            if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(acc[t]);
-            if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(acc[t], (uint32_t)n) : 0ull);
+            const float v = Q8 ? acc[t] * sc : acc[t];
+            if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(v);
+            if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(v, (uint32_t)n) : 0ull);
         }
         return;
     }
@@ -525,6 +619,7 @@ __device__ __forceinline__ void tcsm_reduce_row(const GemmParams &p, const Piece
         for (int u = 0; u < kB; ++u) {
             const int t = t0 + u;
             if (t >= p.M) break;
+            if (Q8) s[u] *= sc;
             if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(s[u]);
             if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(s[u], (uint32_t)n) : 0ull);
         }
@@ -600,8 +695,10 @@ __device__ void tcsm_epilogue(const GemmGroup &g, const Piece *pieces, int npiec
         warp_arrive(b.dempty + dbuf);
         const int64_t n = pc.tile * kTileRows + r;
         if (pc.count == 1) {
+            const float sc = C::kQ8 ? p.scales[n] : 1.0f;  // the Q8 copy's row scale (pad rows: 0)
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
+                if (C::kQ8) acc[t] *= sc;
                 if (t < p.M) {
                     if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(acc[t]);
                     if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(acc[t], (uint32_t)n) : 0ull);
@@ -615,7 +712,7 @@ __device__ void tcsm_epilogue(const GemmGroup &g, const Piece *pieces, int npiec
             ok = meet([&] { return load_acquire_gpu(counter) == (uint32_t)(pc.count - 1); });
             if (!ok) return;
             if (*flag) {
-                tcsm_reduce_row<NT>(p, pc, r, pc.idx, acc);
+                tcsm_reduce_row<NT, C::kQ8>(p, pc, r, pc.idx, acc);
                 if (leader) *counter = 0u;  // every CTA of the tile has arrived
                 continue;
             }
@@ -650,10 +747,10 @@ __device__ void tcsm_epilogue(const GemmGroup &g, const Piece *pieces, int npiec
 }
 
 // ------------------------------------------------------------------ kernel
-template <int NTOK>
-__global__ void __launch_bounds__(TcSmCfg<NTOK>::kThreads, 1)
+template <int NTOK, bool Q8 = false>
+__global__ void __launch_bounds__(TcSmCfg<NTOK, Q8>::kThreads, 1)
     w12_gemm_tc_sm_kernel(const __grid_constant__ GemmGroup grp, const __grid_constant__ CUtensorMap tmap_x) {
-    using C = TcSmCfg<NTOK>;
+    using C = TcSmCfg<NTOK, Q8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBars);
@@ -726,7 +823,7 @@ __global__ void __launch_bounds__(TcSmCfg<NTOK>::kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     if (threadIdx.x == 0) pdl_launch_dependents();
     const int np = (int)*npieces;
-    if (warp == C::kProdWarp && (threadIdx.x & 31) == 0) prefetch_pieces<kChunkBytes, true>(grp, pieces, np);
+    if (warp == C::kProdWarp && (threadIdx.x & 31) == 0) prefetch_pieces<C::kChunkB, !Q8>(grp, pieces, np);
     pdl_wait();
 
     if (warp == C::kProdWarp) {
@@ -739,7 +836,10 @@ __global__ void __launch_bounds__(TcSmCfg<NTOK>::kThreads, 1)
     } else if (warp >= C::kEpiWarp0 && warp < C::kEpiWarp0 + C::kEpiWarps) {
         tcsm_epilogue<C>(grp, pieces, np, b, abort_flag, last_flags, fin_mask, tmem_base, deadline);
     } else {
-        tcsm_decode<C>(grp, pieces, np, smem, b, abort_flag, fin_mask, tmem_base, deadline);
+        if constexpr (Q8)
+            tcsm_decode_q8<C>(grp, pieces, np, smem, b, abort_flag, fin_mask, tmem_base, deadline);
+        else
+            tcsm_decode<C>(grp, pieces, np, smem, b, abort_flag, fin_mask, tmem_base, deadline);
     }
     tc_fence_before();
     __syncthreads();

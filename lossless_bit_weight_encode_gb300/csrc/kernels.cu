@@ -78,7 +78,7 @@ struct DeviceState {
     int q8_occupancy[2] = {0, 0};            // [ntok==32], Q8 copy kernels
     int gemv_occupancy[2] = {0, 0};          // GEMV with 1, 2 token rows
     int gemv_sm_occupancy[2] = {0, 0};       // one-CTA-per-SM GEMV with 1, 2 token rows
-    int tc_sm_occupancy[2] = {0, 0};         // one-CTA-per-SM tensor-core kernel, [ntok==32]
+    int tc_sm_occupancy[2][2] = {{0, 0}, {0, 0}};  // one-CTA-per-SM tensor-core kernel, [q8][ntok==32]
 };
 
 DeviceState g_state[kMaxDevices];
@@ -180,10 +180,10 @@ int prepare_gemv_sm(DeviceState &s, std::string *err) {
     return W12_OK;
 }
 
-template <int NTOK>
+template <int NTOK, bool Q8>
 int prepare_tc_sm(DeviceState &s, std::string *err) {
-    using C = dev::TcSmCfg<NTOK>;
-    void *k = reinterpret_cast<void *>(&dev::w12_gemm_tc_sm_kernel<NTOK>);
+    using C = dev::TcSmCfg<NTOK, Q8>;
+    void *k = reinterpret_cast<void *>(&dev::w12_gemm_tc_sm_kernel<NTOK, Q8>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(tc_sm)", err);
     e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -192,7 +192,7 @@ int prepare_tc_sm(DeviceState &s, std::string *err) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, C::kThreads, (size_t)C::kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(tc_sm)", err);
     // all 512 TMEM columns: one CTA per SM whatever else would fit
-    s.tc_sm_occupancy[NTOK == 32] = occ < 1 ? occ : 1;
+    s.tc_sm_occupancy[Q8][NTOK == 32] = occ < 1 ? occ : 1;
     return W12_OK;
 }
 
@@ -229,8 +229,10 @@ int device_state(DeviceState **out, std::string *err) {
         if (rc == W12_OK) rc = prepare_gemm<32, false>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<16, true>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<32, true>(s, err);
-        if (rc == W12_OK) rc = prepare_tc_sm<16>(s, err);
-        if (rc == W12_OK) rc = prepare_tc_sm<32>(s, err);
+        if (rc == W12_OK) rc = prepare_tc_sm<16, false>(s, err);
+        if (rc == W12_OK) rc = prepare_tc_sm<32, false>(s, err);
+        if (rc == W12_OK) rc = prepare_tc_sm<16, true>(s, err);
+        if (rc == W12_OK) rc = prepare_tc_sm<32, true>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<16, false, true>(s, err);
         if (rc == W12_OK) rc = prepare_gemm<32, false, true>(s, err);
         if (rc != W12_OK) return rc;
@@ -363,11 +365,11 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     if (rc != W12_OK) return rc;
     plan->gemv = !q8 && use_gemv(M);
     plan->gemv_sm = plan->gemv && use_gemv_sm(info, s->sm_count);
-    plan->tc_sm = !plan->gemv && !q8 && use_tc_sm();
+    plan->tc_sm = !plan->gemv && use_tc_sm();
     plan->ntok = plan->gemv ? M : plan->tc_sm ? tc_sm_token_tile(M) : tc_token_tile(M, info.tiles, s->sm_count);
     const int occ = plan->gemv_sm ? s->gemv_sm_occupancy[M - 1]
                     : plan->gemv  ? s->gemv_occupancy[M - 1]
-                    : plan->tc_sm ? s->tc_sm_occupancy[plan->ntok == 32]
+                    : plan->tc_sm ? s->tc_sm_occupancy[q8][plan->ntok == 32]
                     : q8          ? s->q8_occupancy[plan->ntok == 32]
                                   : s->occupancy[plan->ntok == 32][use_smem_a_operand()];
     if (occ < 1) {
@@ -388,6 +390,13 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     // because the tile count does not divide the resident CTA count
     const int64_t units = tiles * segs;
     int64_t sk_ctas = capacity < units ? capacity : units;
+    // the one-CTA-per-SM kernels give each CTA at least kMinRange segments:
+    // below that a CTA's fixed costs (first stage, split-K finish) outweigh its
+    // streaming, and a small matrix (1024 x 5120: 160 segments) would split
+    // every tile twenty ways
+    constexpr int64_t kMinRange = 4;
+    if ((plan->gemv_sm || plan->tc_sm) && units < kMinRange * sk_ctas)
+        sk_ctas = std::max<int64_t>(1, units / kMinRange);
     // the range of a CTA: at most kMaxSegs segment headers and, for the
     // one-CTA-per-SM kernel, at most kMaxPieces tiles; for the two-CTA kernel
     // at most two tiles (a single wave of more CTAs than tiles)
@@ -686,7 +695,13 @@ int gemm_impl(const uint16_t *x_dev, int count, const void *const *blobs, const 
                                   (size_t)GemvC<2>::kSmemBytes, st, p, tm);
     } else if (plan.tc_sm) {
         const dim3 grid = plan.units > 0 ? dim3((unsigned)plan.ctas, 1u) : dim3((unsigned)plan.splits, (unsigned)info.tiles);
-        if (plan.ntok == 16)
+        if (q8 && plan.ntok == 16)
+            e = launch_overlapped(dev::w12_gemm_tc_sm_kernel<16, true>, grid, dim3(dev::TcSmCfg<16, true>::kThreads),
+                                  (size_t)dev::TcSmCfg<16, true>::kSmemBytes, st, p, tm);
+        else if (q8)
+            e = launch_overlapped(dev::w12_gemm_tc_sm_kernel<32, true>, grid, dim3(dev::TcSmCfg<32, true>::kThreads),
+                                  (size_t)dev::TcSmCfg<32, true>::kSmemBytes, st, p, tm);
+        else if (plan.ntok == 16)
             e = launch_overlapped(dev::w12_gemm_tc_sm_kernel<16>, grid, dim3(dev::TcSmCfg<16>::kThreads),
                                   (size_t)dev::TcSmCfg<16>::kSmemBytes, st, p, tm);
         else

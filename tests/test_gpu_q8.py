@@ -1,7 +1,8 @@
-"""Q8 copy GEMM (w12_q8_gemm) on the tensor-core kernel against the oracle's
-fp64 product over its own Q8 copy (same quantizer, same fp32 decisions):
-tolerance on every output, bit-exact where the arithmetic is exact (one-hot
-x), and full layer shapes on sampled rows."""
+"""Q8 copy GEMM (w12_q8_gemm) on both tensor-core kernels (one CTA per SM with
+stream-K ranges, and several CTAs per SM with fixed split-K) against the
+oracle's fp64 product over its own Q8 copy (same quantizer, same fp32
+decisions): tolerance on every output, bit-exact where the arithmetic is exact
+(one-hot x), ranges across tiles, and full layer shapes on sampled rows."""
 import numpy as np
 import pytest
 
@@ -16,6 +17,12 @@ pytestmark = pytest.mark.gpu
 def built():
     from gpu_util import ensure_built
     ensure_built()
+
+
+@pytest.fixture(params=[1, 0], ids=["tc_sm", "tc_multi"])
+def q8_kernel(request, w12_opts):
+    w12_opts(tc_sm=request.param)
+    return request.param
 
 
 def _gemm(mat, x_bits):
@@ -42,7 +49,7 @@ def test_q8_single_output_within_one_ulp():
 
 @pytest.mark.parametrize("shape", [(129, 33), (384, 2048), (300, 1001), (130, 7000)])
 @pytest.mark.parametrize("M", [1, 2, 5, 16, 17, 32])
-def test_q8_gemm_matches_oracle(shape, M):
+def test_q8_gemm_matches_oracle(shape, M, q8_kernel):
     from gpu_util import check_tolerance
     n, k = shape
     w = wl.heavy_tail_weights(n, k, seed=70 + n + k)
@@ -50,7 +57,7 @@ def test_q8_gemm_matches_oracle(shape, M):
     check_tolerance(_gemm(Q8Weight(w), x), oracle.q8_gemm_f64(x, w), f"q8 {shape} M={M}")
 
 
-def test_q8_one_hot_is_exact():
+def test_q8_one_hot_is_exact(q8_kernel):
     """x = e_k: the sum is q[n][k] exactly; y = BF16(fp32(s[n] * q[n][k]))."""
     w = wl.gaussian_weights(256, 512, seed=72)
     s, q = oracle.q8_decode(oracle.q8_encode(w), 256, 512)
@@ -73,3 +80,15 @@ def test_q8_layer_shapes_sampled_rows():
             x = wl.activations(M, w.shape[1], seed=wl.activation_seed("layer", M))
             ref = oracle.q8_gemm_f64(x, np.ascontiguousarray(w[rows]))
             check_tolerance(_gemm(mat, x)[:, rows], ref, f"q8 {name} M={M}")
+
+
+@pytest.mark.parametrize("M", [3, 16, 32])
+def test_q8_stream_k_ranges(M):
+    """Ranges that end inside a tile (12763 x 5020) and many short tiles
+    (60000 x 64) on the one-CTA-per-SM kernel."""
+    from gpu_util import check_tolerance
+    for n, k in [(12763, 5020), (60000, 64)]:
+        w = wl.heavy_tail_weights(n, k, seed=74 + n % 91)
+        x = wl.activations(M, k, seed=75 + M)
+        mat = Q8Weight(w)
+        check_tolerance(_gemm(mat, x), oracle.q8_gemm_f64(x, w), f"q8 {n}x{k} M={M}")

@@ -48,7 +48,10 @@ def test_stream_k_matches_oracle(M, shape, gemv_kernel, w12_opts):
         plan = w12.w12_gemm_launch_info(mat.info, M)
         tiles, segs = int(mat.info.tiles), int(mat.info.segs)
         if mode == "1":
-            assert plan["ctas"] == min(_capacity(plan), tiles * segs), plan
+            expect = min(_capacity(plan), tiles * segs)
+            if plan["ctas_per_sm"] == 1 and tiles * segs < 4 * expect:
+                expect = max(1, tiles * segs // 4)  # at least four segments per CTA
+            assert plan["ctas"] == expect, plan
         else:
             assert plan["ctas"] == tiles * plan["splits"], plan
         y = dev_to_bits(mat.gemm(to_dev_bf16(x)))
