@@ -4,8 +4,11 @@
 //
 // One CTA of 128 threads per (tile, segment); warp q owns quarter q (32 rows),
 // each thread one row.  Per chunk a warp reads its 3 x 512 contiguous bytes
-// with 16-byte loads, decodes in registers (same routine as the GEMM) and
-// writes 64 bytes per row.  Streams 1.5 B in and 2 B out per weight.
+// with 16-byte loads and decodes in registers (same routine as the GEMM).  The
+// 64 output bytes of each row are staged in shared memory and written back
+// 8 rows x 64 bytes per warp instruction, so each store covers whole 32-byte
+// sectors instead of 16 bytes in each of 32 rows.  Streams 1.5 B in and 2 B
+// out per weight.
 #pragma once
 
 #include "w12_device.cuh"
@@ -22,6 +25,10 @@ struct DecodeParams {
 };
 
 __global__ void __launch_bounds__(128) w12_decode_kernel(const __grid_constant__ DecodeParams p) {
+    // 128 rows x 64 bytes; 16-byte piece g of row r sits at piece
+    // g ^ ((r >> 1) & 3), so both the row-wise writes of eight consecutive
+    // lanes and the 2-rows-by-4-pieces reads of eight lanes hit distinct banks
+    __shared__ __align__(16) uint8_t stage[kTileRows * 64];
     const int seg = blockIdx.x;
     const int64_t tile = blockIdx.y;
     const int q = threadIdx.x >> 5;
@@ -55,13 +62,25 @@ __global__ void __launch_bounds__(128) w12_decode_kernel(const __grid_constant__
         assemble(s_lo, s_hi, E, out);
 
         const int64_t k0 = chunk * kChunkK;
-        if (n >= p.N) continue;
-        uint16_t *dst = p.out + n * p.K + k0;
         if (vec_ok && k0 + kChunkK <= p.K) {
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+            // stage this warp's 32 rows, then write them 8 rows x 64 bytes at a
+            // time: lane l takes row 8i + l / 4 of the quarter, bytes 16 (l % 4)
+            const int lane = r & 31;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) d4[g] = make_uint4(out[4 * g], out[4 * g + 1], out[4 * g + 2], out[4 * g + 3]);
-        } else {
+            for (int g = 0; g < 4; ++g)
+                *reinterpret_cast<uint4 *>(stage + 64 * r + 16 * (g ^ ((r >> 1) & 3))) =
+                    make_uint4(out[4 * g], out[4 * g + 1], out[4 * g + 2], out[4 * g + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int rr = 32 * q + 8 * i + (lane >> 2);
+                const int64_t nn = tile * kTileRows + rr;
+                const uint4 v = *reinterpret_cast<const uint4 *>(stage + 64 * rr + 16 * ((lane & 3) ^ ((rr >> 1) & 3)));
+                if (nn < p.N) *reinterpret_cast<uint4 *>(p.out + nn * p.K + k0 + 8 * (lane & 3)) = v;
+            }
+            __syncwarp();  // the stage is rewritten by the next chunk
+        } else if (n < p.N) {
+            uint16_t *dst = p.out + n * p.K + k0;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 if (k0 + 2 * i < p.K) dst[2 * i] = (uint16_t)(out[i] & 0xFFFFu);
