@@ -313,7 +313,7 @@ class LayerStep:
 
     def __init__(self, mats, names, xs_host, M, grouped, q8=False, argmax=False):
         import torch
-        from lossless_bit_weight_encode_gb300 import W12Group, w12
+        from lossless_bit_weight_encode_gb300 import Q8Group, W12Group, w12
 
         self.w12 = w12
         self.mats, self.names, self.M = mats, names, M
@@ -359,10 +359,10 @@ class LayerStep:
                                        (self.xs[i].data_ptr(), mats[i].blob.data_ptr(), mats[i].info,
                                         self.ys[i].data_ptr(), M, ws.data_ptr(), ws.numel(), sh)))
                 else:
-                    grp = W12Group([mats[i] for i in g])
+                    grp = (Q8Group if q8 else W12Group)([mats[i] for i in g])
                     gws = grp.workspace(M)
                     self.keep.append((grp, gws))
-                    self.calls.append((w12.w12_gemm_group_ptr,
+                    self.calls.append((w12.w12_q8_gemm_group_ptr if q8 else w12.w12_gemm_group_ptr,
                                        (self.xs[g[0]].data_ptr(), [mats[i].blob.data_ptr() for i in g], grp.infos,
                                         [self.ys[i].data_ptr() for i in g], M, gws.data_ptr(), gws.numel(), sh)))
         self.launch_names = ["+".join(names[i] for i in g) for g in self.groups]
@@ -373,7 +373,8 @@ class LayerStep:
         self.packed = sum(int(m.info.total_bytes) for m in mats)
         self.weights = sum(m.N * m.K for m in mats)
         if q8:
-            self.kernels = ["w12_gemm_tc_kernel (Q8 copy)"] * len(self.groups)
+            self.kernels = [w12.w12_q8_gemm_group_launch_info([mats[i].info for i in g], M)["kernel_name"]
+                            + " (Q8 copy)" for g in self.groups]
         else:
             self.kernels = [w12.w12_gemm_group_launch_info([mats[i].info for i in g], M)["kernel_name"]
                             for g in self.groups]
@@ -470,7 +471,7 @@ def sweep_point(mats, weights, xs_host, M, K, warmup, dense, q8=False):
     """µs per layer step at M tokens, the packed fraction of the HBM peak and
     the cuBLAS BF16 step on the same shapes and grouping."""
     peak, _ = hbm_peak_gbs()
-    st = LayerStep(mats, [n for n, _ in weights], xs_host, M, grouped=not q8, q8=q8)
+    st = LayerStep(mats, [n for n, _ in weights], xs_host, M, grouped=True, q8=q8)
     for _ in range(warmup):
         st.run()
     ms = time_steps(st.run, K)
@@ -577,7 +578,7 @@ def run_w12(args):
         mats = [Q8Weight(w) if q8 else W12Weight(w) for _, w in weights]
         xs_host = [wl.activations(M, w.shape[1], seed=wl.activation_seed(args.workload, M)) for _, w in weights]
         whole = args.workload in ("layer", "heavy") and names == list(LAYER_NAMES)
-        step = LayerStep(mats, names, xs_host, M, grouped=whole and not args.no_group and not q8, q8=q8,
+        step = LayerStep(mats, names, xs_host, M, grouped=whole and not args.no_group, q8=q8,
                          argmax=args.workload == "lmhead")
 
         def dense_weights():

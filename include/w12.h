@@ -331,6 +331,22 @@ int w12_q8_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_q8_info *
                 uint16_t *y_dev, int M, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Q8 copies of up to W12_MAX_GROUP matrices that multiply the same x (the
+ * q/k/v or gate/up projections) in one launch, as w12_gemm_group does for
+ * W12 blobs: y_devs[i] = the w12_q8_gemm product of x with blob i, with
+ * blob i's own row scales.  blobs_dev[i] 256-byte aligned, y_devs[i] M x N_i
+ * BF16; infos[i] from w12_q8_blob_info; all K equal (SHAPE otherwise).
+ * Workspace: w12_q8_gemm_group_workspace_size bytes; launch_info fills
+ * out[0..4] as w12_gemm_group_launch_info.  Errors as w12_gemm_group.
+ */
+int w12_q8_gemm_group_workspace_size(int count, const w12_q8_info *infos, int M, size_t *bytes);
+
+int w12_q8_gemm_group_launch_info(int count, const w12_q8_info *infos, int M, int32_t out[5]);
+
+int w12_q8_gemm_group(const uint16_t *x_dev, int count, const void *const *blobs_dev, const w12_q8_info *infos,
+                      uint16_t *const *y_devs, int M, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's status word,
  * which kernels set when a bounded wait gives up (TIMEOUT) or the device
  * encoder finds its output buffer too short (BUFFER_TOO_SMALL) or too many

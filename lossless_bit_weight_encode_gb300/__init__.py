@@ -11,7 +11,7 @@ import numpy as np
 from . import w12
 from .w12 import W12Error
 
-__all__ = ["w12", "W12Error", "W12Weight", "W12Group", "Q8Weight"]
+__all__ = ["w12", "W12Error", "W12Weight", "W12Group", "Q8Weight", "Q8Group"]
 
 
 class W12Weight:
@@ -182,3 +182,36 @@ class Q8Weight:
             out = torch.empty((M, self.N), dtype=torch.bfloat16, device=x.device)
         w12.w12_q8_gemm(x, self.blob, self.info, out, M, self.workspace(M), stream)
         return out
+
+
+class Q8Group:
+    """Q8 copies that multiply the same x, run as one launch (as W12Group)."""
+
+    def __init__(self, mats):
+        if not 1 <= len(mats) <= w12.MAX_GROUP or len({m.K for m in mats}) != 1:
+            raise ValueError(f"1..{w12.MAX_GROUP} matrices with the same K")
+        self.mats = list(mats)
+        self.K = mats[0].K
+        self.infos = [m.info for m in mats]
+        self._ws = {}
+
+    def workspace(self, M: int):
+        import torch
+
+        size = w12.w12_q8_gemm_group_workspace_size(self.infos, M)
+        ws = self._ws.get(M)
+        if ws is None or ws.numel() < size:
+            ws = torch.zeros(max(size, 256), dtype=torch.uint8, device=self.mats[0].blob.device)
+            self._ws[M] = ws
+        return ws
+
+    def gemm(self, x, outs=None, stream=None):
+        import torch
+
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != self.K or not x.is_contiguous():
+            raise ValueError("x must be a contiguous BF16 tensor of shape [M, K]")
+        M = int(x.shape[0])
+        if outs is None:
+            outs = [torch.empty((M, m.N), dtype=torch.bfloat16, device=x.device) for m in self.mats]
+        w12.w12_q8_gemm_group(x, [m.blob for m in self.mats], self.infos, outs, M, self.workspace(M), stream)
+        return outs

@@ -424,6 +424,89 @@ int w12_q8_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_q8_info *
     });
 }
 
+namespace {
+int check_q8_group(int count, const w12_q8_info *infos, std::string &err) {
+    if (count < 1 || count > W12_MAX_GROUP || !infos) {
+        err = "count must be in 1.." + std::to_string(W12_MAX_GROUP) + " with non-null infos";
+        return W12_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < count; ++i) {
+        const int rc = check_q8_info(&infos[i], err);
+        if (rc != W12_OK) return rc;
+        if (infos[i].K != infos[0].K) {
+            err = "the matrices of a group must share K (they multiply the same x)";
+            return W12_ERR_SHAPE;
+        }
+    }
+    return W12_OK;
+}
+}  // namespace
+
+int w12_q8_gemm_group_launch_info(int count, const w12_q8_info *infos, int M, int32_t out[5]) {
+    return guarded([&](std::string &err) {
+        int rc = check_q8_group(count, infos, err);
+        if (rc != W12_OK) return rc;
+        if (!out) {
+            err = "out is null";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        w12::launch::GemmPlan plan;
+        rc = w12::launch::q8_group_plan(count, infos, M, &plan, &err);
+        if (rc == W12_OK) {
+            out[0] = plan.ntok;
+            out[1] = plan.splits;
+            out[2] = plan.ctas;
+            out[3] = plan.ctas_per_sm;
+            out[4] = plan.kernel;
+        }
+        return rc;
+    });
+}
+
+int w12_q8_gemm_group_workspace_size(int count, const w12_q8_info *infos, int M, size_t *bytes) {
+    return guarded([&](std::string &err) {
+        int rc = check_q8_group(count, infos, err);
+        if (rc != W12_OK) return rc;
+        if (!bytes || M < 1 || M > 32) {
+            err = "null pointer or M outside 1..32";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        return w12::launch::q8_group_workspace_size(count, infos, M, bytes, &err);
+    });
+}
+
+int w12_q8_gemm_group(const uint16_t *x_dev, int count, const void *const *blobs_dev, const w12_q8_info *infos,
+                      uint16_t *const *y_devs, int M, void *workspace, size_t ws_bytes, void *stream) {
+    return guarded([&](std::string &err) {
+        int rc = check_q8_group(count, infos, err);
+        if (rc != W12_OK) return rc;
+        if (!x_dev || !blobs_dev || !y_devs || !workspace) {
+            err = "null pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (M < 1 || M > 32) {
+            err = "M must be in 1..32";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (!aligned(workspace, 256) || !aligned(x_dev, 2)) {
+            err = "workspace must be 256-byte aligned and x_dev 2-byte aligned";
+            return (int)W12_ERR_ALIGNMENT;
+        }
+        for (int i = 0; i < count; ++i) {
+            if (!blobs_dev[i] || !y_devs[i]) {
+                err = "null blob or output";
+                return (int)W12_ERR_INVALID_ARG;
+            }
+            if (!aligned(blobs_dev[i], 256) || !aligned(y_devs[i], 2)) {
+                err = "each blob must be 256-byte aligned and each y 2-byte aligned";
+                return (int)W12_ERR_ALIGNMENT;
+            }
+        }
+        return w12::launch::q8_gemm_group(x_dev, count, blobs_dev, infos, y_devs, M, workspace, ws_bytes, stream,
+                                          &err);
+    });
+}
+
 int w12_check_status(void *stream) {
     return guarded([&](std::string &err) { return w12::launch::check_status(stream, &err); });
 }

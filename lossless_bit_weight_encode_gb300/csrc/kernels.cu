@@ -497,7 +497,7 @@ cudaError_t launch_gemm_kernel(const dev::GemmGroup &p, const CUtensorMap &tm, i
 namespace {
 int gemm_impl(const uint16_t *x_dev, int count, const void *const *blobs, const w12_info *infos,
               uint16_t *const *ys, unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream,
-              std::string *err, const w12_q8_info *q8 = nullptr);
+              std::string *err, const w12_q8_info *q8 = nullptr);  // q8: one info per matrix, or null
 int gemm_impl(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev,
               unsigned long long *amax, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err,
               const w12_q8_info *q8 = nullptr) {
@@ -544,6 +544,33 @@ int q8_workspace_size(const w12_q8_info &info, int M, size_t *bytes, std::string
 int q8_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_q8_info &info, uint16_t *y_dev, int M,
             void *workspace, size_t ws_bytes, void *stream, std::string *err) {
     return gemm_impl(x_dev, blob_dev, q8_as_info(info), y_dev, nullptr, M, workspace, ws_bytes, stream, err, &info);
+}
+
+namespace {
+// The w12_info views of a Q8 group (count <= kMaxGroup, checked by the caller).
+void q8_group_infos(int count, const w12_q8_info *q8, w12_info (&infos)[dev::kMaxGroup]) {
+    for (int i = 0; i < count; ++i) infos[i] = q8_as_info(q8[i]);
+}
+}  // namespace
+
+int q8_group_plan(int count, const w12_q8_info *q8, int M, GemmPlan *plan, std::string *err) {
+    w12_info infos[dev::kMaxGroup];
+    q8_group_infos(count, q8, infos);
+    return plan_gemm(group_info(count, infos), M, plan, err, true);
+}
+
+int q8_group_workspace_size(int count, const w12_q8_info *q8, int M, size_t *bytes, std::string *err) {
+    GemmPlan plan;
+    const int rc = q8_group_plan(count, q8, M, &plan, err);
+    if (rc == W12_OK) *bytes = plan.ws_bytes;
+    return rc;
+}
+
+int q8_gemm_group(const uint16_t *x_dev, int count, const void *const *blobs, const w12_q8_info *q8,
+                  uint16_t *const *ys, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err) {
+    w12_info infos[dev::kMaxGroup];
+    q8_group_infos(count, q8, infos);
+    return gemm_impl(x_dev, count, blobs, infos, ys, nullptr, M, workspace, ws_bytes, stream, err, q8);
 }
 
 int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,
@@ -668,7 +695,7 @@ int gemm_impl(const uint16_t *x_dev, int count, const void *const *blobs, const 
         q.counters = reinterpret_cast<uint32_t *>(ws + plan.ws_counters) + tile0;
         q.y = ys[i];
         q.amax = amax;
-        q.scales = q8 ? reinterpret_cast<const float *>(q.blob + q8->off_scales) : nullptr;
+        q.scales = q8 ? reinterpret_cast<const float *>(q.blob + q8[i].off_scales) : nullptr;
         q.status = s->status;
         q.timeout_ns = timeout_ns();
         p.tile0[i] = tile0;

@@ -597,18 +597,24 @@ __device__ __forceinline__ uint32_t arrive_relaxed(uint32_t *counter) {
 // lower column in the low half, exactly: byte b ^ 0x80 = b + 128 goes into
 // the low mantissa bits of 2^23 (0x4B000000), and subtracting 2^23 + 128 in
 // fp32 leaves b; |b| <= 128 keeps the value exact in BF16, so its top 16 bits
-// are the BF16 pattern.
+// are the BF16 pattern.  The subtractions run two at a time (sub.f32x2).
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ void q8_half(const uint4 &v, uint32_t (&out)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    constexpr uint64_t kMagic2 = 0x4B0000804B000080ull;  // (2^23 + 128, 2^23 + 128)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const uint32_t u = w[j] ^ 0x80808080u;
-        const float f0 = __uint_as_float(prmt(u, 0x4B000000u, 0x7440u)) - 8388736.0f;
-        const float f1 = __uint_as_float(prmt(u, 0x4B000000u, 0x7441u)) - 8388736.0f;
-        const float f2 = __uint_as_float(prmt(u, 0x4B000000u, 0x7442u)) - 8388736.0f;
-        const float f3 = __uint_as_float(prmt(u, 0x4B000000u, 0x7443u)) - 8388736.0f;
-        out[2 * j] = prmt(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);
-        out[2 * j + 1] = prmt(__float_as_uint(f2), __float_as_uint(f3), 0x7632u);
+        const uint64_t p01 = ((uint64_t)prmt(u, 0x4B000000u, 0x7441u) << 32) | prmt(u, 0x4B000000u, 0x7440u);
+        const uint64_t p23 = ((uint64_t)prmt(u, 0x4B000000u, 0x7443u) << 32) | prmt(u, 0x4B000000u, 0x7442u);
+        const uint64_t d01 = sub_f32x2(p01, kMagic2), d23 = sub_f32x2(p23, kMagic2);
+        out[2 * j] = prmt((uint32_t)d01, (uint32_t)(d01 >> 32), 0x7632u);
+        out[2 * j + 1] = prmt((uint32_t)d23, (uint32_t)(d23 >> 32), 0x7632u);
     }
 }
 

@@ -34,6 +34,13 @@ int q8_workspace_size(const w12_q8_info &info, int M, size_t *bytes, std::string
 int q8_gemm(const uint16_t *x_dev, const void *blob_dev, const w12_q8_info &info, uint16_t *y_dev, int M,
             void *workspace, size_t ws_bytes, void *stream, std::string *err);
 
+int q8_group_plan(int count, const w12_q8_info *infos, int M, GemmPlan *plan, std::string *err);
+
+int q8_group_workspace_size(int count, const w12_q8_info *infos, int M, size_t *bytes, std::string *err);
+
+int q8_gemm_group(const uint16_t *x_dev, int count, const void *const *blobs, const w12_q8_info *infos,
+                  uint16_t *const *ys, int M, void *workspace, size_t ws_bytes, void *stream, std::string *err);
+
 int decode(const void *blob_dev, const w12_info &info, uint16_t *out_dev, void *stream, std::string *err);
 
 int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,

@@ -27,6 +27,7 @@ EXPORTED = (
     "w12_blob_info", "w12_blob_validate", "w12_decode", "w12_gemm_workspace_size", "w12_gemm_launch_info",
     "w12_gemm", "w12_gemm_group_workspace_size", "w12_gemm_group", "w12_gemm_group_launch_info", "w12_gemm_argmax_workspace_size", "w12_gemm_argmax", "w12_gemm_noalloc", "w12_encode_workspace_size", "w12_encoded_size_device", "w12_encode_device",
     "w12_q8_encoded_size", "w12_q8_encode_host", "w12_q8_blob_info", "w12_q8_gemm_workspace_size", "w12_q8_gemm",
+    "w12_q8_gemm_group_workspace_size", "w12_q8_gemm_group_launch_info", "w12_q8_gemm_group",
     "w12_check_status", "w12_selftest_timeout", "w12_set_option", "w12_get_option",
 )
 
@@ -105,6 +106,11 @@ def lib() -> ctypes.CDLL:
     L.w12_q8_blob_info.argtypes = [vp, sz, ctypes.POINTER(w12_q8_info)]
     L.w12_q8_gemm_workspace_size.argtypes = [ctypes.POINTER(w12_q8_info), i32, ctypes.POINTER(sz)]
     L.w12_q8_gemm.argtypes = [vp, vp, ctypes.POINTER(w12_q8_info), vp, i32, vp, sz, vp]
+    L.w12_q8_gemm_group_workspace_size.argtypes = [i32, ctypes.POINTER(w12_q8_info), i32, ctypes.POINTER(sz)]
+    L.w12_q8_gemm_group_launch_info.argtypes = [i32, ctypes.POINTER(w12_q8_info), i32,
+                                                ctypes.POINTER(ctypes.c_int32)]
+    L.w12_q8_gemm_group.argtypes = [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(w12_q8_info), ctypes.POINTER(vp),
+                                    i32, vp, sz, vp]
     L.w12_check_status.argtypes = [vp]
     L.w12_selftest_timeout.argtypes = [ctypes.c_uint32, vp]
     L.w12_set_option.argtypes = [ctypes.c_char_p, i64]
@@ -339,6 +345,39 @@ def w12_q8_gemm_ptr(x_ptr: int, blob_ptr: int, info: w12_q8_info, y_ptr: int, M:
                     stream_handle: int | None) -> int:
     """Raw-pointer form of w12_q8_gemm that returns the status."""
     return lib().w12_q8_gemm(x_ptr, blob_ptr, ctypes.byref(info), y_ptr, int(M), ws_ptr, ws_bytes, stream_handle)
+
+
+def _q8_infos(infos) -> ctypes.Array:
+    return (w12_q8_info * len(infos))(*infos)
+
+
+def w12_q8_gemm_group_workspace_size(infos, M: int) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().w12_q8_gemm_group_workspace_size(len(infos), _q8_infos(infos), int(M), ctypes.byref(out)))
+    return out.value
+
+
+def w12_q8_gemm_group_launch_info(infos, M: int) -> dict:
+    """Plan of a grouped Q8 launch (one info: a single w12_q8_gemm)."""
+    out = (ctypes.c_int32 * 5)()
+    _check(lib().w12_q8_gemm_group_launch_info(len(infos), _q8_infos(infos), int(M), out))
+    return {"ntok": out[0], "splits": out[1], "ctas": out[2], "ctas_per_sm": out[3], "kernel": out[4],
+            "kernel_name": KERNEL_NAMES.get(out[4], str(out[4]))}
+
+
+def w12_q8_gemm_group_ptr(x_ptr: int, blob_ptrs, infos, y_ptrs, M: int, ws_ptr: int, ws_bytes: int,
+                          stream_handle: int | None) -> int:
+    """Raw-pointer form of w12_q8_gemm_group that returns the status."""
+    n = len(infos)
+    return lib().w12_q8_gemm_group(x_ptr, n, (ctypes.c_void_p * n)(*blob_ptrs), _q8_infos(infos),
+                                   (ctypes.c_void_p * n)(*y_ptrs), int(M), ws_ptr, ws_bytes, stream_handle)
+
+
+def w12_q8_gemm_group(x_dev, blobs_dev, infos, ys_dev, M: int, workspace, stream=None) -> None:
+    """ys_dev[i] = the Q8 product of x_dev with copy i, for copies sharing K, in one launch."""
+    _check(w12_q8_gemm_group_ptr(x_dev.data_ptr(), [b.data_ptr() for b in blobs_dev], infos,
+                                 [y.data_ptr() for y in ys_dev], M, workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(), _stream_handle(stream)))
 
 
 def w12_check_status(stream=None) -> None:

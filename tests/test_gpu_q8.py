@@ -92,3 +92,41 @@ def test_q8_stream_k_ranges(M):
         x = wl.activations(M, k, seed=75 + M)
         mat = Q8Weight(w)
         check_tolerance(_gemm(mat, x), oracle.q8_gemm_f64(x, w), f"q8 {n}x{k} M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 32])
+def test_q8_group_matches_oracle(M, q8_kernel):
+    """Q8 copies sharing K in one launch (ragged member heights, a tile that
+    ends inside a member): every output within tolerance of the oracle's
+    product over its own copy, each with its own row scales."""
+    import torch
+    from gpu_util import check_tolerance, dev_to_bits, to_dev_bf16
+    from lossless_bit_weight_encode_gb300 import Q8Group
+    k = 1000
+    ws = [wl.heavy_tail_weights(n, k, seed=76 + n) for n in (300, 129, 640)]
+    x = wl.activations(M, k, seed=77 + M)
+    ys = Q8Group([Q8Weight(w) for w in ws]).gemm(to_dev_bf16(x))
+    w12.w12_check_status()
+    torch.cuda.synchronize()
+    for i, (w, y) in enumerate(zip(ws, ys)):
+        check_tolerance(dev_to_bits(y), oracle.q8_gemm_f64(x, w), f"q8 group member {i} M={M}")
+
+
+def test_q8_layer_groups_sampled_rows():
+    """The layer's q+k+v and gate+up groups at full size, sampled rows."""
+    import torch
+    from gpu_util import check_tolerance, dev_to_bits, to_dev_bf16
+    from lossless_bit_weight_encode_gb300 import Q8Group
+    rng = np.random.default_rng(78)
+    ws = dict(wl.layer_weights("layer"))
+    for names in (("q", "k", "v"), ("gate", "up")):
+        grp = Q8Group([Q8Weight(ws[n]) for n in names])
+        for M in (1, 16, 32):
+            x = wl.activations(M, grp.K, seed=wl.activation_seed("layer", M))
+            ys = grp.gemm(to_dev_bf16(x))
+            w12.w12_check_status()
+            torch.cuda.synchronize()
+            for n, y in zip(names, ys):
+                rows = np.sort(rng.choice(ws[n].shape[0], size=128, replace=False))
+                ref = oracle.q8_gemm_f64(x, np.ascontiguousarray(ws[n][rows]))
+                check_tolerance(dev_to_bits(y)[:, rows], ref, f"q8 {n} (group) M={M}")

@@ -201,6 +201,20 @@ def test_gemm_argument_errors_before_any_device_work():
     q8 = w12.w12_q8_blob_info(w12.w12_q8_encode_host(wl.gaussian_weights(200, 300, seed=42)))
     assert w12.w12_q8_gemm_ptr(0, a, q8, a, 1, a, 1 << 20, None) == INVALID
     assert w12.w12_q8_gemm_ptr(a, a + 8, q8, a, 1, a, 1 << 20, None) == ALIGN
+    # grouped Q8 launch: member count, shared K, a W12 info in place of a Q8
+    # one, null and misaligned members
+    q8_other_k = w12.w12_q8_blob_info(w12.w12_q8_encode_host(wl.gaussian_weights(130, 64, seed=43)))
+    assert w12.w12_q8_gemm_group_ptr(a, [], [], [], 1, a, 1 << 20, None) == INVALID
+    assert w12.w12_q8_gemm_group_ptr(a, [a] * 5, [q8] * 5, [a] * 5, 1, a, 1 << 20, None) == INVALID
+    assert w12.w12_q8_gemm_group_ptr(a, [a, a], [q8, q8_other_k], [a, a], 1, a, 1 << 20, None) == SHAPE
+    assert w12.w12_q8_gemm_group_ptr(a, [a, 0], [q8, q8], [a, a], 1, a, 1 << 20, None) == INVALID
+    assert w12.w12_q8_gemm_group_ptr(a, [a, a + 64], [q8, q8], [a, a], 1, a, 1 << 20, None) == ALIGN
+    assert w12.w12_q8_gemm_group_ptr(a, [a, a], [q8, q8], [a, a], 33, a, 1 << 20, None) == INVALID
+    bad = w12.w12_q8_info()
+    bad.N, bad.K = q8.N, q8.K  # geometry fields left at zero
+    assert w12.w12_q8_gemm_group_ptr(a, [a], [bad], [a], 1, a, 1 << 20, None) != 0
+    out5 = (ctypes.c_int32 * 5)()
+    assert lib.w12_q8_gemm_group_launch_info(0, None, 1, out5) == INVALID
     assert w12.w12_last_error() != ""
 
 
