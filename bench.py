@@ -31,6 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "W12 decode-GEMM effective weight GB/s & µs/layer at M=1–32; % of HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("lossless_bit_weight_encode_gb300/csrc/gemm_tc.cuh",
+                  "lossless_bit_weight_encode_gb300/csrc/gemm_tc_sm.cuh",
                   "lossless_bit_weight_encode_gb300/csrc/gemv.cuh",
                   "lossless_bit_weight_encode_gb300/csrc/gemv_sm.cuh",
                   "lossless_bit_weight_encode_gb300/csrc/w12_device.cuh",

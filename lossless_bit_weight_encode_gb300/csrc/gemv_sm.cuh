@@ -214,6 +214,22 @@ __device__ void gemv_sm_producer(const GemmGroup &g, const Piece *pieces, int np
         }
         hseg += pc.s1 - pc.s0;
     }
+    // the range's last tile: when the CTAs sharing it have all arrived (they
+    // started on it at the beginning of their ranges), pull their slots into
+    // L1 now, a few stages before the decoders finish the piece and add them
+    if (!failed && !*abort_flag && npieces > 0 && pieces[npieces - 1].count > 1) {
+        const Piece &pl = pieces[npieces - 1];
+        const GemmParams &p = g.m[pl.member];
+        if (load_acquire_gpu(p.counters + pl.tile) == (uint32_t)(pl.count - 1)) {
+            const float *base = p.partials + pl.tile * kTileRows;
+            for (int sp = 0; sp < pl.count; ++sp)
+                if (sp != pl.idx)
+                    for (int t = 0; t < p.M; ++t)
+#pragma unroll
+                        for (int l = 0; l < kTileRows; l += 32)
+                            prefetch_l1(base + ((int64_t)sp * p.M + t) * p.Npad + l);
+        }
+    }
     if (first_pending && !failed && !*abort_flag) {
         if (mbar_wait(b.first_done, 0, deadline))
             gemv_first_arrival(g, pieces[0], fin_mask);
@@ -415,8 +431,10 @@ __device__ void gemv_sm_decode(const GemmGroup &g, const Piece *pieces, int npie
                 for (int t = 0; t < MT; ++t) {
                     if (t >= p.M) continue;
                     float s = 0.0f;
+                    // through L1: the acquire above showed the slots complete
+                    // (and the producer may have prefetched them)
                     for (int sp = 0; sp < pc.count; ++sp)
-                        s += sp == pc.idx ? total[t] : __ldcg(src + (int64_t)t * p.Npad + (int64_t)sp * stride);
+                        s += sp == pc.idx ? total[t] : __ldca(src + (int64_t)t * p.Npad + (int64_t)sp * stride);
                     if (p.y != nullptr && n < p.N) p.y[(int64_t)t * p.N + n] = bf16_bits_rn(s);
                     if (p.amax != nullptr) argmax_warp(p.amax + t, n < p.N ? argmax_key(s, (uint32_t)n) : 0ull);
                 }

@@ -574,6 +574,12 @@ __device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t *counter) {
     return old;
 }
 
+// Hint: bring the 128-byte line holding `a` into this SM's L1 (no register
+// is written; a later ld.global.ca of the line hits L1 if it is still there).
+__device__ __forceinline__ void prefetch_l1(const void *a) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+}
+
 // Acquire load of a split-K counter at GPU scope: a value showing that the
 // other CTAs of a tile have arrived also makes their partial sums visible.
 __device__ __forceinline__ uint32_t load_acquire_gpu(const uint32_t *counter) {
