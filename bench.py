@@ -690,6 +690,7 @@ def run_w12(args):
     if rank != 0:
         return
     csum = clocks.summary()
+    read_ceiling = read_ceiling_gbs()
     layers = wl.MODEL64_LAYERS if args.workload == "model64" else 1
     unit_steps = len(mats) if args.workload == "single" else layers
     value = job_weight_gbs(step.weights, world, ms_step)
@@ -712,7 +713,9 @@ def run_w12(args):
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "traffic": traffic,
                      "algorithmic_bytes": int(step.alg[dom]),
                      "step_frac": round(step.packed / (ms_step * 1e-3) / 1e9 / peak, 4),
-                     "launch_frac": lf},
+                     "launch_frac": lf,
+                     "read_ceiling_GBps": round(read_ceiling, 1),
+                     "frac_of_read_ceiling": round(achieved / read_ceiling, 4)},
         "cpu_baseline": cpu,
         "clocks": csum,
         "e2e": e2e,
@@ -734,6 +737,24 @@ def run_w12(args):
         },
     }
     emit(line, args)
+
+
+def read_ceiling_gbs(nbytes: int = 2 << 30, iters: int = 20) -> float:
+    """HBM read ceiling on this GPU: the library's read-stream kernel over a
+    buffer larger than L2 (read once per iteration, nothing written), GB/s."""
+    import torch
+    from lossless_bit_weight_encode_gb300 import w12
+    buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    buf.fill_(1)  # folds to 0 (an even count of equal words), never 0xFFFFFFFF
+    sink = torch.zeros(4, dtype=torch.int32, device="cuda")
+    sh = torch.cuda.current_stream().cuda_stream
+    run = lambda: w12.w12_read_stream_ptr(buf.data_ptr(), nbytes, sink.data_ptr(), 0xFFFFFFFF, sh)
+    for _ in range(3):
+        run()
+    ms = time_steps(run, iters)
+    w12.w12_check_status()
+    del buf
+    return nbytes / (ms * 1e-3) / 1e9
 
 
 def run_detail(args, mats, weights, step, bf16_ms):

@@ -347,6 +347,18 @@ int w12_q8_gemm_group(const uint16_t *x_dev, int count, const void *const *blobs
                       uint16_t *const *y_devs, int M, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Measurement helper with no counterpart on the pages: reads `bytes` (a
+ * multiple of 16) of device memory at buf_dev (16-byte aligned) once, with
+ * 16-byte streaming loads spread over every SM, and writes the 4-byte word at
+ * sink_dev only if the XOR of everything read equals `never` (pick a value
+ * the data cannot fold to, and the kernel writes nothing).  Timed over a
+ * buffer larger than L2, it gives the HBM read ceiling for the GEMM kernels,
+ * which read ~1.5 B per weight and write almost nothing.  Asynchronous on
+ * `stream`; INVALID_ARG / ALIGNMENT on bad pointers or sizes.
+ */
+int w12_read_stream(const void *buf_dev, size_t bytes, void *sink_dev, uint32_t never, void *stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's status word,
  * which kernels set when a bounded wait gives up (TIMEOUT) or the device
  * encoder finds its output buffer too short (BUFFER_TOO_SMALL) or too many

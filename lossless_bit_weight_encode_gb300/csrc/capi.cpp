@@ -507,6 +507,20 @@ int w12_q8_gemm_group(const uint16_t *x_dev, int count, const void *const *blobs
     });
 }
 
+int w12_read_stream(const void *buf_dev, size_t bytes, void *sink_dev, uint32_t never, void *stream) {
+    return guarded([&](std::string &err) {
+        if (!buf_dev || !sink_dev) {
+            err = "null pointer";
+            return (int)W12_ERR_INVALID_ARG;
+        }
+        if (!aligned(buf_dev, 16) || !aligned(sink_dev, 4) || bytes % 16 != 0) {
+            err = "buf_dev must be 16-byte aligned, bytes a multiple of 16, sink_dev 4-byte aligned";
+            return (int)W12_ERR_ALIGNMENT;
+        }
+        return w12::launch::read_stream(buf_dev, bytes, sink_dev, never, stream, &err);
+    });
+}
+
 int w12_check_status(void *stream) {
     return guarded([&](std::string &err) { return w12::launch::check_status(stream, &err); });
 }

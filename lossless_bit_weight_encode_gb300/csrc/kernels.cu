@@ -47,6 +47,28 @@ __global__ void w12_argmax_finalize_kernel(const unsigned long long *__restrict_
     val[m] = __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
 }
 
+// Reads n16 16-byte words once (eight loads in flight per thread, streaming
+// cache hint) and folds them into one word per thread, written only if it
+// equals `never`: the HBM read ceiling the GEMM kernels are measured against.
+__global__ void __launch_bounds__(512, 2) w12_read_stream_kernel(const uint4 *__restrict__ p, int64_t n16,
+                                                             uint32_t never, uint32_t *__restrict__ sink) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t acc = 0;
+    for (; i + 7 * stride < n16; i += 8 * stride) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcs(p + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+    }
+    for (; i < n16; i += stride) {
+        const uint4 v = __ldcs(p + i);
+        acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+    if (acc == never) sink[0] = acc;
+}
+
 // Waits on an mbarrier that nothing arrives on, with a short deadline, and
 // records the timeout: exercises the bounded-wait path without a fault.
 __global__ void w12_selftest_timeout_kernel(uint32_t *status, uint64_t timeout_ns) {
@@ -437,6 +459,21 @@ int plan_gemm(const w12_info &info, int M, GemmPlan *plan, std::string *err, boo
     const size_t partial_bytes = splits > 1 ? up256((size_t)splits * (size_t)M * (size_t)info.N_pad * 4) : 0;
     plan->ws_x = plan->ws_partials + partial_bytes;
     plan->ws_bytes = plan->ws_x + up256((size_t)M * (size_t)k8 * 2);
+    return W12_OK;
+}
+
+int read_stream(const void *buf_dev, size_t bytes, void *sink_dev, uint32_t never, void *stream, std::string *err) {
+    DeviceState *s = nullptr;
+    int rc = device_state(&s, err);
+    if (rc != W12_OK) return rc;
+    // two resident CTAs of 512 threads per SM (64 registers each), eight
+    // 16-byte loads in flight per thread: 128 KB per SM
+    const int64_t n16 = (int64_t)(bytes / 16);
+    const unsigned grid = (unsigned)(2 * s->sm_count);
+    dev::w12_read_stream_kernel<<<grid, 512, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(buf_dev), n16, never, static_cast<uint32_t *>(sink_dev));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "read-stream launch", err);
     return W12_OK;
 }
 

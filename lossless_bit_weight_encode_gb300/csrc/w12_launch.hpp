@@ -43,6 +43,8 @@ int q8_gemm_group(const uint16_t *x_dev, int count, const void *const *blobs, co
 
 int decode(const void *blob_dev, const w12_info &info, uint16_t *out_dev, void *stream, std::string *err);
 
+int read_stream(const void *buf_dev, size_t bytes, void *sink_dev, uint32_t never, void *stream, std::string *err);
+
 int gemm(const uint16_t *x_dev, const void *blob_dev, const w12_info &info, uint16_t *y_dev, int M,
          void *workspace, size_t ws_bytes, void *stream, std::string *err);
 

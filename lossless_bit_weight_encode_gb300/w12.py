@@ -28,7 +28,7 @@ EXPORTED = (
     "w12_gemm", "w12_gemm_group_workspace_size", "w12_gemm_group", "w12_gemm_group_launch_info", "w12_gemm_argmax_workspace_size", "w12_gemm_argmax", "w12_gemm_noalloc", "w12_encode_workspace_size", "w12_encoded_size_device", "w12_encode_device",
     "w12_q8_encoded_size", "w12_q8_encode_host", "w12_q8_blob_info", "w12_q8_gemm_workspace_size", "w12_q8_gemm",
     "w12_q8_gemm_group_workspace_size", "w12_q8_gemm_group_launch_info", "w12_q8_gemm_group",
-    "w12_check_status", "w12_selftest_timeout", "w12_set_option", "w12_get_option",
+    "w12_read_stream", "w12_check_status", "w12_selftest_timeout", "w12_set_option", "w12_get_option",
 )
 
 
@@ -111,6 +111,7 @@ def lib() -> ctypes.CDLL:
                                                 ctypes.POINTER(ctypes.c_int32)]
     L.w12_q8_gemm_group.argtypes = [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(w12_q8_info), ctypes.POINTER(vp),
                                     i32, vp, sz, vp]
+    L.w12_read_stream.argtypes = [vp, sz, vp, ctypes.c_uint32, vp]
     L.w12_check_status.argtypes = [vp]
     L.w12_selftest_timeout.argtypes = [ctypes.c_uint32, vp]
     L.w12_set_option.argtypes = [ctypes.c_char_p, i64]
@@ -378,6 +379,11 @@ def w12_q8_gemm_group(x_dev, blobs_dev, infos, ys_dev, M: int, workspace, stream
     _check(w12_q8_gemm_group_ptr(x_dev.data_ptr(), [b.data_ptr() for b in blobs_dev], infos,
                                  [y.data_ptr() for y in ys_dev], M, workspace.data_ptr(),
                                  workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+
+
+def w12_read_stream_ptr(buf_ptr: int, nbytes: int, sink_ptr: int, never: int, stream_handle: int | None) -> int:
+    """Raw-pointer form of w12_read_stream (the HBM read ceiling) that returns the status."""
+    return lib().w12_read_stream(buf_ptr, nbytes, sink_ptr, never, stream_handle)
 
 
 def w12_check_status(stream=None) -> None:

@@ -215,6 +215,11 @@ def test_gemm_argument_errors_before_any_device_work():
     assert w12.w12_q8_gemm_group_ptr(a, [a], [bad], [a], 1, a, 1 << 20, None) != 0
     out5 = (ctypes.c_int32 * 5)()
     assert lib.w12_q8_gemm_group_launch_info(0, None, 1, out5) == INVALID
+    # read-stream helper: null buffer or sink, misaligned buffer or size
+    assert w12.w12_read_stream_ptr(0, 16, a, 0, None) == INVALID
+    assert w12.w12_read_stream_ptr(a, 16, 0, 0, None) == INVALID
+    assert w12.w12_read_stream_ptr(a + 8, 16, a, 0, None) == ALIGN
+    assert w12.w12_read_stream_ptr(a, 24, a, 0, None) == ALIGN
     assert w12.w12_last_error() != ""
 
 
