@@ -374,13 +374,8 @@ __device__ __noinline__ void tcsm_decoder_finish(const GemmGroup &g, const Piece
 __device__ __forceinline__ void decode_chunk_to_tmem(const Table &T, const uint4 &s0, const uint4 &s1,
                                                      const uint4 &cd, bool has_escapes, const uint8_t *&run,
                                                      uint32_t taddr) {
-    uint32_t lo[8], hi[8], v[16];
-    decode_chunk(T, s0, s1, cd, has_escapes, run, lo, hi);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        v[i] = lo[i];
-        v[8 + i] = hi[i];
-    }
+    uint32_t v[16];
+    decode_chunk_patched(T, s0, s1, cd, has_escapes, run, v);
     tmem_st16(taddr, v);
 }
 

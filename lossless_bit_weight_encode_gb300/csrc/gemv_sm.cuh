@@ -269,6 +269,26 @@ __device__ __forceinline__ void decode_chunk(const Table &T, const uint4 &s0, co
     }
 }
 
+// The same chunk as 16 words of BF16 pairs, decoded as if it had no escapes,
+// with the escaped exponents patched in afterwards (patch_chunk_escapes): the
+// form the tcgen05 kernel uses, whose decode warps are bound by latency
+// rather than instruction count.
+__device__ __forceinline__ void decode_chunk_patched(const Table &T, const uint4 &s0, const uint4 &s1,
+                                                     const uint4 &cd, bool has_escapes, const uint8_t *&run,
+                                                     uint32_t (&w)[16]) {
+    uint32_t E[4], lo[8], hi[8];
+    decode_exponents_half(T, cd.x, cd.y, E);
+    assemble_half(s0, E, lo);
+    decode_exponents_half(T, cd.z, cd.w, E);
+    assemble_half(s1, E, hi);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        w[i] = lo[i];
+        w[8 + i] = hi[i];
+    }
+    if (has_escapes) run += patch_chunk_escapes(cd, run, w);
+}
+
 // Per piece: decode and accumulate its segments, then add the four chunk
 // groups of each row (j = 1..3 hand their sums to j = 0 through shared
 // memory) and write the whole tile's result when the CTA owns the tile, else
@@ -361,6 +381,9 @@ __device__ void gemv_sm_decode(const GemmGroup &g, const Piece *pieces, int npie
             if (vb && (esc_a | esc_b) == 0u) {
                 // common case: both chunks present, no escapes; one
                 // straight-line block of 32 independent lookup/assembly chains
+                // (decoding escapes into it and patching them afterwards, as
+                // the tcgen05 kernel does, measured slower here: the
+                // multiply-adds then wait on the patch)
                 uint32_t wa[16], wb[16];
                 decode_pair_plain(T, a0, a1, acd, b0, b1, bcd, wa, wb);
                 dot32_bf<MT>(wa, xs, acc);

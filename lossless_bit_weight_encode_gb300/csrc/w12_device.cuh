@@ -551,6 +551,39 @@ __device__ __forceinline__ uint32_t decode_exponents_chunk_esc(const Table &T, c
     return total;
 }
 
+// Escapes of one quarter-chunk, patched after a plain decode: the ordinary
+// lookup has given every escaped weight (code 15) a wrong exponent and the
+// right sign and mantissa (both come from the S byte), so only its exponent
+// field is replaced, from the escape run in row then column order: lane l's
+// bytes start after the escapes of lanes 0..l-1 (a ballot prefix), and within
+// the row they follow the columns.  w[i] holds the BF16 pair of columns 2i
+// (low half) and 2i + 1 (high half); code word k of cd holds columns 8k..8k+7,
+// one per nibble.  Returns the warp's escape count (to advance the run).
+// Only lanes that hold escapes enter the patch loop.
+__device__ __forceinline__ uint32_t patch_chunk_escapes(const uint4 &cd, const uint8_t *run, uint32_t (&w)[16]) {
+    const uint32_t f[4] = {escape_flags(cd.x), escape_flags(cd.y), escape_flags(cd.z), escape_flags(cd.w)};
+    const uint32_t cnt = __popc(f[0]) + __popc(f[1]) + __popc(f[2]) + __popc(f[3]);
+    uint32_t excl, total;
+    lane_prefix(cnt, excl, total);
+    if (cnt != 0u) {
+        const uint8_t *src = run + excl;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t fk = f[k];
+            while (fk != 0u) {
+                const uint32_t p = ((uint32_t)__ffs(fk) - 1u) >> 2;  // column 8k + p
+                fk &= fk - 1u;
+                const uint32_t sh = (p & 1u) ? 23u : 7u;             // exponent field of the high or low half
+                const uint32_t keep = ~(0xFFu << sh), e = (uint32_t)(*src++) << sh;
+                const uint32_t word = p >> 1;                       // w[4k + word]
+#pragma unroll
+                for (int i = 0; i < 4; ++i) w[4 * k + i] = word == (uint32_t)i ? (w[4 * k + i] & keep) | e : w[4 * k + i];
+            }
+        }
+    }
+    return total;
+}
+
 // Arrive on an mbarrier once for the whole warp (after ordering every lane's
 // earlier accesses), without a divergent branch.
 __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
