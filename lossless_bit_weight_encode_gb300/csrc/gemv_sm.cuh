@@ -378,14 +378,19 @@ __device__ void gemv_sm_decode(const GemmGroup &g, const Piece *pieces, int npie
             warp_arrive(b.wempty + slot);
 
             const uint32_t xs = xb0 + (uint32_t)(sslot * C::kXbBytes);
-            if (vb && (esc_a | esc_b) == 0u) {
-                // common case: both chunks present, no escapes; one
-                // straight-line block of 32 independent lookup/assembly chains
-                // (decoding escapes into it and patching them afterwards, as
-                // the tcgen05 kernel does, measured slower here: the
-                // multiply-adds then wait on the patch)
+            if (vb && ((esc_a | esc_b) == 0u || MT == 2)) {
+                // both chunks present, no escapes: one straight-line block of
+                // 32 independent lookup/assembly chains.  With two token rows
+                // escaped chunks take it too and have their exponents patched
+                // afterwards (as in the tcgen05 kernel); with one, that
+                // measured slower (the multiply-adds wait on the patch) and
+                // the per-lane table path below serves them
                 uint32_t wa[16], wb[16];
                 decode_pair_plain(T, a0, a1, acd, b0, b1, bcd, wa, wb);
+                if constexpr (MT == 2) {
+                    if (esc_a) run += patch_chunk_escapes(acd, run, wa);
+                    if (esc_b) run += patch_chunk_escapes(bcd, run, wb);
+                }
                 dot32_bf<MT>(wa, xs, acc);
                 dot32_bf<MT>(wb, xs + (uint32_t)(kChunkK * 2), acc);
             } else {
